@@ -1,0 +1,429 @@
+"""Pins of the float64 oracle against facts independent of its own code.
+
+Every check here compares the oracle with something it does not share code
+with: torch's float8/bfloat16 casts, torch's float64 scaled-dot-product
+attention and logsumexp, hand-worked fixtures under tests/golden/, a
+simulation of a paged KV cache filled one token at a time, closed forms and
+invariants the pages state.  Runs on CPU.
+"""
+import json
+import math
+import os
+import struct
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_mla_decode_dcp_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+SM_SCALE = 1.0 / math.sqrt(192.0)
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ----------------------------------------------------------------- fp8, bf16
+def test_e4m3_table_matches_torch_all_codes():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    nan_ref, nan_got = np.isnan(ref), np.isnan(got)
+    assert np.array_equal(nan_ref, nan_got)
+    assert nan_got.sum() == 2  # 0x7F and 0xFF only
+    assert np.array_equal(ref[~nan_ref], got[~nan_got])
+    # signed zeros decode with their sign
+    assert np.array_equal(np.signbit(ref[~nan_ref]), np.signbit(got[~nan_got]))
+
+
+def test_e4m3_spec_values():
+    g = _golden("e4m3_spec_values.json")
+    for code_hex, val in g["values"].items():
+        got = oracle.e4m3_to_f64(np.array([int(code_hex, 16)], dtype=np.uint8))[0]
+        if val == "nan":
+            assert math.isnan(got), code_hex
+        else:
+            assert got == val and math.copysign(1, got) == math.copysign(1, val), code_hex
+
+
+def test_bf16_widen_matches_torch():
+    rng = np.random.default_rng(1)
+    bits = np.concatenate([
+        rng.integers(0, 1 << 16, size=20000, dtype=np.uint64).astype(np.uint16),
+        np.array([0x0000, 0x8000, 0x0001, 0x8001, 0x007F, 0x0080, 0x3F80,
+                  0xBF80, 0x7F7F, 0xFF7F, 0x7F80, 0xFF80], dtype=np.uint16)])
+    ref = (torch.from_numpy(bits.astype(np.int32)).to(torch.int16)
+           .view(torch.bfloat16).to(torch.float64).numpy())
+    got = oracle.bf16_bits_to_f64(bits)
+    same = (ref == got) | (np.isnan(ref) & np.isnan(got))
+    assert same.all()
+
+
+# ----------------------------------------------------------------- row parse
+def _pack_row(codes_u8, scales_f32, rope_bf16_bits):
+    """Pack one row with struct (independent of the oracle's parser)."""
+    b = bytes(codes_u8.tolist())
+    b += struct.pack("<4f", *[float(s) for s in scales_f32])
+    b += struct.pack("<64H", *[int(x) for x in rope_bf16_bits])
+    assert len(b) == 656
+    return np.frombuffer(b, dtype=np.uint8)
+
+
+def test_parse_rows_roundtrip_known_values():
+    rng = np.random.default_rng(2)
+    vals = torch.from_numpy(rng.uniform(-448, 448, size=512)).to(torch.float8_e4m3fn)
+    codes = vals.view(torch.uint8).numpy()
+    scales = np.array([0.5, 3.0e-3, 7.25, 1.0], dtype=np.float32)
+    rope = torch.from_numpy(rng.normal(size=64)).to(torch.bfloat16)
+    rope_bits = rope.view(torch.int16).numpy().astype(np.uint16)
+    row = _pack_row(codes, scales, rope_bits)
+    nope, rope_got = oracle.parse_rows(row[None])
+    expect_nope = vals.to(torch.float64).numpy() * np.repeat(
+        scales.astype(np.float64), 128)
+    assert np.array_equal(nope[0], expect_nope)
+    assert np.array_equal(rope_got[0], rope.to(torch.float64).numpy())
+
+
+def test_parse_rows_generator_rows_dequantise_close_to_source():
+    """Rows made by the generator decode to within e4m3 precision of N(0,1)
+    samples: |nope| <= absmax of its group, codes reach +-448 in each group."""
+    gen = torch.Generator().manual_seed(3)
+    rows = inputs.random_rows(64, gen, "cpu").numpy()
+    nope, rope = oracle.parse_rows(rows)
+    scales = rows[:, 512:528].copy().view("<f4").astype(np.float64)
+    for g in range(4):
+        grp = nope[:, 128 * g:128 * (g + 1)]
+        # the group's largest magnitude is exactly 448 * scale (absmax / 448 scale)
+        assert np.allclose(np.abs(grp).max(axis=1), 448.0 * scales[:, g], rtol=0, atol=0)
+    assert np.all(np.isfinite(rope)) and 0.5 < rope.std() < 2.0
+
+
+# ---------------------------------------------------------- filter + convert
+def test_index_worked_examples():
+    g = _golden("index_worked_example.json")
+    for case in g["cases"]:
+        slots, count = oracle.dcp_filter_convert_index(
+            np.array(case["req_id"]), np.array(case["block_table"]),
+            np.array(case["topk"]), case["D"], case["rank"], case["block_size"])
+        assert slots.tolist() == case["local_slots"], case["note"]
+        assert count.tolist() == case["valid_count"], case["note"]
+
+
+def _simulate_paged_cache(ctx, D, bs, rng):
+    """Fill a D-rank paged KV cache one token at a time, the way a cache
+    manager appends: each rank keeps a running row counter per request and
+    takes a fresh random free block when the current one is full.  Returns
+    per-rank block tables and where[(r, t)] = (rank, slot)."""
+    R = len(ctx)
+    tables = [[[] for _ in range(R)] for _ in range(D)]
+    free = [list(rng.permutation(4 * sum(ctx) // bs + 8 * R + 8)) for _ in range(D)]
+    counters = np.zeros((D, R), dtype=np.int64)
+    where = {}
+    for r in range(R):
+        for t in range(ctx[r]):
+            d = t % D  # interleave 1: position t is owned by rank t mod D
+            c = counters[d, r]
+            if c % bs == 0:
+                tables[d][r].append(int(free[d].pop()))
+            where[(r, t)] = (d, tables[d][r][-1] * bs + c % bs)
+            counters[d, r] += 1
+    bts = []
+    for d in range(D):
+        W = max(1, max(len(x) for x in tables[d]))
+        bt = np.full((R, W + 1), -1, dtype=np.int32)
+        for r in range(R):
+            bt[r, :len(tables[d][r])] = tables[d][r]
+        bts.append(bt)
+    return bts, where, counters
+
+
+@pytest.mark.parametrize("D,bs,ctx", [
+    (1, 4, [13, 5]), (2, 4, [13, 1, 9]), (3, 2, [7, 2, 11]),
+    (4, 16, [200, 3, 1, 64]), (8, 4, [50, 7])])
+def test_index_matches_append_simulation(D, bs, ctx):
+    rng = np.random.default_rng(D * 100 + bs)
+    bts, where, counters = _simulate_paged_cache(ctx, D, bs, rng)
+    R = len(ctx)
+    rows, req = [], []
+    for r in range(R):
+        for _ in range(3):
+            K = 12
+            row = rng.integers(-2, ctx[r], size=K)  # some negative ids too
+            rows.append(row)
+            req.append(r)
+    topk = np.array(rows, dtype=np.int32)
+    req_id = np.array(req, dtype=np.int32)
+    owned = np.zeros(topk.shape, dtype=np.int64)
+    for d in range(D):
+        slots, count = oracle.dcp_filter_convert_index(req_id, bts[d], topk, D, d, bs)
+        for i in range(topk.shape[0]):
+            for j in range(topk.shape[1]):
+                t = int(topk[i, j])
+                if t >= 0 and where[(int(req_id[i]), t)][0] == d:
+                    assert slots[i, j] == where[(int(req_id[i]), t)][1]
+                    owned[i, j] += 1
+                else:
+                    assert slots[i, j] == -1
+        assert np.array_equal(count, (slots >= 0).sum(axis=1))
+    # partition: every non-negative id is owned by exactly one rank
+    assert np.array_equal(owned, (topk >= 0).astype(np.int64))
+    # per-rank counts of a request equal the local sequence length helper
+    for d in range(D):
+        for r in range(R):
+            assert counters[d, r] == oracle.dcp_local_seq_len(ctx[r], D, d)
+
+
+def test_index_all_positions_counts_equal_local_seq_lens():
+    rng = np.random.default_rng(5)
+    ctx = [37, 200]
+    for D in (1, 2, 4):
+        bts, where, _ = _simulate_paged_cache(ctx, D, 16, rng)
+        topk = np.full((2, 256), -1, dtype=np.int32)
+        for r in range(2):
+            topk[r, :ctx[r]] = rng.permutation(ctx[r])
+        for d in range(D):
+            _, count = oracle.dcp_filter_convert_index(
+                np.arange(2), bts[d], topk, D, d, 16)
+            assert count.tolist() == [oracle.dcp_local_seq_len(c, D, d) for c in ctx]
+
+
+def test_local_seq_len_closed_form():
+    # ceil((ctx - rank) / D) for ctx > rank, else 0
+    for ctx in range(0, 40):
+        for D in (1, 2, 3, 4, 8):
+            for rank in range(D):
+                want = max(0, -(-(ctx - rank) // D))
+                assert oracle.dcp_local_seq_len(ctx, D, rank) == want
+
+
+# ----------------------------------------------------------------- attention
+def _dense_case(n, H, seed):
+    gen = torch.Generator().manual_seed(seed)
+    rows = inputs.random_rows(n, gen, "cpu")
+    q = torch.randn((H, 576), generator=gen).to(torch.bfloat16)
+    return rows, q
+
+
+def _torch_dequant(rows: torch.Tensor):
+    """K [n, 576] and V [n, 512] in float64 through torch's own casts."""
+    codes = rows[:, :512].contiguous().view(torch.float8_e4m3fn).to(torch.float64)
+    scales = rows[:, 512:528].contiguous().view(torch.float32).to(torch.float64)
+    nope = codes * scales.repeat_interleave(128, dim=1)
+    rope = rows[:, 528:].contiguous().view(torch.bfloat16).to(torch.float64)
+    return torch.cat([nope, rope], dim=1), nope
+
+
+def _q_bits(q_bf16: torch.Tensor) -> np.ndarray:
+    return q_bf16.contiguous().view(torch.int16).numpy().astype(np.uint16)
+
+
+@pytest.mark.parametrize("n,H", [(1, 4), (7, 16), (64, 8), (300, 3)])
+def test_attention_dense_matches_torch_sdpa(n, H):
+    rows, q = _dense_case(n, H, seed=n)
+    k, v = _torch_dequant(rows)
+    qd = q.to(torch.float64)
+    ref_out = torch.nn.functional.scaled_dot_product_attention(
+        qd.unsqueeze(1), k.unsqueeze(0).expand(H, n, 576),
+        v.unsqueeze(0).expand(H, n, 512), scale=SM_SCALE).squeeze(1)
+    ref_lse = torch.logsumexp(SM_SCALE * (qd @ k.T), dim=1)
+    # top-k = every position, in a random order, with -1s sprinkled in
+    rng = np.random.default_rng(n)
+    slots = np.concatenate([rng.permutation(n), -np.ones(5, dtype=np.int64)])
+    slots = rng.permutation(slots)[None]
+    out, lse = oracle.sparse_mla_decode(_q_bits(q)[None], rows.numpy(), slots, SM_SCALE)
+    assert np.allclose(out[0], ref_out.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.allclose(lse[0], ref_lse.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_attention_q_zero_closed_form():
+    rows, _ = _dense_case(37, 2, seed=9)
+    _, v = _torch_dequant(rows)
+    q = torch.zeros((2, 576), dtype=torch.bfloat16)
+    out, lse = oracle.sparse_mla_decode(_q_bits(q)[None], rows.numpy(),
+                                        np.arange(37)[None], SM_SCALE)
+    assert np.allclose(lse[0], math.log(37), rtol=0, atol=1e-14)
+    assert np.allclose(out[0], v.mean(dim=0).numpy()[None], rtol=1e-13, atol=1e-14)
+
+
+def test_attention_single_slot_closed_form():
+    rows, q = _dense_case(5, 6, seed=10)
+    k, v = _torch_dequant(rows)
+    slots = np.array([[-1, 3, -1, -1]])
+    out, lse = oracle.sparse_mla_decode(_q_bits(q)[None], rows.numpy(), slots, SM_SCALE)
+    s = SM_SCALE * (q.to(torch.float64) @ k[3])
+    assert np.allclose(lse[0], s.numpy(), rtol=1e-15, atol=1e-15)
+    assert np.array_equal(out[0], np.broadcast_to(v[3].numpy(), (6, 512)))
+
+
+def test_attention_order_invariance():
+    rows, q = _dense_case(100, 4, seed=11)
+    rng = np.random.default_rng(11)
+    base = np.concatenate([rng.choice(100, 40, replace=False), -np.ones(8, np.int64)])
+    a = oracle.sparse_mla_decode(_q_bits(q)[None], rows.numpy(), base[None], SM_SCALE)
+    b = oracle.sparse_mla_decode(_q_bits(q)[None], rows.numpy(),
+                                 rng.permutation(base)[None], SM_SCALE)
+    assert np.allclose(a[0], b[0], rtol=0, atol=1e-12)
+    assert np.allclose(a[1], b[1], rtol=0, atol=1e-12)
+
+
+def test_attention_duplicate_slots_count_twice():
+    """Reading taken: a slot listed twice is attended twice (the multiset)."""
+    rows, q = _dense_case(3, 2, seed=12)
+    k, v = _torch_dequant(rows)
+    out, lse = oracle.sparse_mla_decode(_q_bits(q)[None], rows.numpy(),
+                                        np.array([[0, 0, 2]]), SM_SCALE)
+    kk = torch.stack([k[0], k[0], k[2]])
+    vv = torch.stack([v[0], v[0], v[2]])
+    s = SM_SCALE * (q.to(torch.float64) @ kk.T)
+    assert np.allclose(lse[0], torch.logsumexp(s, 1).numpy(), atol=1e-13)
+    assert np.allclose(out[0], (torch.softmax(s, 1) @ vv).numpy(), atol=1e-13)
+
+
+def test_empty_row_case_from_pages():
+    g = _golden("empty_row_case.json")
+    T, H = g["num_tokens"], g["num_heads"]
+    rows, _ = _dense_case(4, H, seed=13)
+    q = torch.randn((T, H, 576), generator=torch.Generator().manual_seed(13))
+    out, lse = oracle.sparse_mla_decode(_q_bits(q.to(torch.bfloat16)), rows.numpy(),
+                                        np.array(g["local_indices"]), SM_SCALE)
+    for r in g["empty_rows"]:
+        assert np.array_equal(out[r], np.zeros_like(out[r]))
+        assert np.all(np.isneginf(lse[r]))
+    for r in g["nonempty_rows"]:
+        assert np.all(np.isfinite(lse[r]))
+    assert not np.isnan(out).any() and not np.isnan(lse).any()
+
+
+# --------------------------------------------------------------------- merge
+def _unsharded(wl, T_rows=None):
+    """Attention over the union of every shard's rows for each query row:
+    gather each valid global id's row from the shard the conversion puts it
+    on, then one softmax over all of them."""
+    pools = [s.pool.numpy() for s in wl.shards]
+    q = _q_bits(wl.q)
+    per_shard = [oracle.dcp_filter_convert_index(wl.req_id, s.block_table, wl.topk,
+                                                 wl.D, d, wl.spec.block_size)[0]
+                 for d, s in enumerate(wl.shards)]
+    outs, lses = [], []
+    for i in range(wl.T):
+        rows = np.concatenate([pools[d][per_shard[d][i][per_shard[d][i] >= 0]]
+                               for d in range(wl.D)])
+        o, l = oracle.sparse_mla_decode_rows(oracle.bf16_bits_to_f64(q[i]), rows,
+                                             wl.spec.sm_scale)
+        outs.append(o)
+        lses.append(l)
+    return np.stack(outs), np.stack(lses)
+
+
+def _sharded(wl):
+    q = _q_bits(wl.q)
+    outs, lses = [], []
+    for d, s in enumerate(wl.shards):
+        slots, _ = oracle.dcp_filter_convert_index(wl.req_id, s.block_table, wl.topk,
+                                                   wl.D, d, wl.spec.block_size)
+        o, l = oracle.sparse_mla_decode(q, s.pool.numpy(), slots, wl.spec.sm_scale)
+        outs.append(o)
+        lses.append(l)
+    return outs, lses
+
+
+def test_merge_of_shards_equals_unsharded_tiny():
+    wl = inputs.make_workload("tiny", seed=0)
+    outs, lses = _sharded(wl)
+    out, lse = oracle.lse_merge(outs, lses)
+    u_out, u_lse = _unsharded(wl)
+    assert np.allclose(out, u_out, rtol=0, atol=1e-12)
+    assert np.allclose(lse, u_lse, rtol=0, atol=1e-12)
+    # every token reached the gathered rows through exactly one shard
+    assert np.isfinite(lse).all()
+
+
+def test_merge_of_shards_equals_unsharded_with_empty_shards():
+    spec = inputs.WorkloadSpec(
+        name="t", num_reqs=4, tokens_per_req=1, heads=4, topk=16, dcp=4,
+        block_size=4, ctx_kind="fixed", ctx_fixed=(1, 2, 3, 40))
+    wl = inputs.make_workload(spec, seed=4)
+    outs, lses = _sharded(wl)
+    # the ctx-1 request has nothing on ranks 1..3, ctx-2 nothing on 2..3
+    assert np.isneginf(lses[1][0]).all() and np.isneginf(lses[3][1]).all()
+    out, lse = oracle.lse_merge(outs, lses)
+    u_out, u_lse = _unsharded(wl)
+    assert np.allclose(out, u_out, rtol=0, atol=1e-12)
+    assert np.allclose(lse, u_lse, rtol=0, atol=1e-12)
+
+
+def test_merge_matches_torch_logsumexp():
+    rng = np.random.default_rng(6)
+    lses = [rng.normal(size=(3, 5)) * 4 for _ in range(4)]
+    outs = [rng.normal(size=(3, 5, 512)) for _ in range(4)]
+    out, lse = oracle.lse_merge(outs, lses)
+    L = torch.from_numpy(np.stack(lses))
+    ref_lse = torch.logsumexp(L, dim=0)
+    w = torch.softmax(L, dim=0)
+    ref_out = (w.unsqueeze(-1) * torch.from_numpy(np.stack(outs))).sum(0)
+    assert np.allclose(lse, ref_lse.numpy(), atol=1e-13)
+    assert np.allclose(out, ref_out.numpy(), atol=1e-13)
+
+
+def test_merge_identity_changes_nothing_and_no_nan():
+    rng = np.random.default_rng(7)
+    o = rng.normal(size=(2, 3, 512))
+    l = rng.normal(size=(2, 3))
+    out, lse = oracle.lse_merge([o, np.zeros_like(o)], [l, np.full_like(l, -np.inf)])
+    assert np.array_equal(out, o) and np.array_equal(lse, l)
+    out, lse = oracle.lse_merge([np.zeros_like(o), o], [np.full_like(l, -np.inf), l])
+    assert np.array_equal(out, o) and np.array_equal(lse, l)
+
+
+def test_merge_all_empty_is_identity():
+    z = np.zeros((2, 3, 512))
+    ninf = np.full((2, 3), -np.inf)
+    out, lse = oracle.lse_merge([z, z, z], [ninf, ninf, ninf])
+    assert np.array_equal(out, z) and np.isneginf(lse).all()
+    assert not np.isnan(out).any()
+
+
+# --------------------------------------------------------------- spec decode
+def test_spec_decode_rows_equal_per_token_results():
+    spec = inputs.WorkloadSpec(
+        name="mtp_small", num_reqs=3, tokens_per_req=2, heads=4, topk=32, dcp=2,
+        block_size=8, ctx_kind="uniform", ctx_lo=20, ctx_hi=90)
+    wl = inputs.make_workload(spec, seed=8)
+    q = _q_bits(wl.q)
+    for d, s in enumerate(wl.shards):
+        slots, _ = oracle.dcp_filter_convert_index(wl.req_id, s.block_table, wl.topk,
+                                                   wl.D, d, spec.block_size)
+        out, lse = oracle.sparse_mla_decode(q, s.pool.numpy(), slots, spec.sm_scale)
+        assert lse.shape == (6, 4)
+        for b in range(3):
+            for t in range(2):
+                o1, l1 = oracle.sparse_mla_decode(q[b * 2 + t][None], s.pool.numpy(),
+                                                  slots[b * 2 + t][None], spec.sm_scale)
+                assert np.array_equal(lse[b * 2 + t], l1[0])
+                assert np.array_equal(out[b * 2 + t], o1[0])
+    # causality comes only from the indices: no id exceeds its own position
+    for b in range(3):
+        for t in range(2):
+            pos = wl.ctx[b] - 2 + t
+            assert wl.topk[b * 2 + t].max() <= pos
+
+
+# ------------------------------------------------------- generator structure
+def test_generator_structure_tiny():
+    wl = inputs.make_workload("tiny", seed=0)
+    assert wl.topk.shape == (2, 64) and wl.q.shape == (2, 16, 576)
+    # ctx 37 row: 37 valid + 27 pad, then 6 random -1s (may overlap pads)
+    for i, c in enumerate(wl.ctx):
+        row = wl.topk[i]
+        valid = row[row >= 0]
+        assert len(set(valid.tolist())) == len(valid)
+        assert valid.max() < c
+        assert min(64, c) - 6 <= len(valid) <= min(64, c)
+    for d, s in enumerate(wl.shards):
+        assert s.live_rows == sum(oracle.dcp_local_seq_len(c, 2, d) for c in wl.ctx)
+        poison = (s.pool.numpy() == 0xFF).all(axis=1)
+        assert (~poison).sum() == s.live_rows
