@@ -1,0 +1,379 @@
+"""Benchmark: sparse-MLA decode query-tokens/s under DCP on GB300.
+
+One step = the whole hot path over one decode batch of the DCP=4 long-context
+workload (64 requests x 1 query token, H=128 gathered heads, top-k 2048, four
+simulated shards): per shard filter+convert and sparse MLA decode, then the
+LSE merge of the four partials.  Inputs are resident in HBM when the timed
+region starts; L2 is flushed (a 256 MiB write) before every timed step, outside
+the step's CUDA events.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the float64 CPU
+oracle instead (the reference arm of this build), on the same workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-MLA decode query-tokens/s and % roofline (H=128, topk=2048, DCP=4)"
+UNIT = "query-tokens/s"
+DEFAULT_WORKLOAD = "dcp4_long"
+FLUSH_BYTES = 256 << 20
+QK_DIM, V_DIM, ROW_BYTES = 576, 512, 656
+DECODE_SOURCES = ["sparse_mla_decode_dcp_gb300/csrc/smla_decode.cu"]  # hashed for traffic validity
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-sample-tokens", type=int, default=64)
+    return p.parse_args(argv)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
+                "bf16_tflops_sustained": float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------ helpers
+def algorithmic_units(step):
+    """Valid (non -1) slots per shard: the units the decode roofline counts."""
+    import torch
+    step.run()
+    torch.cuda.synchronize()
+    return [int(v.sum().item()) for v in step.valid_count]
+
+
+def profile_traffic(workload: str):
+    """DRAM bytes per decode launch from a committed ncu summary, if that
+    summary was taken on the decode kernel source as it is now."""
+    path = os.path.join(ROOT, "profiles", f"sparse_mla_decode_{workload}.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        prof = json.load(f)
+    h = hashlib.sha256()
+    for src in DECODE_SOURCES:
+        p = os.path.join(ROOT, src)
+        if not os.path.exists(p):
+            return None
+        with open(p, "rb") as g:
+            h.update(g.read())
+    if prof.get("source_sha256") != h.hexdigest():
+        return None
+    return prof.get("dram_bytes_per_launch")
+
+
+def cpu_baseline(wl, sample_tokens: int):
+    """The float64 oracle as it stands, timed on this host on a bounded sample
+    of the same workload: the first `sample_tokens` query rows, every shard's
+    convert + decode, then the merge."""
+    import oracle
+    import torch
+    n = min(sample_tokens, wl.T)
+    q_bits = wl.q[:n].detach().cpu().contiguous().view(torch.int16).numpy().astype(np.uint16)
+    pools = [s.pool.cpu().numpy() for s in wl.shards]
+    t0 = time.perf_counter()
+    outs, lses = [], []
+    for d, s in enumerate(wl.shards):
+        sl, _ = oracle.dcp_filter_convert_index(wl.req_id[:n], s.block_table, wl.topk[:n],
+                                                wl.D, d, wl.spec.block_size)
+        o, l = oracle.sparse_mla_decode(q_bits, pools[d], sl, wl.spec.sm_scale)
+        outs.append(o)
+        lses.append(l)
+    oracle.lse_merge(outs, lses)
+    dt = time.perf_counter() - t0
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.environ.get("OPENBLAS_NUM_THREADS",
+                                                                  os.cpu_count() or 1)))
+    return {"value": n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"first {n} of {wl.T} query rows of {wl.spec.name}, all {wl.D} shards "
+                      f"(convert + decode) + merge, float64 numpy; {dt:.2f} s"}
+
+
+# ------------------------------------------------------------ GPU arm
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    from sparse_mla_decode_dcp_gb300 import capi, inputs
+    from sparse_mla_decode_dcp_gb300.pipeline import DcpDecodeStep
+
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    capi.load()
+
+    wl = inputs.make_workload(args.workload, seed=args.seed + rank, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    step = DcpDecodeStep(wl, device=dev)
+    units = algorithmic_units(step)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    T, H, K, D = wl.T, wl.H, wl.K, wl.D
+
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1)
+        step.run()
+    torch.cuda.synchronize()
+
+    # Per-kernel pass: CUDA events around every decode launch (on the
+    # launching stream), used only for the roofline of the dominant kernel.
+    n_kern = max(10, min(args.steps, 50))
+    dec_ms = []
+    for _ in range(n_kern):
+        flush.fill_(1)
+        evs = []
+        for d in range(D):
+            step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            capi.dcp_filter_convert_index(
+                step.req_id, step.block_tables[d], step.topk, D, d, wl.spec.block_size,
+                bt_width=step.bt_widths[d], local_slots=step.local_slots[d],
+                valid_count=step.valid_count[d])
+            step_ev[0].record(stream)
+            capi.sparse_mla_decode(step.q, step.pools[d], step.local_slots[d], wl.spec.sm_scale,
+                                   out=step.part_out[d], lse=step.part_lse[d],
+                                   workspace=step.workspace)
+            step_ev[1].record(stream)
+            evs.append(step_ev)
+        capi.dcp_lse_merge(step.part_out, step.part_lse, out=step.out, lse=step.lse)
+        torch.cuda.synchronize()
+        dec_ms.append([a.elapsed_time(b) for a, b in evs])
+    dec_ms = np.array(dec_ms)  # [iters, D]
+
+    # Timed region: exactly `steps` steps, each bracketed by its own events,
+    # L2 flushed before each step outside the events.
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.25)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(1)
+        starts[i].record(stream)
+        step.run()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = float(sum(step_ms))
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * T * args.steps / (total_ms / 1e3)
+
+    # End to end through the public API with host buffers: every step copies
+    # q and the top-k ids from pinned host memory and reads out + lse back.
+    q_host = wl.q.detach().cpu().pin_memory()
+    topk_host = torch.from_numpy(wl.topk).pin_memory()
+    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    lse_host = torch.empty(step.lse.shape, dtype=step.lse.dtype).pin_memory()
+    h2d = q_host.numel() * q_host.element_size() + topk_host.numel() * 4
+    d2h = out_host.numel() * out_host.element_size() + lse_host.numel() * 4
+    e2e_steps = max(3, min(args.steps, 100))
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    for i in range(e2e_steps):
+        flush.fill_(1)
+        e_s[i].record(stream)
+        step.q.copy_(q_host, non_blocking=True)
+        step.topk.copy_(topk_host, non_blocking=True)
+        step.run()
+        out_host.copy_(step.out, non_blocking=True)
+        lse_host.copy_(step.lse, non_blocking=True)
+        e_e[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e_s, e_e)) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    peaks = load_peaks()
+    flop_per_key = 2.0 * H * (QK_DIM + V_DIM)
+    total_keys = sum(units)
+    dec_launch_ms = float(dec_ms.mean())
+    flops_per_launch = flop_per_key * total_keys / D
+    bytes_per_launch = ROW_BYTES * total_keys / D
+    ai = flop_per_key / ROW_BYTES
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if ai >= ridge:
+        roof = {"bound": "tensor", "achieved": flops_per_launch / (dec_launch_ms * 1e-3) / 1e12,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": bytes_per_launch / (dec_launch_ms * 1e-3) / 1e9,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = profile_traffic(args.workload)
+    roof.update({
+        "kernel": "smla_sparse_mla_decode",
+        "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json burst; fp16 MMA nominal = bf16)",
+        "launch_us": dec_launch_ms * 1e3,
+        "launches_per_step": D,
+        "algorithmic_flops_per_launch": flops_per_launch,
+        "algorithmic_bytes_per_launch": bytes_per_launch,
+        "valid_slots_per_shard": units,
+        "roofline_us_per_step": max(flop_per_key * total_keys / (peaks["bf16_tflops"] * 1e12),
+                                    ROW_BYTES * total_keys / (peaks["hbm_gbs"] * 1e9)) * 1e6,
+    })
+    roof["frac_of_step_decode_time"] = roof["roofline_us_per_step"] / (dec_ms.sum(axis=1).mean() * 1e3)
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "T": T, "H": H, "K": K, "D": D,
+                   "block_size": wl.spec.block_size, "requests": wl.spec.num_reqs,
+                   "cached_tokens": int(sum(int(c) for c in wl.ctx)),
+                   "l2": "flushed before every step (256 MiB write, outside the events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU, D shards simulated"},
+        "roofline": roof,
+        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * step.launches_per_step,
+        "clocks": clocks,
+        "wall_s_timed": wall,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wl, args.cpu_sample_tokens)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+# ------------------------------------------------------------ reference arm
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import torch
+
+    from sparse_mla_decode_dcp_gb300 import inputs
+    wl = inputs.make_workload(args.workload, seed=args.seed, device="cpu")
+    n = min(args.cpu_sample_tokens, wl.T)
+    for _ in range(args.warmup):
+        cpu_baseline(wl, max(1, n // 4))
+    times = []
+    for _ in range(args.steps):
+        b = cpu_baseline(wl, n)
+        times.append(n / b["value"])
+    value = n * len(times) / sum(times)
+    b["value"] = value
+    result = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "T": wl.T, "H": wl.H, "K": wl.K, "D": wl.D,
+                   "sample_tokens_per_step": n},
+        "cpu_baseline": b,
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(result), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,190 @@
+/*
+ * smla.h -- C ABI of the GB300 sparse MLA decode library under
+ * decode-context-parallel (DCP).
+ *
+ * The hot path has three steps, one call each:
+ *
+ *   1. smla_dcp_filter_convert_index  global top-k ids -> this rank's slots
+ *   2. smla_sparse_mla_decode         attention over the packed fp8 cache,
+ *                                     returning out and the softmax LSE
+ *   3. smla_dcp_lse_merge             LSE-weighted merge of D partials
+ *
+ * Sources (page title, then section):
+ *   [P1] "[eldritch] attention: support DCP in SM120 FlashInfer sparse MLA"
+ *   [P2] "[Bugfix][Attention] Stabilize sparse-MLA DCP for GLM PCP evals"
+ *   [P3] "FlashMLA sparse fp8 path + DCP + MTP" (vLLM PR #46514 summary)
+ *
+ * Conventions shared by every call:
+ *   - Pointers marked "device" point to memory of the current CUDA device;
+ *     the caller allocates and owns all of it.  The library never allocates,
+ *     frees or synchronises, and keeps no pointer after a call returns.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*,
+ *     NULL = legacy default stream) and takes every scalar by value, so no
+ *     call issues a host->device copy or a host sync [P2 "DCP decode rank
+ *     scalar"].
+ *   - Arguments are checked on the host before any launch; a failing check
+ *     returns a status and launches nothing.  A failed launch returns
+ *     SMLA_ERR_CUDA.  No C++ exception crosses this boundary.
+ *   - T = 0 is a no-op that returns SMLA_OK.
+ *   - Inputs the host cannot check (an id that runs past its block table, a
+ *     slot past the pool) are caught in the kernels: the offending entry is
+ *     treated as -1 and a bit is set in the device error word, readable with
+ *     smla_get_device_error.  No kernel traps.
+ *   - Index tensors are int32, row-major and contiguous.
+ */
+#ifndef SMLA_H_
+#define SMLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int smla_status;
+
+enum {
+  SMLA_OK = 0,
+  SMLA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned buffer   */
+  SMLA_ERR_UNSUPPORTED = 2, /* valid but outside the supported envelope    */
+  SMLA_ERR_WORKSPACE = 3,   /* workspace missing, too small or misaligned  */
+  SMLA_ERR_CUDA = 4         /* a CUDA runtime call or launch failed        */
+};
+
+/* Bits of the device error word. */
+enum {
+  SMLA_DEVERR_BLOCK_TABLE = 1u, /* id past the block table / unallocated block */
+  SMLA_DEVERR_REQ_ID = 2u,      /* req_id_per_token outside [0, num_reqs)      */
+  SMLA_DEVERR_SLOT_RANGE = 4u,  /* local slot >= num_slots                     */
+  SMLA_DEVERR_TIMEOUT = 8u      /* a bounded wait inside a kernel gave up      */
+};
+
+/* Largest gathered head count the decode kernel takes [P3 implementation
+ * breakdown step 4: heads pad to the 64/128 kernel envelope]. */
+#define SMLA_MAX_HEADS 128
+/* Largest number of partials smla_dcp_lse_merge combines in one call. */
+#define SMLA_MAX_DCP 16
+/* Packed fp8_ds_mla row: 512 e4m3 codes | 4 fp32 scales | 64 bf16 rope. */
+#define SMLA_ROW_BYTES 656
+#define SMLA_QK_DIM 576
+#define SMLA_V_DIM 512
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* smla_status_string(smla_status status);
+
+/* Reads the device error word of the current device into *flags (a host
+ * pointer) as an OR of SMLA_DEVERR_* bits; clears it when `clear` != 0.
+ * This call synchronises with the device (it is a diagnostic, not part of
+ * the hot path). */
+smla_status smla_get_device_error(uint32_t* flags, int clear);
+
+/*
+ * Step 1 -- DCP filter + convert [P3 implementation breakdown step 2 and
+ * the _forward_fp8_kv_mixed_batch snippet; P1 Summary].
+ *
+ * For row i (request r = req_id_per_token[i]) and entry j, with t =
+ * topk_global[i*K + j]:
+ *   t < 0 or t mod D != rank          -> local_slots[i*K + j] = -1
+ *   otherwise lp = t div D (interleave 1: rank-local position),
+ *             local_slots[i*K + j] = block_table[r*bt_row_stride + lp div
+ *                                    block_size] * block_size + lp mod block_size
+ * The -1s stay in place (compact_valid_to_front = False).  With D = 1 and
+ * rank = 0 this is the plain paged request-index -> slot conversion.
+ * valid_count[i] (optional, may be NULL) receives the number of
+ * non-negative outputs of row i.
+ *
+ *   req_id_per_token  device int32 [T]
+ *   block_table       device int32 [num_reqs, bt_row_stride]; columns
+ *                     [0, bt_width) are meaningful, -1 = unallocated
+ *   topk_global       device int32 [T, K], global token positions, -1 padded
+ *   local_slots       device int32 [T, K] output (may not alias inputs)
+ *   valid_count       device int32 [T] output or NULL
+ * Errors: INVALID_ARG for null pointers (T > 0), T < 0, K < 1, D < 1,
+ * rank outside [0, D), block_size < 1, num_reqs < 1, bt_width < 1 or
+ * bt_row_stride < bt_width.  On the device an out-of-range request id or a
+ * position past the block table (or in a -1 block) yields -1 and sets a
+ * device error bit.
+ */
+smla_status smla_dcp_filter_convert_index(
+    const int32_t* req_id_per_token, const int32_t* block_table,
+    int64_t bt_row_stride, int32_t bt_width, int32_t num_reqs,
+    const int32_t* topk_global, int32_t T, int32_t K, int32_t D, int32_t rank,
+    int32_t block_size, int32_t* local_slots, int32_t* valid_count,
+    void* stream);
+
+/*
+ * Bytes of caller-owned workspace smla_sparse_mla_decode needs for (T, H,
+ * K); 0 means none.  The size follows from the shape alone, so a caller can
+ * allocate it once at start-up for its largest batch [P1 Implementation
+ * Notes: per-device scratch allocated at initialisation; P2 "FlashInfer
+ * sparse-MLA DCP workspace": size derived from tokens x gathered heads].
+ * Returns 0 for invalid shapes.
+ */
+size_t smla_decode_workspace_size(int32_t T, int32_t H, int32_t K);
+
+/*
+ * Step 2 -- sparse MLA decode with LSE return [P1 Why; P3 implementation
+ * breakdown steps 1 and 3; the _forward_fp8_kv_mixed_batch snippet].
+ *
+ * For row i, head h, over the valid entries j of local_slots row i
+ * (slot >= 0; every occurrence counts):
+ *   k_j   = dequant(kv_cache row slot_j)              576 dims
+ *           (latent dim c = e4m3(code c) * scale[c div 128], rope = bf16)
+ *   s_j   = sm_scale * <q[i,h,:], k_j>
+ *   lse   = log(sum_j exp(s_j))           natural log, sm_scale included
+ *   out   = sum_j exp(s_j - lse) * latent_j           512 dims
+ * A row with no valid entry is written as the merge identity out = 0,
+ * lse = -inf [P3 executive summary 1, implementation breakdown step 3].
+ *
+ *   q           device bf16 [T, H, 576] (16-byte aligned); H is the
+ *               gathered head count [P1 Implementation Notes]
+ *   kv_cache    device uint8 [num_slots, 656] (16-byte aligned)
+ *   local_slots device int32 [T, K], -1 = masked (scattered, any order)
+ *   out         device bf16 [T, H, 512] output, contiguous, 16-byte aligned
+ *   lse         device fp32 [T, H] output, row = token (spec decode rows
+ *               b*S + s) [P3 implementation breakdown steps 1 and 5]
+ *   workspace   device scratch of at least
+ *               smla_decode_workspace_size(T, H, K) bytes, 256-byte aligned,
+ *               zero-filled before its first use (every call leaves it
+ *               zero-filled again); may be NULL when that size is 0.
+ *               Calls that run concurrently need distinct workspaces.
+ * Errors: INVALID_ARG for null pointers, T < 0, K < 1, H < 1, num_slots < 0,
+ * misaligned q/kv_cache/out; UNSUPPORTED for H > SMLA_MAX_HEADS; WORKSPACE
+ * when the workspace is too small, NULL or misaligned.  A slot >= num_slots
+ * is treated as -1 and sets SMLA_DEVERR_SLOT_RANGE.
+ */
+smla_status smla_sparse_mla_decode(
+    const uint16_t* q, const uint8_t* kv_cache, int64_t num_slots,
+    const int32_t* local_slots, int32_t T, int32_t H, int32_t K,
+    float sm_scale, uint16_t* out, float* lse, void* workspace,
+    size_t workspace_bytes, void* stream);
+
+/*
+ * Step 3 -- LSE-weighted merge of D partials [P1 Why, Scope / Limitations
+ * (the ag_rs flow); P3 executive summary 1 and implementation breakdown
+ * step 3].  With M = max_d lse_d[t,h]:
+ *   M = -inf  -> out = 0, lse = -inf
+ *   otherwise lse = M + log(sum_d exp(lse_d - M)),
+ *             out = sum_d exp(lse_d - lse) * out_d
+ * On one GPU this stands in for the cross-rank LSE all-gather plus output
+ * reduce-scatter.
+ *
+ *   outs  host array of D device pointers, each bf16 [T, H, 512], 16-byte
+ *         aligned
+ *   lses  host array of D device pointers, each fp32 [T, H]
+ *   out   device bf16 [T, H, 512] output (may alias none of the inputs)
+ *   lse   device fp32 [T, H] output
+ * Errors: INVALID_ARG for null pointers, D < 1, T < 0, H < 1, misaligned
+ * buffers; UNSUPPORTED for D > SMLA_MAX_DCP.
+ */
+smla_status smla_dcp_lse_merge(const uint16_t* const* outs,
+                               const float* const* lses, int32_t D, int32_t T,
+                               int32_t H, uint16_t* out, float* lse,
+                               void* stream);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* SMLA_H_ */

@@ -1,0 +1,216 @@
+"""Thin Python binding of ``include/smla.h`` (ctypes).
+
+Argument marshalling only: it checks dtypes/devices/contiguity, allocates
+outputs with torch when the caller passes none, and hands raw device
+pointers plus the current CUDA stream to the C ABI.  Every step of the path
+runs in the library's kernels.  Loading fails loudly when ``libsmla.so`` has
+not been built; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence, Tuple
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsmla.so")
+
+SMLA_OK = 0
+SMLA_ERR_INVALID_ARG = 1
+SMLA_ERR_UNSUPPORTED = 2
+SMLA_ERR_WORKSPACE = 3
+SMLA_ERR_CUDA = 4
+
+DEVERR_BLOCK_TABLE = 1
+DEVERR_REQ_ID = 2
+DEVERR_SLOT_RANGE = 4
+DEVERR_TIMEOUT = 8
+
+MAX_HEADS = 128
+MAX_DCP = 16
+ROW_BYTES = 656
+QK_DIM = 576
+V_DIM = 512
+
+_c_i32, _c_i64, _c_sz, _c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
+
+# name -> (restype, argtypes); mirrors include/smla.h
+SIGNATURES = {
+    "smla_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "smla_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
+    "smla_dcp_filter_convert_index": (ctypes.c_int, [
+        _c_vp, _c_vp, _c_i64, _c_i32, _c_i32, _c_vp, _c_i32, _c_i32, _c_i32, _c_i32,
+        _c_i32, _c_vp, _c_vp, _c_vp]),
+    "smla_decode_workspace_size": (_c_sz, [_c_i32, _c_i32, _c_i32]),
+    "smla_sparse_mla_decode": (ctypes.c_int, [
+        _c_vp, _c_vp, _c_i64, _c_vp, _c_i32, _c_i32, _c_i32, ctypes.c_float, _c_vp,
+        _c_vp, _c_vp, _c_sz, _c_vp]),
+    "smla_dcp_lse_merge": (ctypes.c_int, [
+        _c_vp, _c_vp, _c_i32, _c_i32, _c_i32, _c_vp, _c_vp, _c_vp]),
+}
+
+_lib = None
+
+
+class SmlaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+
+
+def load() -> ctypes.CDLL:
+    """Load libsmla.so once (raises if it was never built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().smla_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != SMLA_OK:
+        raise SmlaError(fn, status)
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream], device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return int(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, device):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def get_device_error(clear: bool = True) -> int:
+    """OR of DEVERR_* bits raised by kernels on the current device."""
+    v = ctypes.c_uint32(0)
+    _check("smla_get_device_error", load().smla_get_device_error(ctypes.byref(v), int(clear)))
+    return int(v.value)
+
+
+def dcp_filter_convert_index(req_id_per_token: torch.Tensor, block_table: torch.Tensor,
+                             topk_global: torch.Tensor, D: int, rank: int,
+                             block_size: int, *, bt_width: Optional[int] = None,
+                             local_slots: Optional[torch.Tensor] = None,
+                             valid_count: Optional[torch.Tensor] = None,
+                             with_valid_count: bool = True,
+                             stream: Optional[torch.cuda.Stream] = None
+                             ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    dev = topk_global.device
+    _need(req_id_per_token, "req_id_per_token", torch.int32, dev)
+    _need(topk_global, "topk_global", torch.int32, dev)
+    if block_table.dtype != torch.int32 or block_table.device != dev or block_table.dim() != 2:
+        raise ValueError("block_table must be a 2-D int32 tensor on the top-k device")
+    if block_table.stride(1) != 1:
+        raise ValueError("block_table rows must be contiguous")
+    T, K = topk_global.shape
+    if local_slots is None:
+        local_slots = torch.empty((T, K), dtype=torch.int32, device=dev)
+    _need(local_slots, "local_slots", torch.int32, dev)
+    if valid_count is None and with_valid_count:
+        valid_count = torch.empty((T,), dtype=torch.int32, device=dev)
+    if valid_count is not None:
+        _need(valid_count, "valid_count", torch.int32, dev)
+    width = block_table.shape[1] if bt_width is None else int(bt_width)
+    st = load().smla_dcp_filter_convert_index(
+        req_id_per_token.data_ptr(), block_table.data_ptr(), block_table.stride(0),
+        width, block_table.shape[0], topk_global.data_ptr(), T, K, D, rank,
+        block_size, local_slots.data_ptr(),
+        valid_count.data_ptr() if valid_count is not None else None,
+        _stream_ptr(stream, dev))
+    _check("smla_dcp_filter_convert_index", st)
+    return local_slots, valid_count
+
+
+def decode_workspace_size(T: int, H: int, K: int) -> int:
+    return int(load().smla_decode_workspace_size(T, H, K))
+
+
+def alloc_decode_workspace(T: int, H: int, K: int, device) -> Optional[torch.Tensor]:
+    """Zero-filled workspace for smla_sparse_mla_decode (None if none needed)."""
+    n = decode_workspace_size(T, H, K)
+    if n == 0:
+        return None
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def sparse_mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, local_slots: torch.Tensor,
+                      sm_scale: float, *, out: Optional[torch.Tensor] = None,
+                      lse: Optional[torch.Tensor] = None,
+                      workspace: Optional[torch.Tensor] = None,
+                      stream: Optional[torch.cuda.Stream] = None
+                      ) -> Tuple[torch.Tensor, torch.Tensor]:
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev)
+    _need(kv_cache, "kv_cache", torch.uint8, dev)
+    _need(local_slots, "local_slots", torch.int32, dev)
+    T, H, Dq = q.shape
+    if Dq != QK_DIM:
+        raise ValueError(f"q last dim must be {QK_DIM}")
+    if kv_cache.dim() != 2 or kv_cache.shape[1] != ROW_BYTES:
+        raise ValueError(f"kv_cache must be [num_slots, {ROW_BYTES}] uint8")
+    K = local_slots.shape[1]
+    if local_slots.shape[0] != T:
+        raise ValueError("local_slots rows must equal q tokens")
+    if out is None:
+        out = torch.empty((T, H, V_DIM), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, dev)
+    _need(lse, "lse", torch.float32, dev)
+    if workspace is None:
+        workspace = alloc_decode_workspace(T, H, K, dev)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().smla_sparse_mla_decode(
+        q.data_ptr(), kv_cache.data_ptr(), kv_cache.shape[0], local_slots.data_ptr(),
+        T, H, K, float(sm_scale), out.data_ptr(), lse.data_ptr(), ws_ptr, ws_bytes,
+        _stream_ptr(stream, dev))
+    _check("smla_sparse_mla_decode", st)
+    return out, lse
+
+
+def dcp_lse_merge(outs: Sequence[torch.Tensor], lses: Sequence[torch.Tensor], *,
+                  out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                  stream: Optional[torch.cuda.Stream] = None
+                  ) -> Tuple[torch.Tensor, torch.Tensor]:
+    D = len(outs)
+    if D != len(lses) or D < 1:
+        raise ValueError("need as many lse tensors as out tensors (>= 1)")
+    dev = outs[0].device
+    T, H, V = outs[0].shape
+    for o, l in zip(outs, lses):
+        _need(o, "outs[d]", torch.bfloat16, dev)
+        _need(l, "lses[d]", torch.float32, dev)
+        if tuple(o.shape) != (T, H, V) or tuple(l.shape) != (T, H):
+            raise ValueError("all partials must share [T, H, 512] / [T, H]")
+    if out is None:
+        out = torch.empty((T, H, V_DIM), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, dev)
+    _need(lse, "lse", torch.float32, dev)
+    out_ptrs = (ctypes.c_void_p * D)(*[o.data_ptr() for o in outs])
+    lse_ptrs = (ctypes.c_void_p * D)(*[l.data_ptr() for l in lses])
+    st = load().smla_dcp_lse_merge(out_ptrs, lse_ptrs, D, T, H, out.data_ptr(),
+                                   lse.data_ptr(), _stream_ptr(stream, dev))
+    _check("smla_dcp_lse_merge", st)
+    return out, lse

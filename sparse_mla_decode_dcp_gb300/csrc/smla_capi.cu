@@ -1,0 +1,142 @@
+// C ABI of the library: host-side argument checks, then one launch per call.
+// Every check runs before anything touches the GPU, so a rejected call has
+// no side effect and needs no device.
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/smla.h"
+#include "smla_internal.h"
+
+namespace {
+
+inline bool misaligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) != 0;
+}
+
+inline smla_status from_cuda(cudaError_t e) {
+  return e == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* smla_status_string(smla_status status) {
+  switch (status) {
+    case SMLA_OK: return "SMLA_OK";
+    case SMLA_ERR_INVALID_ARG: return "SMLA_ERR_INVALID_ARG";
+    case SMLA_ERR_UNSUPPORTED: return "SMLA_ERR_UNSUPPORTED";
+    case SMLA_ERR_WORKSPACE: return "SMLA_ERR_WORKSPACE";
+    case SMLA_ERR_CUDA: return "SMLA_ERR_CUDA";
+    default: return "SMLA_UNKNOWN_STATUS";
+  }
+}
+
+smla_status smla_get_device_error(uint32_t* flags, int clear) {
+  if (flags == nullptr) return SMLA_ERR_INVALID_ARG;
+  *flags = 0;
+  cudaError_t e = smla::index_error_word(flags, clear != 0);
+  if (e == cudaSuccess) e = smla::decode_error_word(flags, clear != 0);
+  return from_cuda(e);
+}
+
+smla_status smla_dcp_filter_convert_index(
+    const int32_t* req_id_per_token, const int32_t* block_table,
+    int64_t bt_row_stride, int32_t bt_width, int32_t num_reqs,
+    const int32_t* topk_global, int32_t T, int32_t K, int32_t D, int32_t rank,
+    int32_t block_size, int32_t* local_slots, int32_t* valid_count,
+    void* stream) {
+  if (T < 0 || K < 1 || D < 1 || rank < 0 || rank >= D || block_size < 1 ||
+      num_reqs < 1 || bt_width < 1 || bt_row_stride < bt_width)
+    return SMLA_ERR_INVALID_ARG;
+  if (T == 0) return SMLA_OK;
+  if (!req_id_per_token || !block_table || !topk_global || !local_slots)
+    return SMLA_ERR_INVALID_ARG;
+  if (misaligned(req_id_per_token, 4) || misaligned(block_table, 4) ||
+      misaligned(topk_global, 4) || misaligned(local_slots, 4) ||
+      (valid_count && misaligned(valid_count, 4)))
+    return SMLA_ERR_INVALID_ARG;
+  smla::IndexArgs a;
+  a.req_id = req_id_per_token;
+  a.block_table = block_table;
+  a.bt_row_stride = bt_row_stride;
+  a.bt_width = bt_width;
+  a.num_reqs = num_reqs;
+  a.topk = topk_global;
+  a.T = T;
+  a.K = K;
+  a.D = D;
+  a.rank = rank;
+  a.block_size = block_size;
+  a.local_slots = local_slots;
+  a.valid_count = valid_count;
+  return from_cuda(smla::launch_filter_convert(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t smla_decode_workspace_size(int32_t T, int32_t H, int32_t K) {
+  if (T < 0 || H < 1 || H > SMLA_MAX_HEADS || K < 1) return 0;
+  return smla::decode_workspace_bytes(T, H, K);
+}
+
+smla_status smla_sparse_mla_decode(
+    const uint16_t* q, const uint8_t* kv_cache, int64_t num_slots,
+    const int32_t* local_slots, int32_t T, int32_t H, int32_t K,
+    float sm_scale, uint16_t* out, float* lse, void* workspace,
+    size_t workspace_bytes, void* stream) {
+  if (T < 0 || K < 1 || H < 1 || num_slots < 0 || !std::isfinite(sm_scale))
+    return SMLA_ERR_INVALID_ARG;
+  if (H > SMLA_MAX_HEADS) return SMLA_ERR_UNSUPPORTED;
+  if (T == 0) return SMLA_OK;
+  if (!q || !kv_cache || !local_slots || !out || !lse) return SMLA_ERR_INVALID_ARG;
+  if (misaligned(q, 16) || misaligned(kv_cache, 16) || misaligned(out, 16) ||
+      misaligned(local_slots, 4) || misaligned(lse, 4))
+    return SMLA_ERR_INVALID_ARG;
+  const size_t need = smla::decode_workspace_bytes(T, H, K);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
+                   misaligned(workspace, 256)))
+    return SMLA_ERR_WORKSPACE;
+  smla::DecodeArgs a;
+  a.q = q;
+  a.kv = kv_cache;
+  a.num_slots = num_slots;
+  a.slots = local_slots;
+  a.T = T;
+  a.H = H;
+  a.K = K;
+  a.sm_scale = sm_scale;
+  a.out = out;
+  a.lse = lse;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  return from_cuda(smla::launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+smla_status smla_dcp_lse_merge(const uint16_t* const* outs,
+                               const float* const* lses, int32_t D, int32_t T,
+                               int32_t H, uint16_t* out, float* lse,
+                               void* stream) {
+  if (D < 1 || T < 0 || H < 1) return SMLA_ERR_INVALID_ARG;
+  if (D > SMLA_MAX_DCP) return SMLA_ERR_UNSUPPORTED;
+  if (T == 0) return SMLA_OK;
+  if (!outs || !lses || !out || !lse) return SMLA_ERR_INVALID_ARG;
+  if (misaligned(out, 16) || misaligned(lse, 4)) return SMLA_ERR_INVALID_ARG;
+  smla::MergeArgs a;
+  for (int d = 0; d < D; ++d) {
+    if (!outs[d] || !lses[d] || misaligned(outs[d], 16) || misaligned(lses[d], 4))
+      return SMLA_ERR_INVALID_ARG;
+    a.outs[d] = outs[d];
+    a.lses[d] = lses[d];
+  }
+  for (int d = D; d < smla::kMaxMerge; ++d) {
+    a.outs[d] = nullptr;
+    a.lses[d] = nullptr;
+  }
+  a.D = D;
+  a.T = T;
+  a.H = H;
+  a.out = out;
+  a.lse = lse;
+  return from_cuda(smla::launch_merge(a, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

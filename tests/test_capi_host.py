@@ -1,0 +1,175 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and
+loads, exports every function include/smla.h declares, and rejects bad
+arguments with the documented status before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_mla_decode_dcp_gb300 import build as smla_build
+from sparse_mla_decode_dcp_gb300 import capi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "smla.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    smla_build.build()
+    return capi.load()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    src = re.sub(r"#define[^\n]*", "", src)
+    return sorted(set(re.findall(r"\b(smla_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_three_path_calls():
+    names = _declared_functions()
+    for n in ("smla_dcp_filter_convert_index", "smla_sparse_mla_decode",
+              "smla_dcp_lse_merge", "smla_decode_workspace_size",
+              "smla_status_string", "smla_get_device_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_function(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"libsmla.so does not export {name}"
+        assert name in capi.SIGNATURES, f"binding lacks a signature for {name}"
+
+
+def test_status_strings(lib):
+    assert capi.status_string(0) == "SMLA_OK"
+    assert capi.status_string(1) == "SMLA_ERR_INVALID_ARG"
+    assert capi.status_string(2) == "SMLA_ERR_UNSUPPORTED"
+    assert capi.status_string(3) == "SMLA_ERR_WORKSPACE"
+    assert capi.status_string(4) == "SMLA_ERR_CUDA"
+    assert capi.status_string(99) == "SMLA_UNKNOWN_STATUS"
+
+
+FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced
+
+
+def _convert(lib, **kw):
+    a = dict(req=FAKE, bt=FAKE, stride=4, width=4, nreq=2, topk=FAKE, T=3, K=8,
+             D=2, rank=0, bs=16, out=FAKE, cnt=None)
+    a.update(kw)
+    return lib.smla_dcp_filter_convert_index(
+        a["req"], a["bt"], a["stride"], a["width"], a["nreq"], a["topk"], a["T"],
+        a["K"], a["D"], a["rank"], a["bs"], a["out"], a["cnt"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=-1), capi.SMLA_ERR_INVALID_ARG),
+    (dict(K=0), capi.SMLA_ERR_INVALID_ARG),
+    (dict(D=0), capi.SMLA_ERR_INVALID_ARG),
+    (dict(rank=2), capi.SMLA_ERR_INVALID_ARG),
+    (dict(rank=-1), capi.SMLA_ERR_INVALID_ARG),
+    (dict(bs=0), capi.SMLA_ERR_INVALID_ARG),
+    (dict(nreq=0), capi.SMLA_ERR_INVALID_ARG),
+    (dict(width=0), capi.SMLA_ERR_INVALID_ARG),
+    (dict(stride=3), capi.SMLA_ERR_INVALID_ARG),
+    (dict(req=None), capi.SMLA_ERR_INVALID_ARG),
+    (dict(bt=None), capi.SMLA_ERR_INVALID_ARG),
+    (dict(topk=None), capi.SMLA_ERR_INVALID_ARG),
+    (dict(out=None), capi.SMLA_ERR_INVALID_ARG),
+    (dict(out=FAKE + 2), capi.SMLA_ERR_INVALID_ARG),
+    (dict(cnt=FAKE + 1), capi.SMLA_ERR_INVALID_ARG),
+    (dict(T=0, req=None, topk=None, out=None), capi.SMLA_OK),
+])
+def test_convert_argument_checks(lib, kw, status):
+    assert _convert(lib, **kw) == status
+
+
+def _decode(lib, **kw):
+    a = dict(q=FAKE, kv=FAKE, ns=100, slots=FAKE, T=2, H=16, K=64, scale=0.07,
+             out=FAKE, lse=FAKE, ws=None, wsb=0)
+    a.update(kw)
+    if "ws_auto" in kw:
+        need = lib.smla_decode_workspace_size(a["T"], a["H"], a["K"])
+        a["ws"], a["wsb"] = (FAKE if need else None), need
+    return lib.smla_sparse_mla_decode(
+        a["q"], a["kv"], a["ns"], a["slots"], a["T"], a["H"], a["K"],
+        ctypes.c_float(a["scale"]), a["out"], a["lse"], a["ws"], a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=-1), capi.SMLA_ERR_INVALID_ARG),
+    (dict(K=0), capi.SMLA_ERR_INVALID_ARG),
+    (dict(H=0), capi.SMLA_ERR_INVALID_ARG),
+    (dict(H=129), capi.SMLA_ERR_UNSUPPORTED),
+    (dict(H=256), capi.SMLA_ERR_UNSUPPORTED),
+    (dict(ns=-1), capi.SMLA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), capi.SMLA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), capi.SMLA_ERR_INVALID_ARG),
+    (dict(q=None), capi.SMLA_ERR_INVALID_ARG),
+    (dict(kv=None), capi.SMLA_ERR_INVALID_ARG),
+    (dict(slots=None), capi.SMLA_ERR_INVALID_ARG),
+    (dict(out=None), capi.SMLA_ERR_INVALID_ARG),
+    (dict(lse=None), capi.SMLA_ERR_INVALID_ARG),
+    (dict(q=FAKE + 8), capi.SMLA_ERR_INVALID_ARG),
+    (dict(kv=FAKE + 4), capi.SMLA_ERR_INVALID_ARG),
+    (dict(out=FAKE + 2), capi.SMLA_ERR_INVALID_ARG),
+    (dict(T=0, q=None, kv=None, slots=None, out=None, lse=None), capi.SMLA_OK),
+])
+def test_decode_argument_checks(lib, kw, status):
+    assert _decode(lib, **kw) == status
+
+
+def test_decode_workspace_checks(lib):
+    for T, H, K in [(64, 128, 2048), (32, 64, 2048), (2, 16, 64), (128, 128, 2048)]:
+        need = capi.decode_workspace_size(T, H, K)
+        if need == 0:
+            continue
+        assert _decode(lib, T=T, H=H, K=K, ws=None, wsb=0) == capi.SMLA_ERR_WORKSPACE
+        assert _decode(lib, T=T, H=H, K=K, ws=FAKE, wsb=need - 1) == capi.SMLA_ERR_WORKSPACE
+        assert _decode(lib, T=T, H=H, K=K, ws=FAKE + 16, wsb=need) == capi.SMLA_ERR_WORKSPACE
+
+
+def test_workspace_size_shape_only(lib):
+    assert capi.decode_workspace_size(-1, 16, 64) == 0
+    assert capi.decode_workspace_size(2, 0, 64) == 0
+    assert capi.decode_workspace_size(2, 129, 64) == 0
+    assert capi.decode_workspace_size(2, 16, 0) == 0
+    # pure function of the shape
+    assert capi.decode_workspace_size(64, 128, 2048) == capi.decode_workspace_size(64, 128, 2048)
+    # monotone in T
+    assert capi.decode_workspace_size(128, 128, 2048) >= capi.decode_workspace_size(64, 128, 2048)
+
+
+def _merge(lib, D=2, T=3, H=4, outs=None, lses=None, out=FAKE, lse=FAKE):
+    if outs is None:
+        outs = [FAKE] * max(D, 1)
+    if lses is None:
+        lses = [FAKE] * max(D, 1)
+    op = (ctypes.c_void_p * len(outs))(*outs)
+    lp = (ctypes.c_void_p * len(lses))(*lses)
+    return lib.smla_dcp_lse_merge(op, lp, D, T, H, out, lse, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=0), capi.SMLA_ERR_INVALID_ARG),
+    (dict(D=17), capi.SMLA_ERR_UNSUPPORTED),
+    (dict(T=-1), capi.SMLA_ERR_INVALID_ARG),
+    (dict(H=0), capi.SMLA_ERR_INVALID_ARG),
+    (dict(out=None), capi.SMLA_ERR_INVALID_ARG),
+    (dict(lse=None), capi.SMLA_ERR_INVALID_ARG),
+    (dict(out=FAKE + 8), capi.SMLA_ERR_INVALID_ARG),
+    (dict(outs=[FAKE, None]), capi.SMLA_ERR_INVALID_ARG),
+    (dict(outs=[FAKE, FAKE + 8]), capi.SMLA_ERR_INVALID_ARG),
+    (dict(lses=[FAKE, FAKE + 2]), capi.SMLA_ERR_INVALID_ARG),
+    (dict(T=0), capi.SMLA_OK),
+])
+def test_merge_argument_checks(lib, kw, status):
+    assert _merge(lib, **kw) == status
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(capi, "_lib", None)
+    monkeypatch.setattr(capi, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        capi.load()

@@ -1,0 +1,374 @@
+"""GPU parity: every step of the path through the C ABI against the float64
+oracle on the same seeded inputs, for all five workloads at full size plus
+edge cases.  Indices and valid counts must be bit-exact; out/lse follow the
+tolerances in oracle/compare.py."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle.compare import compare_out_lse
+from sparse_mla_decode_dcp_gb300 import capi, inputs
+from sparse_mla_decode_dcp_gb300.pipeline import DcpDecodeStep
+
+pytestmark = pytest.mark.gpu
+
+
+def _q_bits(q):
+    return q.detach().cpu().contiguous().view(torch.int16).numpy().astype(np.uint16)
+
+
+class Run:
+    """One workload on the GPU plus its oracle results (computed lazily)."""
+
+    def __init__(self, name, dev):
+        self.wl = inputs.make_workload(name, seed=0, device=dev)
+        self.step = DcpDecodeStep(self.wl, device=dev)
+        capi.load()
+        capi.get_device_error(clear=True)
+        self.out, self.lse = self.step.run()
+        torch.cuda.synchronize()
+        self.deverr = capi.get_device_error(clear=True)
+        self._ref = None
+
+    def ref(self):
+        if self._ref is None:
+            wl = self.wl
+            q = _q_bits(wl.q)
+            slots, counts, outs, lses = [], [], [], []
+            for d, s in enumerate(wl.shards):
+                sl, c = oracle.dcp_filter_convert_index(wl.req_id, s.block_table, wl.topk,
+                                                        wl.D, d, wl.spec.block_size)
+                o, l = oracle.sparse_mla_decode(q, s.pool.cpu().numpy(), sl, wl.spec.sm_scale)
+                slots.append(sl)
+                counts.append(c)
+                outs.append(o)
+                lses.append(l)
+            self._ref = (slots, counts, outs, lses)
+        return self._ref
+
+
+_RUNS = {}
+
+
+@pytest.fixture(scope="module", params=inputs.WORKLOAD_ORDER)
+def run(request, cuda_device):
+    name = request.param
+    if name not in _RUNS:
+        _RUNS.clear()
+        torch.cuda.empty_cache()
+        _RUNS[name] = Run(name, cuda_device)
+    return _RUNS[name]
+
+
+def test_index_bit_exact(run):
+    slots, counts, _, _ = run.ref()
+    for d in range(run.wl.D):
+        assert np.array_equal(run.step.local_slots[d].cpu().numpy(), slots[d]), f"shard {d}"
+        assert np.array_equal(run.step.valid_count[d].cpu().numpy(), counts[d]), f"shard {d}"
+    assert run.deverr == 0
+
+
+def test_decode_matches_oracle_per_shard(run):
+    _, _, outs, lses = run.ref()
+    for d in range(run.wl.D):
+        compare_out_lse(run.step.part_out[d], run.step.part_lse[d], outs[d], lses[d],
+                        where=f"{run.wl.spec.name} shard {d}")
+
+
+def test_merged_matches_oracle(run):
+    _, _, outs, lses = run.ref()
+    ref_out, ref_lse = oracle.lse_merge(outs, lses)
+    compare_out_lse(run.out, run.lse, ref_out, ref_lse, where=f"{run.wl.spec.name} merged")
+
+
+def test_merge_kernel_alone_on_gpu_partials(run):
+    """The oracle merge fed with the GPU's own bf16/fp32 partials isolates the
+    merge kernel's error from the decode kernel's."""
+    outs = [oracle.compare.to_f64(o) for o in run.step.part_out]
+    lses = [oracle.compare.to_f64(l) for l in run.step.part_lse]
+    ref_out, ref_lse = oracle.lse_merge(outs, lses)
+    compare_out_lse(run.out, run.lse, ref_out, ref_lse, where="merge only")
+    fin = np.isfinite(ref_lse)
+    assert np.abs(run.lse.cpu().numpy()[fin] - ref_lse[fin]).max(initial=0) < 1e-5
+
+
+def test_empty_shard_rows_are_identity(run):
+    """Rows whose shard holds no candidate come out as exact (0, -inf)."""
+    for d in range(run.wl.D):
+        empty = run.step.valid_count[d].cpu().numpy() == 0
+        if not empty.any():
+            continue
+        bits = run.step.part_out[d].cpu().view(torch.int16).numpy()[empty]
+        assert np.all(bits == 0)
+        assert torch.isneginf(run.step.part_lse[d].cpu()[torch.from_numpy(empty)]).all()
+
+
+# --------------------------------------------------------------- edge cases
+def _small_pool(n, dev, seed=1):
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    return inputs.random_rows(n, gen, dev)
+
+
+def _decode_vs_oracle(q, pool, slots, sm_scale, where):
+    out, lse = capi.sparse_mla_decode(q, pool, slots, sm_scale)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle.sparse_mla_decode(_q_bits(q), pool.cpu().numpy(),
+                                                slots.cpu().numpy(), sm_scale)
+    compare_out_lse(out, lse, ref_out, ref_lse, where=where)
+    return out, lse
+
+
+def test_empty_row_case_from_pages(cuda_device):
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
+                                    "empty_row_case.json")))
+    pool = _small_pool(4, cuda_device)
+    gen = torch.Generator(device=cuda_device).manual_seed(5)
+    q = torch.randn((g["num_tokens"], g["num_heads"], 576), generator=gen,
+                    device=cuda_device).to(torch.bfloat16)
+    slots = torch.tensor(g["local_indices"], dtype=torch.int32, device=cuda_device)
+    out, lse = _decode_vs_oracle(q, pool, slots, 1 / math.sqrt(192), "pages' case")
+    for r in g["empty_rows"]:
+        assert torch.all(out[r].view(torch.int16) == 0)
+        assert torch.isneginf(lse[r]).all()
+    for r in g["nonempty_rows"]:
+        assert torch.isfinite(lse[r]).all()
+    assert out.is_contiguous() and not out.isnan().any() and not lse.isnan().any()
+
+
+@pytest.mark.parametrize("H", [1, 2, 16, 33, 64, 100, 127, 128])
+def test_decode_head_counts(cuda_device, H):
+    dev = cuda_device
+    pool = _small_pool(300, dev, seed=H)
+    g = torch.Generator(device=dev).manual_seed(H)
+    T, K = 5, 96
+    q = torch.randn((T, H, 576), generator=g, device=dev).to(torch.bfloat16)
+    rng = np.random.default_rng(H)
+    s = np.stack([rng.permutation(np.concatenate([rng.choice(300, K - 10 * i, replace=False),
+                                                  -np.ones(10 * i, np.int64)]))
+                  for i in range(T)]).astype(np.int32)
+    s[3] = -1  # one fully empty row
+    slots = torch.from_numpy(s).to(dev)
+    _decode_vs_oracle(q, pool, slots, 1 / math.sqrt(192), f"H={H}")
+
+
+@pytest.mark.parametrize("K", [1, 3, 37, 64, 129, 2048, 4096])
+def test_decode_topk_sizes(cuda_device, K):
+    dev = cuda_device
+    n = max(K, 8) + 50
+    pool = _small_pool(n, dev, seed=K)
+    g = torch.Generator(device=dev).manual_seed(K)
+    T, H = 3, 128
+    q = torch.randn((T, H, 576), generator=g, device=dev).to(torch.bfloat16)
+    rng = np.random.default_rng(K)
+    s = np.stack([rng.choice(n, K, replace=False) for _ in range(T)]).astype(np.int32)
+    s[1, ::2] = -1
+    _decode_vs_oracle(q, pool, torch.from_numpy(s).to(dev), 1 / math.sqrt(192), f"K={K}")
+
+
+def test_decode_single_valid_slot_lse_is_score(cuda_device):
+    dev = cuda_device
+    pool = _small_pool(10, dev, seed=3)
+    g = torch.Generator(device=dev).manual_seed(3)
+    q = torch.randn((4, 128, 576), generator=g, device=dev).to(torch.bfloat16)
+    s = torch.full((4, 64), -1, dtype=torch.int32, device=dev)
+    for i in range(4):
+        s[i, 7 * i] = i + 2
+    _decode_vs_oracle(q, pool, s, 1 / math.sqrt(192), "single slot")
+
+
+def test_decode_duplicate_slots(cuda_device):
+    dev = cuda_device
+    pool = _small_pool(20, dev, seed=4)
+    g = torch.Generator(device=dev).manual_seed(4)
+    q = torch.randn((2, 64, 576), generator=g, device=dev).to(torch.bfloat16)
+    s = torch.tensor([[0, 0, 5, 5, 5, -1, 7, 0], [3, -1, 3, 3, -1, -1, 19, 3]],
+                     dtype=torch.int32, device=dev)
+    _decode_vs_oracle(q, pool, s, 1 / math.sqrt(192), "duplicates")
+
+
+def test_decode_order_invariance(cuda_device):
+    dev = cuda_device
+    pool = _small_pool(5000, dev, seed=6)
+    g = torch.Generator(device=dev).manual_seed(6)
+    q = torch.randn((4, 128, 576), generator=g, device=dev).to(torch.bfloat16)
+    rng = np.random.default_rng(6)
+    s = np.stack([rng.choice(5000, 2048, replace=False) for _ in range(4)]).astype(np.int32)
+    s[:, rng.choice(2048, 500, replace=False)] = -1
+    perm = np.stack([rng.permutation(row) for row in s])
+    o1, l1 = _decode_vs_oracle(q, pool, torch.from_numpy(s).to(dev), 0.072, "order a")
+    o2, l2 = _decode_vs_oracle(q, pool, torch.from_numpy(perm).to(dev), 0.072, "order b")
+    assert (l1 - l2).abs().max().item() < 2e-3
+
+
+def test_decode_slot_out_of_range_is_masked_and_flagged(cuda_device):
+    dev = cuda_device
+    pool = _small_pool(16, dev, seed=7)
+    g = torch.Generator(device=dev).manual_seed(7)
+    q = torch.randn((2, 16, 576), generator=g, device=dev).to(torch.bfloat16)
+    bad = torch.tensor([[1, 2, 16, 3], [100000, -1, -1, -1]], dtype=torch.int32, device=dev)
+    good = torch.tensor([[1, 2, -1, 3], [-1, -1, -1, -1]], dtype=torch.int32, device=dev)
+    capi.get_device_error(clear=True)
+    out_b, lse_b = capi.sparse_mla_decode(q, pool, bad, 0.07)
+    torch.cuda.synchronize()
+    assert capi.get_device_error(clear=True) & capi.DEVERR_SLOT_RANGE
+    out_g, lse_g = capi.sparse_mla_decode(q, pool, good, 0.07)
+    torch.cuda.synchronize()
+    assert torch.equal(out_b, out_g) and torch.equal(lse_b, lse_g)
+    assert torch.isneginf(lse_b[1]).all()
+
+
+def test_zero_tokens_is_noop(cuda_device):
+    dev = cuda_device
+    pool = _small_pool(4, dev)
+    q = torch.empty((0, 16, 576), dtype=torch.bfloat16, device=dev)
+    s = torch.empty((0, 8), dtype=torch.int32, device=dev)
+    out, lse = capi.sparse_mla_decode(q, pool, s, 0.07)
+    assert out.shape == (0, 16, 512) and lse.shape == (0, 16)
+    req = torch.empty((0,), dtype=torch.int32, device=dev)
+    bt = torch.zeros((1, 1), dtype=torch.int32, device=dev)
+    ls, cnt = capi.dcp_filter_convert_index(req, bt, s, 2, 0, 16)
+    assert ls.shape == (0, 8)
+    o, l = capi.dcp_lse_merge([out, out], [lse, lse])
+    assert o.shape == (0, 16, 512)
+
+
+# ---------------------------------------------------------- index edge cases
+def _convert_vs_oracle(req, bt, topk, D, rank, bs, dev, width=None):
+    ls, cnt = capi.dcp_filter_convert_index(
+        torch.from_numpy(req).to(dev), torch.from_numpy(bt).to(dev),
+        torch.from_numpy(topk).to(dev), D, rank, bs, bt_width=width)
+    torch.cuda.synchronize()
+    ref_ls, ref_cnt = oracle.dcp_filter_convert_index(
+        req, bt if width is None else bt[:, :width], topk, D, rank, bs)
+    assert np.array_equal(ls.cpu().numpy(), ref_ls)
+    assert np.array_equal(cnt.cpu().numpy(), ref_cnt)
+
+
+def test_index_worked_examples_on_gpu(cuda_device):
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
+                                    "index_worked_example.json")))
+    for case in g["cases"]:
+        ls, cnt = capi.dcp_filter_convert_index(
+            torch.tensor(case["req_id"], dtype=torch.int32, device=cuda_device),
+            torch.tensor(case["block_table"], dtype=torch.int32, device=cuda_device),
+            torch.tensor(case["topk"], dtype=torch.int32, device=cuda_device),
+            case["D"], case["rank"], case["block_size"])
+        assert ls.cpu().tolist() == case["local_slots"], case["note"]
+        assert cnt.cpu().tolist() == case["valid_count"], case["note"]
+
+
+@pytest.mark.parametrize("K", [1, 5, 37, 64, 2048, 3001])
+@pytest.mark.parametrize("D", [1, 2, 3, 4, 8])
+def test_index_random_shapes(cuda_device, K, D):
+    rng = np.random.default_rng(K * 10 + D)
+    R, bs = 5, 16
+    ctx = rng.integers(1, 5000, size=R)
+    W = int(max(-(-(c // D + 1) // bs) for c in ctx)) + 1
+    for rank in range(D):
+        bt = np.full((R, W + 3), -1, dtype=np.int32)
+        for r in range(R):
+            n = len(range(rank, int(ctx[r]), D))
+            nb = -(-n // bs)
+            bt[r, :nb] = rng.permutation(10000)[:nb]
+        req = rng.integers(0, R, size=7).astype(np.int32)
+        topk = np.stack([np.where(rng.random(K) < 0.1, -1,
+                                  rng.integers(0, int(ctx[r]), size=K)) for r in req]).astype(np.int32)
+        _convert_vs_oracle(req, bt, topk, D, rank, bs, cuda_device)
+
+
+def test_index_bad_inputs_masked_and_flagged(cuda_device):
+    dev = cuda_device
+    bt = torch.tensor([[3, -1], [5, 6]], dtype=torch.int32, device=dev)
+    req = torch.tensor([0, 7, 1], dtype=torch.int32, device=dev)  # 7: bad request
+    # row 0: 40 -> local 20 -> block col 1 = -1 (unallocated); 100 -> col 3 past width
+    topk = torch.tensor([[0, 40, 100, 2], [0, 2, 4, 6], [0, 20, 2, -5]],
+                        dtype=torch.int32, device=dev)
+    capi.get_device_error(clear=True)
+    ls, cnt = capi.dcp_filter_convert_index(req, bt, topk, 2, 0, 16)
+    torch.cuda.synchronize()
+    err = capi.get_device_error(clear=True)
+    assert err & capi.DEVERR_BLOCK_TABLE and err & capi.DEVERR_REQ_ID
+    assert ls.cpu().tolist() == [[48, -1, -1, 49], [-1, -1, -1, -1], [80, 90, 81, -1]]
+    assert cnt.cpu().tolist() == [2, 0, 3]
+
+
+def test_index_row_stride_and_width(cuda_device):
+    rng = np.random.default_rng(9)
+    bt = np.full((3, 12), -1, dtype=np.int32)
+    bt[:, :4] = rng.permutation(100)[:12].reshape(3, 4)
+    req = np.array([2, 0, 1, 1], dtype=np.int32)
+    topk = rng.integers(-1, 4 * 16 * 2, size=(4, 40)).astype(np.int32)
+    _convert_vs_oracle(req, bt, topk, 2, 1, 16, cuda_device, width=4)
+
+
+def test_index_permutation_equivariance(cuda_device):
+    dev = cuda_device
+    wl = inputs.make_workload("tiny", seed=3)
+    perm = np.random.default_rng(3).permutation(wl.K)
+    for d, s in enumerate(wl.shards):
+        bt = torch.from_numpy(s.block_table).to(dev)
+        req = torch.from_numpy(wl.req_id).to(dev)
+        a, _ = capi.dcp_filter_convert_index(req, bt, torch.from_numpy(wl.topk).to(dev),
+                                             wl.D, d, wl.spec.block_size)
+        b, _ = capi.dcp_filter_convert_index(req, bt,
+                                             torch.from_numpy(wl.topk[:, perm].copy()).to(dev),
+                                             wl.D, d, wl.spec.block_size)
+        assert torch.equal(a[:, torch.from_numpy(perm).to(dev)], b)
+
+
+# ---------------------------------------------------------- merge edge cases
+def test_merge_all_empty_and_identity(cuda_device):
+    dev = cuda_device
+    T, H = 3, 8
+    g = torch.Generator(device=dev).manual_seed(11)
+    o = torch.randn((T, H, 512), generator=g, device=dev).to(torch.bfloat16)
+    l = torch.randn((T, H), generator=g, device=dev)
+    z = torch.zeros_like(o)
+    ninf = torch.full_like(l, -math.inf)
+    out, lse = capi.dcp_lse_merge([z, o, z], [ninf, l, ninf])
+    assert torch.equal(out, o)
+    assert (lse - l).abs().max().item() < 1e-6
+    out, lse = capi.dcp_lse_merge([z, z], [ninf, ninf])
+    assert torch.all(out.view(torch.int16) == 0) and torch.isneginf(lse).all()
+
+
+@pytest.mark.parametrize("D", [1, 2, 5, 16])
+def test_merge_random_vs_oracle(cuda_device, D):
+    dev = cuda_device
+    T, H = 7, 33
+    g = torch.Generator(device=dev).manual_seed(D)
+    outs = [torch.randn((T, H, 512), generator=g, device=dev).to(torch.bfloat16)
+            for _ in range(D)]
+    lses = [torch.randn((T, H), generator=g, device=dev) * 5 for _ in range(D)]
+    lses[0][2] = -math.inf
+    out, lse = capi.dcp_lse_merge(outs, lses)
+    ref_out, ref_lse = oracle.lse_merge([oracle.compare.to_f64(x) for x in outs],
+                                        [oracle.compare.to_f64(x) for x in lses])
+    compare_out_lse(out, lse, ref_out, ref_lse, where=f"merge D={D}")
+
+
+# ---------------------------------------------------------------- spec decode
+def test_spec_decode_rows_equal_single_token_calls(cuda_device):
+    """The MTP step's batched rows (b*2 + s) equal per-token calls."""
+    dev = cuda_device
+    spec = inputs.WorkloadSpec(
+        name="mtp_small", num_reqs=6, tokens_per_req=2, heads=128, topk=512, dcp=2,
+        block_size=64, ctx_kind="uniform", ctx_lo=600, ctx_hi=3000)
+    wl = inputs.make_workload(spec, seed=12, device=dev)
+    step = DcpDecodeStep(wl, device=dev)
+    step.run()
+    torch.cuda.synchronize()
+    for d in range(wl.D):
+        for i in range(wl.T):
+            o, l = capi.sparse_mla_decode(step.q[i:i + 1], step.pools[d],
+                                          step.local_slots[d][i:i + 1], spec.sm_scale)
+            assert (o[0].float() - step.part_out[d][i].float()).abs().max().item() < 2e-2
+            assert (l[0] - step.part_lse[d][i]).abs().max().item() < 2e-3
