@@ -3,7 +3,10 @@
 One step = the whole hot path over one decode batch of the DCP=4 long-context
 workload (64 requests x 1 query token, H=128 gathered heads, top-k 2048, four
 simulated shards): per shard filter+convert and sparse MLA decode, then the
-LSE merge of the four partials.  Inputs are resident in HBM when the timed
+LSE merge of the four partials.  `--path fused` (default) runs the step as one
+launch (conversion, decode and merge fused); `--path pipeline` as the 2D+1
+launches of the three C-ABI calls.  Both are timed; the JSON line reports the
+chosen one as `value` and both under `paths`.  Inputs are resident in HBM when the timed
 region starts; L2 is flushed (a 256 MiB write) before every timed step, outside
 the step's CUDA events.
 
@@ -19,6 +22,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -35,7 +39,9 @@ UNIT = "query-tokens/s"
 DEFAULT_WORKLOAD = "dcp4_long"
 FLUSH_BYTES = 256 << 20
 QK_DIM, V_DIM, ROW_BYTES = 576, 512, 656
-DECODE_SOURCES = ["sparse_mla_decode_dcp_gb300/csrc/smla_decode.cu"]  # hashed for traffic validity
+# hashed to decide whether a committed ncu traffic figure still applies
+DECODE_SOURCES = ["sparse_mla_decode_dcp_gb300/csrc/smla_decode.cu",
+                  "sparse_mla_decode_dcp_gb300/csrc/smla_sm100.cuh"]
 
 
 def parse_args(argv=None):
@@ -45,6 +51,8 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--path", default="fused", choices=["fused", "pipeline"],
+                   help="fused: one launch per step; pipeline: D x convert + D x decode + merge")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample-tokens", type=int, default=64)
@@ -127,24 +135,33 @@ def algorithmic_units(step):
     return [int(v.sum().item()) for v in step.valid_count]
 
 
-def profile_traffic(workload: str):
-    """DRAM bytes per decode launch from a committed ncu summary, if that
-    summary was taken on the decode kernel source as it is now."""
-    path = os.path.join(ROOT, "profiles", f"sparse_mla_decode_{workload}.json")
-    if not os.path.exists(path):
-        return None
-    with open(path) as f:
-        prof = json.load(f)
+def decode_source_sha256() -> str:
     h = hashlib.sha256()
     for src in DECODE_SOURCES:
-        p = os.path.join(ROOT, src)
-        if not os.path.exists(p):
-            return None
-        with open(p, "rb") as g:
+        with open(os.path.join(ROOT, src), "rb") as g:
             h.update(g.read())
-    if prof.get("source_sha256") != h.hexdigest():
+    return h.hexdigest()
+
+
+def profile_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary
+    profiles/<kernel>_<workload>.md, if that summary was taken on the decode
+    source as it is now (its `source_sha256:` line); else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
         return None
-    return prof.get("dram_bytes_per_launch")
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            m = re.match(r"^\s*-?\s*`?([a-z_0-9]+)`?\s*:\s*`?([^`\s]+)`?", line)
+            if m:
+                fields.setdefault(m.group(1), m.group(2))
+    if fields.get("source_sha256") != decode_source_sha256():
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 def cpu_baseline(wl, sample_tokens: int):
@@ -173,7 +190,97 @@ def cpu_baseline(wl, sample_tokens: int):
                       f"(convert + decode) + merge, float64 numpy; {dt:.2f} s"}
 
 
+# ------------------------------------------------------------ multi-rank
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a per-rank float over the default process group (identity when
+    no group is initialised)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(tokens_per_step: int, steps: int, total_ms_this_rank: float,
+                         world: int, device=None):
+    """Whole-job value: every rank processed `tokens_per_step * steps` query
+    tokens; the job took the slowest rank's time.  Returns (value, ms_per_step)."""
+    total_ms = max_over_ranks(total_ms_this_rank, device)
+    return world * tokens_per_step * steps / (total_ms / 1e3), total_ms / steps
+
+
 # ------------------------------------------------------------ GPU arm
+def _timed_steps(fn, n, flush, stream):
+    """Per-step device times (ms) of `fn`, L2 flushed before each step
+    outside the step's CUDA events."""
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for i in range(n):
+        flush.fill_(1)
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)]
+
+
+def _pipeline_decode_ms(step, wl, n, flush, stream):
+    """Per-launch times of the per-shard decode kernel inside the 2D+1 launch
+    pipeline (events on the launching stream around each decode launch)."""
+    import torch
+
+    from sparse_mla_decode_dcp_gb300 import capi
+    D = wl.D
+    out = []
+    for _ in range(n):
+        flush.fill_(1)
+        evs = []
+        for d in range(D):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            capi.dcp_filter_convert_index(
+                step.req_id, step.block_tables[d], step.topk, D, d, wl.spec.block_size,
+                bt_width=step.bt_widths[d], local_slots=step.local_slots[d],
+                valid_count=step.valid_count[d])
+            ev[0].record(stream)
+            capi.sparse_mla_decode(step.q, step.pools[d], step.local_slots[d], wl.spec.sm_scale,
+                                   out=step.part_out[d], lse=step.part_lse[d],
+                                   workspace=step.workspace)
+            ev[1].record(stream)
+            evs.append(ev)
+        capi.dcp_lse_merge(step.part_out, step.part_lse, out=step.out, lse=step.lse)
+        torch.cuda.synchronize()
+        out.append([a.elapsed_time(b) for a, b in evs])
+    return np.array(out)  # [n, D]
+
+
+def _roofline(kernel, launch_ms, keys_per_launch, H, peaks, workload):
+    flop_per_key = 2.0 * H * (QK_DIM + V_DIM)
+    flops = flop_per_key * keys_per_launch
+    nbytes = ROW_BYTES * keys_per_launch
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if flop_per_key / ROW_BYTES >= ridge:
+        roof = {"bound": "tensor", "achieved": flops / (launch_ms * 1e-3) / 1e12,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": nbytes / (launch_ms * 1e-3) / 1e9,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = profile_traffic(kernel, workload)
+    roof.update({
+        "kernel": kernel,
+        "peak_source": f"{peaks['source']} MEASURED_PEAKS.json burst figure"
+                       + ("; fp16 MMA nominal rate = bf16" if roof["bound"] == "tensor" else ""),
+        "launch_us": launch_ms * 1e3,
+        "algorithmic_flops_per_launch": flops,
+        "algorithmic_bytes_per_launch": nbytes,
+        "achieved_hbm_gbs": nbytes / (launch_ms * 1e-3) / 1e9,
+    })
+    return roof
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -194,65 +301,55 @@ def run_gpu(args):
     units = algorithmic_units(step)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     T, H, K, D = wl.T, wl.H, wl.K, wl.D
+    paths = {"fused": (step.run_fused, 1), "pipeline": (step.run, step.launches_per_step)}
+    main_fn, main_launches = paths[args.path]
+    alt_name = "pipeline" if args.path == "fused" else "fused"
+    alt_fn, _ = paths[alt_name]
 
     for _ in range(max(args.warmup, 3)):
         flush.fill_(1)
-        step.run()
+        main_fn()
+        flush.fill_(1)
+        alt_fn()
     torch.cuda.synchronize()
 
-    # Per-kernel pass: CUDA events around every decode launch (on the
-    # launching stream), used only for the roofline of the dominant kernel.
-    n_kern = max(10, min(args.steps, 50))
-    dec_ms = []
-    for _ in range(n_kern):
-        flush.fill_(1)
-        evs = []
-        for d in range(D):
-            step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-            capi.dcp_filter_convert_index(
-                step.req_id, step.block_tables[d], step.topk, D, d, wl.spec.block_size,
-                bt_width=step.bt_widths[d], local_slots=step.local_slots[d],
-                valid_count=step.valid_count[d])
-            step_ev[0].record(stream)
-            capi.sparse_mla_decode(step.q, step.pools[d], step.local_slots[d], wl.spec.sm_scale,
-                                   out=step.part_out[d], lse=step.part_lse[d],
-                                   workspace=step.workspace)
-            step_ev[1].record(stream)
-            evs.append(step_ev)
-        capi.dcp_lse_merge(step.part_out, step.part_lse, out=step.out, lse=step.lse)
-        torch.cuda.synchronize()
-        dec_ms.append([a.elapsed_time(b) for a, b in evs])
-    dec_ms = np.array(dec_ms)  # [iters, D]
-
-    # Timed region: exactly `steps` steps, each bracketed by its own events,
-    # L2 flushed before each step outside the events.
+    # Timed region: exactly `steps` steps of the reported path.
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.25)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.fill_(1)
-        starts[i].record(stream)
-        step.run()
-        ends[i].record(stream)
-    torch.cuda.synchronize()
+    step_ms = _timed_steps(main_fn, args.steps, flush, stream)
     wall = time.perf_counter() - wall0
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    total_ms = float(sum(step_ms))
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
-    value = world * T * args.steps / (total_ms / 1e3)
+    value, ms_per_step = aggregate_throughput(T, args.steps, float(sum(step_ms)), world, dev)
+
+    # The other form of the same step, and per-launch decode times.
+    n_aux = max(10, min(args.steps, 50))
+    alt_ms = float(np.mean(_timed_steps(alt_fn, n_aux, flush, stream)))
+    dec_ms = _pipeline_decode_ms(step, wl, n_aux, flush, stream)
+    total_keys = sum(units)
+    peaks = load_peaks()
+    if args.path == "fused":
+        roof = _roofline("smla_dcp_sparse_mla_decode_fused", ms_per_step, total_keys, H, peaks,
+                         args.workload)
+        roof["launches_per_step"] = 1
+    else:
+        roof = _roofline("smla_sparse_mla_decode", float(dec_ms.mean()), total_keys / D, H, peaks,
+                         args.workload)
+        roof["launches_per_step"] = D
+    roof["valid_slots_per_shard"] = units
+    roof["roofline_us_per_step"] = max(
+        2.0 * H * (QK_DIM + V_DIM) * total_keys / (peaks["bf16_tflops"] * 1e12),
+        ROW_BYTES * total_keys / (peaks["hbm_gbs"] * 1e9)) * 1e6
+    pipeline_ms = alt_ms if args.path == "fused" else ms_per_step
+    fused_ms = ms_per_step if args.path == "fused" else alt_ms
+    per_shard_roof = _roofline("smla_sparse_mla_decode", float(dec_ms.mean()), total_keys / D, H,
+                               peaks, args.workload)
 
     # End to end through the public API with host buffers: every step copies
     # q and the top-k ids from pinned host memory and reads out + lse back.
@@ -262,68 +359,40 @@ def run_gpu(args):
     lse_host = torch.empty(step.lse.shape, dtype=step.lse.dtype).pin_memory()
     h2d = q_host.numel() * q_host.element_size() + topk_host.numel() * 4
     d2h = out_host.numel() * out_host.element_size() + lse_host.numel() * 4
-    e2e_steps = max(3, min(args.steps, 100))
-    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
-    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
-    for i in range(e2e_steps):
-        flush.fill_(1)
-        e_s[i].record(stream)
+
+    def e2e_step():
         step.q.copy_(q_host, non_blocking=True)
         step.topk.copy_(topk_host, non_blocking=True)
-        step.run()
+        main_fn()
         out_host.copy_(step.out, non_blocking=True)
         lse_host.copy_(step.lse, non_blocking=True)
-        e_e[i].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e_s, e_e)) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
 
-    peaks = load_peaks()
-    flop_per_key = 2.0 * H * (QK_DIM + V_DIM)
-    total_keys = sum(units)
-    dec_launch_ms = float(dec_ms.mean())
-    flops_per_launch = flop_per_key * total_keys / D
-    bytes_per_launch = ROW_BYTES * total_keys / D
-    ai = flop_per_key / ROW_BYTES
-    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    if ai >= ridge:
-        roof = {"bound": "tensor", "achieved": flops_per_launch / (dec_launch_ms * 1e-3) / 1e12,
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
-    else:
-        roof = {"bound": "hbm", "achieved": bytes_per_launch / (dec_launch_ms * 1e-3) / 1e9,
-                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = profile_traffic(args.workload)
-    roof.update({
-        "kernel": "smla_sparse_mla_decode",
-        "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json burst; fp16 MMA nominal = bf16)",
-        "launch_us": dec_launch_ms * 1e3,
-        "launches_per_step": D,
-        "algorithmic_flops_per_launch": flops_per_launch,
-        "algorithmic_bytes_per_launch": bytes_per_launch,
-        "valid_slots_per_shard": units,
-        "roofline_us_per_step": max(flop_per_key * total_keys / (peaks["bf16_tflops"] * 1e12),
-                                    ROW_BYTES * total_keys / (peaks["hbm_gbs"] * 1e9)) * 1e6,
-    })
-    roof["frac_of_step_decode_time"] = roof["roofline_us_per_step"] / (dec_ms.sum(axis=1).mean() * 1e3)
+    e2e_ms = max_over_ranks(
+        float(np.mean(_timed_steps(e2e_step, max(3, min(args.steps, 100)), flush, stream))), dev)
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic",
-        "config": {"workload": args.workload, "T": T, "H": H, "K": K, "D": D,
+        "dtype": "f16xf16->f32 (MMA), f32 softmax", "data": "synthetic",
+        "config": {"workload": args.workload, "path": args.path, "T": T, "H": H, "K": K, "D": D,
                    "block_size": wl.spec.block_size, "requests": wl.spec.num_reqs,
                    "cached_tokens": int(sum(int(c) for c in wl.ctx)),
                    "l2": "flushed before every step (256 MiB write, outside the events)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU, D shards simulated"},
+                   "parallelism": f"replicas x{world}" if world > 1 else
+                                  "single GPU, D shards simulated as D pools"},
         "roofline": roof,
+        "paths": {
+            "fused": {"ms_per_step": fused_ms, "value": world * T / (fused_ms * 1e-3),
+                      "launches_per_step": 1},
+            "pipeline": {"ms_per_step": pipeline_ms, "value": world * T / (pipeline_ms * 1e-3),
+                         "launches_per_step": step.launches_per_step,
+                         "decode_launch_us": [float(x) * 1e3 for x in dec_ms.mean(axis=0)],
+                         "decode_roofline": per_shard_roof},
+        },
         "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps * step.launches_per_step,
+        "gpu_launches": args.steps * main_launches,
         "clocks": clocks,
         "wall_s_timed": wall,
     }

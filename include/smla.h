@@ -161,6 +161,43 @@ smla_status smla_sparse_mla_decode(
     size_t workspace_bytes, void* stream);
 
 /*
+ * Steps 1-3 in one launch (fused DCP step for D shards held by one GPU).
+ *
+ * Computes exactly what the three calls above compute for D shard pools --
+ * filter + convert per shard, sparse MLA decode per shard, LSE merge -- in a
+ * single kernel: the global-to-local conversion of "FlashMLA sparse fp8 path
+ * + DCP + MTP" (implementation breakdown step 2) runs in the kernel's
+ * prologue for every shard, the compacted keys of all shards share one online
+ * softmax, and since the LSE merge of per-shard softmax partials equals the
+ * softmax over the union of their keys ("[eldritch] attention: support DCP in
+ * SM120 FlashInfer sparse MLA", Why: the merge reduces partial attention
+ * results), the output is the merged (out, lse) directly.  A row whose ids
+ * all map to nothing is written as (0, -inf).
+ *
+ *   q, T, H, K, sm_scale, out, lse   as in smla_sparse_mla_decode (out/lse
+ *                                    receive the merged result)
+ *   req_id_per_token, topk_global, num_reqs, D, block_size
+ *                                    as in smla_dcp_filter_convert_index
+ *   kv_caches      host array of D device pointers, pool d = uint8
+ *                  [num_slots[d], 656], 16-byte aligned
+ *   num_slots      host array of D pool sizes
+ *   block_tables   host array of D device pointers, table d = int32
+ *                  [num_reqs, bt_row_strides[d]], columns [0, bt_widths[d])
+ *   workspace      >= smla_decode_workspace_size(T, H, K) bytes, same rules
+ *                  as for smla_sparse_mla_decode
+ * Errors: as the three calls above; UNSUPPORTED for D > SMLA_MAX_DCP.
+ * Device-side input errors (ids past a block table, bad request ids, slots
+ * past a pool) drop the entry and set the device error word.
+ */
+smla_status smla_dcp_sparse_mla_decode_fused(
+    const uint16_t* q, int32_t T, int32_t H, int32_t K, float sm_scale,
+    const int32_t* req_id_per_token, const int32_t* topk_global, int32_t num_reqs,
+    int32_t D, int32_t block_size, const uint8_t* const* kv_caches,
+    const int64_t* num_slots, const int32_t* const* block_tables,
+    const int64_t* bt_row_strides, const int32_t* bt_widths, uint16_t* out,
+    float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Step 3 -- LSE-weighted merge of D partials [P1 Why, Scope / Limitations
  * (the ag_rs flow); P3 executive summary 1 and implementation breakdown
  * step 3].  With M = max_d lse_d[t,h]:

@@ -46,6 +46,9 @@ SIGNATURES = {
     "smla_sparse_mla_decode": (ctypes.c_int, [
         _c_vp, _c_vp, _c_i64, _c_vp, _c_i32, _c_i32, _c_i32, ctypes.c_float, _c_vp,
         _c_vp, _c_vp, _c_sz, _c_vp]),
+    "smla_dcp_sparse_mla_decode_fused": (ctypes.c_int, [
+        _c_vp, _c_i32, _c_i32, _c_i32, ctypes.c_float, _c_vp, _c_vp, _c_i32, _c_i32, _c_i32,
+        _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]),
     "smla_dcp_lse_merge": (ctypes.c_int, [
         _c_vp, _c_vp, _c_i32, _c_i32, _c_i32, _c_vp, _c_vp, _c_vp]),
 }
@@ -185,6 +188,60 @@ def sparse_mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, local_slots: torc
         T, H, K, float(sm_scale), out.data_ptr(), lse.data_ptr(), ws_ptr, ws_bytes,
         _stream_ptr(stream, dev))
     _check("smla_sparse_mla_decode", st)
+    return out, lse
+
+
+def dcp_sparse_mla_decode_fused(q: torch.Tensor, req_id_per_token: torch.Tensor,
+                                topk_global: torch.Tensor, kv_caches: Sequence[torch.Tensor],
+                                block_tables: Sequence[torch.Tensor], block_size: int,
+                                sm_scale: float, *, bt_widths: Optional[Sequence[int]] = None,
+                                out: Optional[torch.Tensor] = None,
+                                lse: Optional[torch.Tensor] = None,
+                                workspace: Optional[torch.Tensor] = None,
+                                stream: Optional[torch.cuda.Stream] = None
+                                ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Filter+convert, decode and merge of D shards in one launch; returns the
+    merged (out, lse)."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev)
+    _need(req_id_per_token, "req_id_per_token", torch.int32, dev)
+    _need(topk_global, "topk_global", torch.int32, dev)
+    D = len(kv_caches)
+    if D != len(block_tables) or D < 1:
+        raise ValueError("need one block table per KV pool (>= 1)")
+    T, H, Dq = q.shape
+    K = topk_global.shape[1]
+    if Dq != QK_DIM or topk_global.shape[0] != T:
+        raise ValueError("q must be [T, H, 576] and topk [T, K]")
+    num_reqs = None
+    for kv, bt in zip(kv_caches, block_tables):
+        _need(kv, "kv_caches[d]", torch.uint8, dev)
+        if kv.dim() != 2 or kv.shape[1] != ROW_BYTES:
+            raise ValueError(f"kv_caches[d] must be [num_slots, {ROW_BYTES}] uint8")
+        if bt.dtype != torch.int32 or bt.device != dev or bt.dim() != 2 or bt.stride(1) != 1:
+            raise ValueError("block_tables[d] must be 2-D int32 with contiguous rows")
+        num_reqs = bt.shape[0] if num_reqs is None else min(num_reqs, bt.shape[0])
+    if out is None:
+        out = torch.empty((T, H, V_DIM), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, dev)
+    _need(lse, "lse", torch.float32, dev)
+    if workspace is None:
+        workspace = alloc_decode_workspace(T, H, K, dev)
+    widths = [bt.shape[1] for bt in block_tables] if bt_widths is None else list(bt_widths)
+    pools = (ctypes.c_void_p * D)(*[kv.data_ptr() for kv in kv_caches])
+    nslots = (ctypes.c_int64 * D)(*[kv.shape[0] for kv in kv_caches])
+    bts = (ctypes.c_void_p * D)(*[bt.data_ptr() for bt in block_tables])
+    strides = (ctypes.c_int64 * D)(*[bt.stride(0) for bt in block_tables])
+    wids = (ctypes.c_int32 * D)(*widths)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().smla_dcp_sparse_mla_decode_fused(
+        q.data_ptr(), T, H, K, float(sm_scale), req_id_per_token.data_ptr(),
+        topk_global.data_ptr(), num_reqs, D, block_size, pools, nslots, bts, strides, wids,
+        out.data_ptr(), lse.data_ptr(), ws_ptr, ws_bytes, _stream_ptr(stream, dev))
+    _check("smla_dcp_sparse_mla_decode_fused", st)
     return out, lse
 
 

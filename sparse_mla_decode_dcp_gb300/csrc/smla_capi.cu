@@ -95,7 +95,7 @@ smla_status smla_sparse_mla_decode(
   if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
                    misaligned(workspace, 256)))
     return SMLA_ERR_WORKSPACE;
-  smla::DecodeArgs a;
+  smla::DecodeArgs a{};
   a.q = q;
   a.kv = kv_cache;
   a.num_slots = num_slots;
@@ -109,6 +109,57 @@ smla_status smla_sparse_mla_decode(
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
   return from_cuda(smla::launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+smla_status smla_dcp_sparse_mla_decode_fused(
+    const uint16_t* q, int32_t T, int32_t H, int32_t K, float sm_scale,
+    const int32_t* req_id_per_token, const int32_t* topk_global, int32_t num_reqs,
+    int32_t D, int32_t block_size, const uint8_t* const* kv_caches,
+    const int64_t* num_slots, const int32_t* const* block_tables,
+    const int64_t* bt_row_strides, const int32_t* bt_widths, uint16_t* out,
+    float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (T < 0 || K < 1 || H < 1 || D < 1 || block_size < 1 || num_reqs < 1 ||
+      !std::isfinite(sm_scale))
+    return SMLA_ERR_INVALID_ARG;
+  if (H > SMLA_MAX_HEADS || D > SMLA_MAX_DCP) return SMLA_ERR_UNSUPPORTED;
+  if (T == 0) return SMLA_OK;
+  if (!q || !req_id_per_token || !topk_global || !out || !lse || !kv_caches ||
+      !num_slots || !block_tables || !bt_row_strides || !bt_widths)
+    return SMLA_ERR_INVALID_ARG;
+  if (misaligned(q, 16) || misaligned(out, 16) || misaligned(lse, 4) ||
+      misaligned(req_id_per_token, 4) || misaligned(topk_global, 4))
+    return SMLA_ERR_INVALID_ARG;
+  smla::DecodeArgs a{};
+  for (int d = 0; d < D; ++d) {
+    if (!kv_caches[d] || misaligned(kv_caches[d], 16) || num_slots[d] < 0 ||
+        !block_tables[d] || misaligned(block_tables[d], 4) || bt_widths[d] < 1 ||
+        bt_row_strides[d] < bt_widths[d])
+      return SMLA_ERR_INVALID_ARG;
+    a.pools[d] = kv_caches[d];
+    a.pool_slots[d] = num_slots[d];
+    a.bts[d] = block_tables[d];
+    a.bt_stride[d] = bt_row_strides[d];
+    a.bt_width[d] = bt_widths[d];
+  }
+  const size_t need = smla::decode_workspace_bytes(T, H, K);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
+                   misaligned(workspace, 256)))
+    return SMLA_ERR_WORKSPACE;
+  a.q = q;
+  a.T = T;
+  a.H = H;
+  a.K = K;
+  a.sm_scale = sm_scale;
+  a.out = out;
+  a.lse = lse;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.D = D;
+  a.block_size = block_size;
+  a.num_reqs = num_reqs;
+  a.req_id = req_id_per_token;
+  a.topk = topk_global;
+  return from_cuda(smla::launch_decode_fused(a, static_cast<cudaStream_t>(stream)));
 }
 
 smla_status smla_dcp_lse_merge(const uint16_t* const* outs,

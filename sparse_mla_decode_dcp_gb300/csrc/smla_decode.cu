@@ -1,0 +1,823 @@
+// Sparse MLA decode over the packed fp8_ds_mla cache on tcgen05 tensor cores.
+//
+// What it computes ("FlashMLA sparse fp8 path + DCP + MTP", implementation
+// breakdown steps 1 and 3; "[eldritch] attention: support DCP in SM120
+// FlashInfer sparse MLA", Why): for query row t and head h, over the valid
+// local slots j of row t,
+//     s_j = sm_scale * <q[t,h,0:576], (latent_j || rope_j)>
+//     lse = ln sum_j exp(s_j),   out = sum_j exp(s_j - lse) * latent_j
+// with latent_j = e4m3(code) * scale[dim / 128].  A row with no valid slot is
+// written as the merge identity (out = 0, lse = -inf).
+//
+// Design (GB300, one cluster of two CTAs per query row):
+//   * Heads are the MMA M dimension (M = 128, heads padded with zero rows),
+//     so the 576-wide latent keys are shared by all heads (MQA-style).
+//   * The fp32 accumulator O[128 x 512] alone fills a whole SM's tensor
+//     memory, so CTA c of the pair owns value dims [256c, 256c + 256).  The
+//     QK^T contraction is split by key dimension the same way: CTA 0 does
+//     latent dims 0..255, CTA 1 latent dims 256..511 plus the 64 rope dims.
+//     The two fp32 partial score tiles are exchanged through distributed
+//     shared memory each tile, so no FLOP is recomputed and every cache byte
+//     is read once.  Both CTAs then run the identical online softmax.
+//   * Q (this CTA's key-dim half) and P live in tensor memory as the A
+//     operand; K/V tiles are the B operand in shared memory (128-byte
+//     swizzle): one buffer serves as K (K-major) for QK^T and as V
+//     (MN-major) for PV.
+//   * Keys are dequantised to fp16 with a single rounding: the e4m3 code is
+//     exact in fp16 and the fp32 scale is split into fp16 hi + lo parts, so
+//     code*hi + code*lo is rounded once by a fused multiply-add.  fp16 keeps
+//     3 more mantissa bits than bf16, which keeps score errors well inside
+//     the LSE tolerance even for rows with a single valid slot.
+//   * Valid slots are compacted in order in the prologue (-1 never costs a
+//     load or an MMA); rows are gathered with 16-byte cp.async into a
+//     two-stage raw buffer, so the gather of tile i+1 overlaps tile i.
+//   * Softmax in the log2 domain with a lazily moved reference maximum: the
+//     O accumulator in TMEM is rescaled only when the row maximum grows by
+//     more than 2^8.
+//
+// Warp roles (288 threads): warps 0-3 softmax/epilogue (TMEM lanes 0-127,
+// one head row per thread), warps 4-7 gather + dequantise, warp 8 allocates
+// TMEM and issues the MMAs (one thread).  Every wait is bounded; a wait that
+// runs out sets SMLA_DEVERR_TIMEOUT and the CTA unwinds.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "../../include/smla.h"
+#include "smla_internal.h"
+#include "smla_sm100.cuh"
+
+namespace smla {
+namespace {
+
+using namespace sm100;
+
+__device__ unsigned int g_decode_error;
+
+constexpr int kTileN = 64;        // keys per tile (MMA N of QK^T, K of PV)
+constexpr int kThreads = 288;     // 9 warps
+constexpr int kMmaWarp = 8;
+constexpr int kMaxList = 2048;    // compacted slots one cluster handles
+constexpr uint32_t kSpinLimit = 1u << 22;
+
+// tensor-memory columns (512 allocated)
+constexpr uint32_t kOCol = 0;     // O half: 256 fp32 columns
+constexpr uint32_t kSCol = 256;   // S tile: 64 fp32 columns
+constexpr uint32_t kPCol = 320;   // P tile: 64 fp16 = 32 columns
+constexpr uint32_t kQCol = 352;   // Q half: up to 320 fp16 = 160 columns
+constexpr uint32_t kTmemCols = 512;
+
+// shared-memory layout (offsets from a 1024-byte aligned base)
+constexpr int kKBlockBytes = kTileN * 128;          // 64 keys x 64 fp16
+constexpr int kOpTileBytes = 5 * kKBlockBytes;      // up to 320 key dims
+constexpr int kRawStride = 400;                     // raw bytes per key
+constexpr int kRawBytes = kTileN * kRawStride;
+constexpr int kXBytes = 128 * kTileN * 4;           // fp32 partial S tile
+constexpr int kOffOp = 0;
+constexpr int kOffRaw = kOffOp + 2 * kOpTileBytes;
+constexpr int kOffX = kOffRaw + 2 * kRawBytes;
+constexpr int kOffList = kOffX + 2 * kXBytes;
+constexpr int kOffListShard = kOffList + kMaxList * 4;  // fused step: shard of each key
+constexpr int kOffCtl = kOffListShard + kMaxList;
+constexpr int kSmemBytes = kOffCtl + 256 + 1024;    // + control block + alignment slack
+
+struct Ctl {
+  uint64_t q_ready, full[2], freed[2], s_full, s_free, p_full, pv_done, x[2], end;
+  uint32_t tbase;
+  int n_list;
+  int abort;
+  int is_last;
+  int warp_cnt[8];
+};
+static_assert(sizeof(Ctl) <= 256, "control block");
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  uint32_t it = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort || ++it > kSpinLimit) {
+      atomicOr(&g_decode_error, SMLA_DEVERR_TIMEOUT);
+      *abort = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ bool wait_bar_cluster(uint64_t* bar, uint32_t parity,
+                                                 volatile int* abort) {
+  uint32_t it = 0;
+  while (!mbar_try_wait_cluster(bar, parity)) {
+    if (*abort || ++it > kSpinLimit) {
+      atomicOr(&g_decode_error, SMLA_DEVERR_TIMEOUT);
+      *abort = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+// 8 bf16 -> 8 fp16 (exact for values in fp16 range)
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    o[k] = h2_bits(__floats2half2_rn(__uint_as_float(w[k] << 16),
+                                     __uint_as_float(w[k] & 0xffff0000u)));
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// 8 e4m3 codes -> 8 fp16 values code * (hi + lo), one rounding
+__device__ __forceinline__ uint4 e4m3x8_scaled(uint2 codes, __half2 hi, __half2 lo) {
+  const uint32_t w[2] = {codes.x, codes.y};
+  uint32_t o[4];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(
+          static_cast<__nv_fp8x2_storage_t>((w[k] >> (16 * p)) & 0xffffu), __NV_E4M3);
+      const __half2 c = *reinterpret_cast<const __half2*>(&r);
+      o[2 * k + p] = h2_bits(__hfma2(c, hi, __hmul2(c, lo)));
+    }
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Per-CTA constants of the two halves of the pair.
+template <int C>
+struct Half {
+  static constexpr int kKDims = C == 0 ? 256 : 320;      // QK^T key dims
+  static constexpr int kKSteps = kKDims / 16;             // MMA K = 16
+  static constexpr int kQCols = kKDims / 2;
+  static constexpr int kRawChunks = C == 0 ? 17 : 25;     // 16-byte chunks per key
+  static constexpr int kOutChunks = kKDims / 8;           // fp16 chunks per key
+  static constexpr int kQDim0 = C == 0 ? 0 : 256;         // first q dim
+};
+
+// Source offset (bytes within the 656-byte row) of raw chunk `ch`.  The raw
+// row keeps codes at [0,256), the four scales at [256,272) and (CTA 1) the
+// rope values at [272,400).
+template <int C>
+__device__ __forceinline__ int raw_src_offset(int ch) {
+  if (C == 0) return ch < 16 ? ch * 16 : 512;
+  return 256 + ch * 16;
+}
+
+template <int C, bool kFused>
+__device__ void issue_tile_loads(const DecodeArgs& a, const int* list, const uint8_t* shard,
+                                 int n, int tile, uint8_t* raw, int d) {
+  using HC = Half<C>;
+  const int k0 = tile * kTileN;
+  for (int q = d; q < kTileN * HC::kRawChunks; q += 128) {
+    const int key = q / HC::kRawChunks;
+    const int ch = q - key * HC::kRawChunks;
+    if (k0 + key < n) {
+      const uint8_t* pool = kFused ? a.pools[shard[k0 + key]] : a.kv;
+      const uint8_t* src = pool + int64_t(list[k0 + key]) * SMLA_ROW_BYTES + raw_src_offset<C>(ch);
+      cp_async_16(smem_u32(raw + key * kRawStride + ch * 16), src);
+    }
+  }
+}
+
+template <int C>
+__device__ void dequant_tile(const uint8_t* raw, uint8_t* op, int valid, int d) {
+  using HC = Half<C>;
+  const int key = d >> 1;
+  const int part = d & 1;
+  const int oc0 = part * (HC::kOutChunks / 2);
+  const int oc1 = oc0 + HC::kOutChunks / 2;
+  const uint8_t* row = raw + key * kRawStride;
+  const bool live = key < valid;
+  __half2 hi[2], lo[2];
+  if (live) {
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+      const float s = *reinterpret_cast<const float*>(row + 256 + 4 * (2 * C + g));
+      const __half h = __float2half_rn(s);
+      const __half l = __float2half_rn(s - __half2float(h));
+      hi[g] = __half2half2(h);
+      lo[g] = __half2half2(l);
+    }
+  }
+  for (int oc = oc0; oc < oc1; ++oc) {
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (live) {
+      if (oc < 32) {
+        const uint2 codes = *reinterpret_cast<const uint2*>(row + oc * 8);
+        const int g = oc >> 4;
+        v = e4m3x8_scaled(codes, hi[g], lo[g]);
+      } else {
+        v = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(row + 272 + (oc - 32) * 16));
+      }
+    }
+    const int kb = oc >> 3;
+    *reinterpret_cast<uint4*>(op + kb * kKBlockBytes + sw128_offset(key, oc & 7)) = v;
+  }
+}
+
+// Split-K epilogue: write this split's unnormalised O half, its log2-domain
+// reference maximum and its sum; the last split of the row to arrive (per
+// value half) combines all of them and resets the row's arrival counter.
+template <int C>
+__device__ void split_epilogue(const DecodeArgs& a, Ctl* ctl, int64_t t, int split, int ntiles,
+                               float m_ref, float l, uint32_t tb, int warp, int h) {
+  const int S = a.splits;
+  const bool live = h < a.H;
+  const int64_t row = (t * S + split) * a.H + (live ? h : 0);
+  float4* wo = reinterpret_cast<float4*>(a.ws_o + row * SMLA_V_DIM + C * 256);
+  if (ntiles > 0) {
+#pragma unroll 1
+    for (int cc = 0; cc < 8; ++cc) {
+      uint32_t r[32];
+      tmem_ld32(tmem_addr(tb, 32 * warp, kOCol + 32 * cc), r);
+      tmem_ld_wait();
+      if (live) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          wo[cc * 8 + k] = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                       __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+      }
+    }
+  }
+  float* ml = a.ws_ml + ((t * S + split) * 2 + C) * 2 * a.H;
+  if (live) {
+    ml[h] = (ntiles > 0) ? m_ref : -INFINITY;
+    ml[a.H + h] = (ntiles > 0) ? l : 0.f;
+  }
+  __threadfence();
+  named_bar_sync(2, 128);
+  if (h == 0) ctl->is_last = (atomicAdd(a.ws_tick + t * 2 + C, 1) == S - 1);
+  named_bar_sync(2, 128);
+  if (!ctl->is_last) return;
+  __threadfence();
+  if (live) {
+    float M = -INFINITY;
+    for (int sp = 0; sp < S; ++sp) {
+      const float* mls = a.ws_ml + ((t * S + sp) * 2 + C) * 2 * a.H;
+      const float ms = __ldcg(mls + h), ls = __ldcg(mls + a.H + h);
+      if (ls != 0.f && (ms > M || ms != ms)) M = ms;  // NaN propagates
+    }
+    uint4* dst = reinterpret_cast<uint4*>(a.out + (t * a.H + h) * SMLA_V_DIM + C * 256);
+    if (M == -INFINITY) {
+#pragma unroll 1
+      for (int k = 0; k < 32; ++k) dst[k] = make_uint4(0, 0, 0, 0);
+      if (C == 0) a.lse[t * a.H + h] = -INFINITY;
+    } else {
+      float L = 0.f;
+      for (int sp = 0; sp < S; ++sp) {
+        const float* mls = a.ws_ml + ((t * S + sp) * 2 + C) * 2 * a.H;
+        const float ls = __ldcg(mls + a.H + h);
+        if (ls != 0.f) L += ls * ex2(__ldcg(mls + h) - M);
+      }
+      const float invL = 1.f / L;
+#pragma unroll 1
+      for (int cc = 0; cc < 8; ++cc) {
+        float acc[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+        for (int sp = 0; sp < S; ++sp) {
+          const float* mls = a.ws_ml + ((t * S + sp) * 2 + C) * 2 * a.H;
+          const float ls = __ldcg(mls + a.H + h);
+          if (ls == 0.f) continue;
+          const float w = ex2(__ldcg(mls + h) - M) * invL;
+          const float4* src = reinterpret_cast<const float4*>(
+              a.ws_o + ((t * S + sp) * a.H + h) * SMLA_V_DIM + C * 256 + cc * 32);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float4 v = __ldcg(src + k);
+            acc[4 * k] = fmaf(w, v.x, acc[4 * k]);
+            acc[4 * k + 1] = fmaf(w, v.y, acc[4 * k + 1]);
+            acc[4 * k + 2] = fmaf(w, v.z, acc[4 * k + 2]);
+            acc[4 * k + 3] = fmaf(w, v.w, acc[4 * k + 3]);
+          }
+        }
+        uint32_t o[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          __nv_bfloat162 v = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
+          o[j] = *reinterpret_cast<uint32_t*>(&v);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          dst[cc * 4 + k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+      }
+      if (C == 0) a.lse[t * a.H + h] = (M + log2f(L)) * kLn2;
+    }
+  }
+  if (h == 0) a.ws_tick[t * 2 + C] = 0;
+}
+
+// Load this CTA's half of q[t, h, :] (bf16) into tensor memory as fp16
+// pairs (the A operand of QK^T), one head row per thread, two 64-dim chunks
+// of loads in flight at a time.
+template <int C>
+__device__ void load_q_to_tmem(const DecodeArgs& a, int64_t t, uint32_t tb, int warp, int h) {
+  using HC = Half<C>;
+  constexpr int kChunks = HC::kQCols / 32;  // 32 TMEM columns = 64 dims each
+  const bool live = h < a.H;
+  const uint4* qsrc = reinterpret_cast<const uint4*>(
+      a.q + (t * a.H + (live ? h : 0)) * SMLA_QK_DIM + HC::kQDim0);
+#pragma unroll 1
+  for (int c0 = 0; c0 < kChunks; c0 += 2) {
+    uint4 raw[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+      raw[k] = (live && c0 + (k >> 3) < kChunks) ? __ldg(qsrc + c0 * 8 + k) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      if (c0 + cc < kChunks) {
+        uint32_t qr[32];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 v = bf16x8_to_f16x8(raw[cc * 8 + k]);
+          qr[4 * k + 0] = v.x;
+          qr[4 * k + 1] = v.y;
+          qr[4 * k + 2] = v.z;
+          qr[4 * k + 3] = v.w;
+        }
+        tmem_st32(tmem_addr(tb, 32 * warp, kQCol + 32 * (c0 + cc)), qr);
+      }
+    }
+  }
+  tmem_st_wait();
+}
+
+template <int C, bool kFused>
+__device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, int64_t t, int split,
+                        uint32_t peer) {
+  using HC = Half<C>;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  volatile int* abort = &ctl->abort;
+  const int* list = reinterpret_cast<const int*>(sm + kOffList);
+  const uint8_t* list_shard = sm + kOffListShard;
+  const int n = ctl->n_list;
+  const int ntiles = (n + kTileN - 1) / kTileN;
+  const uint32_t tb = ctl->tbase;
+
+  if (warp < 4) {
+    // ------------------------------------------------ softmax + epilogue
+    const int h = tid;  // head row == TMEM lane
+    const float scale_log2 = a.sm_scale * kLog2e;
+    float m_ref = -INFINITY;  // log2-domain reference maximum
+    float l = 0.f;
+    uint8_t* xbase = sm + kOffX;
+    const uint32_t peer_x0 = map_to_cta(smem_u32(xbase), peer);
+    bool ok = true;
+    for (int i = 0; i < ntiles && ok; ++i) {
+      ok = __all_sync(0xffffffffu, wait_bar(&ctl->s_full, i & 1, abort));
+      if (!ok) break;
+      tc_fence_after();
+      float s[64];
+      {
+        uint32_t r[32];
+        tmem_ld32(tmem_addr(tb, 32 * warp, kSCol), r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) s[j] = __uint_as_float(r[j]);
+        tmem_ld32(tmem_addr(tb, 32 * warp, kSCol + 32), r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) s[32 + j] = __uint_as_float(r[j]);
+      }
+      tc_fence_before();
+      mbar_arrive(&ctl->s_free);
+      // exchange partial scores with the peer CTA
+      const int b = i & 1;
+      const uint32_t px = peer_x0 + b * kXBytes;
+#pragma unroll
+      for (int j4 = 0; j4 < 16; ++j4)
+        st_cluster_v4(px + (j4 * 128 + h) * 16, s[4 * j4], s[4 * j4 + 1], s[4 * j4 + 2],
+                      s[4 * j4 + 3]);
+      mbar_arrive_remote(&ctl->x[b], peer);
+      ok = __all_sync(0xffffffffu, wait_bar_cluster(&ctl->x[b], (i >> 1) & 1, abort));
+      if (!ok) break;
+      const float4* mine = reinterpret_cast<const float4*>(xbase + b * kXBytes);
+#pragma unroll
+      for (int j4 = 0; j4 < 16; ++j4) {
+        const float4 v = mine[j4 * 128 + h];
+        s[4 * j4] += v.x;
+        s[4 * j4 + 1] += v.y;
+        s[4 * j4 + 2] += v.z;
+        s[4 * j4 + 3] += v.w;
+      }
+      const int valid = min(kTileN, n - i * kTileN);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        s[j] = (j < valid) ? s[j] * scale_log2 : -INFINITY;
+        mx = fmaxf(mx, s[j]);
+      }
+      float alpha = 1.f;
+      bool rescale = false;
+      if (mx > m_ref + 8.f) {
+        alpha = ex2(m_ref - mx);  // 0 on the first tile
+        m_ref = mx;
+        rescale = (i > 0);
+      }
+      float sum = 0.f;
+      uint32_t pk[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float p0 = ex2(s[2 * j] - m_ref);
+        const float p1 = ex2(s[2 * j + 1] - m_ref);
+        sum += p0 + p1;
+        pk[j] = h2_bits(__floats2half2_rn(p0, p1));
+      }
+      l = l * alpha + sum;
+      if (i > 0) {
+        ok = __all_sync(0xffffffffu, wait_bar(&ctl->pv_done, (i - 1) & 1, abort));
+        if (!ok) break;
+        tc_fence_after();
+        if (rescale) {
+#pragma unroll 1
+          for (int cc = 0; cc < 8; ++cc) {
+            uint32_t r[32];
+            const uint32_t addr = tmem_addr(tb, 32 * warp, kOCol + 32 * cc);
+            tmem_ld32(addr, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+            tmem_st32(addr, r);
+          }
+        }
+      }
+      tmem_st32(tmem_addr(tb, 32 * warp, kPCol), pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&ctl->p_full);
+    }
+    // epilogue
+    if (ok && ntiles > 0) {
+      ok = __all_sync(0xffffffffu, wait_bar(&ctl->pv_done, (ntiles - 1) & 1, abort));
+      tc_fence_after();
+    }
+    if (ok && a.splits == 1) {
+      // tcgen05.ld is warp-collective: every lane loads, only live heads store
+      const bool live = h < a.H;
+      uint4* dst = reinterpret_cast<uint4*>(a.out + (t * a.H + (live ? h : 0)) * SMLA_V_DIM +
+                                            C * 256);
+      if (ntiles == 0) {
+        if (live) {
+#pragma unroll 1
+          for (int k = 0; k < 32; ++k) dst[k] = make_uint4(0, 0, 0, 0);
+        }
+      } else {
+        const float inv = 1.f / l;
+#pragma unroll 1
+        for (int cc = 0; cc < 8; ++cc) {
+          uint32_t r[32];
+          tmem_ld32(tmem_addr(tb, 32 * warp, kOCol + 32 * cc), r);
+          tmem_ld_wait();
+          uint32_t o[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(r[2 * j]) * inv,
+                                                     __uint_as_float(r[2 * j + 1]) * inv);
+            o[j] = *reinterpret_cast<uint32_t*>(&v);
+          }
+          if (live) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              dst[cc * 4 + k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+          }
+        }
+      }
+      if (C == 0 && live)
+        a.lse[t * a.H + h] = (ntiles == 0) ? -INFINITY : (m_ref + log2f(l)) * kLn2;
+    } else if (ok) {
+      split_epilogue<C>(a, ctl, t, split, ntiles, m_ref, l, tb, warp, h);
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------ gather + dequantise
+    const int d = tid - 128;
+    uint8_t* raw = sm + kOffRaw;
+    uint8_t* op = sm + kOffOp;
+    if (ntiles > 0) {
+      issue_tile_loads<C, kFused>(a, list, list_shard, n, 0, raw, d);
+      cp_async_commit();
+    }
+    for (int i = 0; i < ntiles; ++i) {
+      if (i + 1 < ntiles) {
+        issue_tile_loads<C, kFused>(a, list, list_shard, n, i + 1,
+                                    raw + ((i + 1) & 1) * kRawBytes, d);
+        cp_async_commit();
+        cp_async_wait<1>();
+      } else {
+        cp_async_wait<0>();
+      }
+      bool bad = (i >= 2) && !wait_bar(&ctl->freed[i & 1], ((i - 2) >> 1) & 1, abort);
+      if (named_bar_or(1, 128, bad || *abort)) break;  // raw tile i landed for all
+      dequant_tile<C>(raw + (i & 1) * kRawBytes, op + (i & 1) * kOpTileBytes,
+                      min(kTileN, n - i * kTileN), d);
+      fence_async_shared();
+      mbar_arrive(&ctl->full[i & 1]);
+      if (named_bar_or(1, 128, *abort != 0)) break;  // raw stage free for reuse
+    }
+    cp_async_wait<0>();
+  } else if (lane == 0) {
+    // ------------------------------------------------ MMA issue (one thread)
+    constexpr uint32_t idesc_qk = idesc_f16_f32(128, kTileN, false, false);
+    constexpr uint32_t idesc_pv = idesc_f16_f32(128, 256, false, true);
+    const uint32_t op0 = smem_u32(sm + kOffOp);
+    bool ok = wait_bar(&ctl->q_ready, 0, abort);
+    tc_fence_after();
+    for (int i = 0; ok && i <= ntiles; ++i) {
+      if (i < ntiles) {
+        if (!wait_bar(&ctl->full[i & 1], (i >> 1) & 1, abort)) break;
+        if (i > 0 && !wait_bar(&ctl->s_free, (i - 1) & 1, abort)) break;
+        tc_fence_after();
+        const uint32_t base = op0 + (i & 1) * kOpTileBytes;
+#pragma unroll
+        for (int k = 0; k < HC::kKSteps; ++k) {
+          const uint64_t bd = sdesc_sw128(base + (k >> 2) * kKBlockBytes + (k & 3) * 32, 16, 1024);
+          mma_ts(tb + kSCol, tb + kQCol + 8 * k, bd, idesc_qk, k > 0);
+        }
+        mma_commit(&ctl->s_full);
+      }
+      if (i > 0) {
+        const int j = i - 1;
+        if (!wait_bar(&ctl->p_full, j & 1, abort)) break;
+        tc_fence_after();
+        const uint32_t base = op0 + (j & 1) * kOpTileBytes;
+#pragma unroll
+        for (int k = 0; k < kTileN / 16; ++k) {
+          const uint64_t bd = sdesc_sw128(base + k * 2048, kKBlockBytes, 1024);
+          mma_ts(tb + kOCol, tb + kPCol + 8 * k, bd, idesc_pv, (j > 0 || k > 0));
+        }
+        mma_commit(&ctl->pv_done);
+        mma_commit(&ctl->freed[j & 1]);
+      }
+    }
+    // drain: every MMA issued above has completed before TMEM is released
+    // (waited on even after an abort, with its own bound)
+    mma_commit(&ctl->end);
+    int no_abort = 0;
+    wait_bar(&ctl->end, 0, &no_abort);
+  }
+}
+
+// Resolve entry j of row `row` to (slot, shard).  Per-shard launch: the
+// entry already is a local slot.  Fused DCP step: the entry is a global
+// position t, owned by shard t mod D at local position t div D (interleave
+// 1), then mapped through that shard's block table.  Returns false for -1 /
+// foreign / invalid entries (recording input errors in `err`).
+template <bool kFused>
+__device__ __forceinline__ bool resolve_entry(const DecodeArgs& a, int64_t row, int32_t req,
+                                              int j, int32_t& slot, int& shard, unsigned& err) {
+  if (!kFused) {
+    const int32_t v = a.slots[row * a.K + j];
+    if (v >= a.num_slots) {
+      err |= SMLA_DEVERR_SLOT_RANGE;
+      return false;
+    }
+    slot = v;
+    shard = 0;
+    return v >= 0;
+  }
+  const int32_t tk = a.topk[row * a.K + j];
+  if (tk < 0 || req < 0) return false;
+  const int d = tk % a.D;
+  const int32_t lp = tk / a.D;
+  const int32_t col = lp / a.block_size;
+  if (col >= a.bt_width[d]) {
+    err |= SMLA_DEVERR_BLOCK_TABLE;
+    return false;
+  }
+  const int32_t blk = __ldg(a.bts[d] + req * a.bt_stride[d] + col);
+  if (blk < 0) {
+    err |= SMLA_DEVERR_BLOCK_TABLE;
+    return false;
+  }
+  const int64_t s64 = int64_t(blk) * a.block_size + (lp - col * a.block_size);
+  if (s64 >= a.pool_slots[d]) {
+    err |= SMLA_DEVERR_SLOT_RANGE;
+    return false;
+  }
+  slot = int32_t(s64);
+  shard = d;
+  return true;
+}
+
+template <bool kFused>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    sparse_mla_decode_kernel(const __grid_constant__ DecodeArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Ctl* ctl = reinterpret_cast<Ctl*>(sm + kOffCtl);
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const uint32_t c = cluster_ctarank();
+  const uint32_t peer = c ^ 1u;
+  const int64_t item = blockIdx.x >> 1;
+  const int64_t t = item / a.splits;
+  const int split = int(item - t * a.splits);
+  const int per_split = (a.K + a.splits - 1) / a.splits;
+  const int e_begin = split * per_split;
+  const int e_end = min(a.K, e_begin + per_split);
+
+  if (warp == kMmaWarp) {
+    tmem_alloc(&ctl->tbase, kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&ctl->q_ready, 128);
+    mbar_init(&ctl->full[0], 128);
+    mbar_init(&ctl->full[1], 128);
+    mbar_init(&ctl->freed[0], 1);
+    mbar_init(&ctl->freed[1], 1);
+    mbar_init(&ctl->s_full, 1);
+    mbar_init(&ctl->s_free, 128);
+    mbar_init(&ctl->p_full, 128);
+    mbar_init(&ctl->pv_done, 1);
+    mbar_init(&ctl->x[0], 128);
+    mbar_init(&ctl->x[1], 128);
+    mbar_init(&ctl->end, 1);
+    ctl->abort = 0;
+    fence_mbar_init_cluster();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (warp < 4) {
+    // Q half -> TMEM, overlapping the compaction below
+    if (c == 0)
+      load_q_to_tmem<0>(a, t, ctl->tbase, warp, tid);
+    else
+      load_q_to_tmem<1>(a, t, ctl->tbase, warp, tid);
+    tc_fence_before();
+    mbar_arrive(&ctl->q_ready);
+  } else if (warp < 8) {
+    // Ordered compaction of the split's valid entries: thread d owns the
+    // contiguous entries [e_begin + 16d, e_begin + 16d + 16), resolves them
+    // with all loads in flight at once, and a block scan gives each thread
+    // its output offset.  Both CTAs of the pair build the same list, so
+    // their tiles hold the same keys.
+    const int d = tid - 128;
+    int* list = reinterpret_cast<int*>(sm + kOffList);
+    uint8_t* list_shard = sm + kOffListShard;
+    constexpr int kPer = kMaxList / 128;
+    unsigned err = 0;
+    int32_t req = 0;
+    if (kFused) {
+      req = a.req_id[t];
+      if (req < 0 || req >= a.num_reqs) {
+        if (d == 0) err |= SMLA_DEVERR_REQ_ID;
+        req = -1;
+      }
+    }
+    const int j0 = e_begin + d * kPer;
+    int32_t vs[kPer];
+    int shards[kPer];
+    unsigned keep = 0;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      vs[k] = -1;
+      shards[k] = 0;
+      if (j0 + k < e_end && resolve_entry<kFused>(a, t, req, j0 + k, vs[k], shards[k], err))
+        keep |= 1u << k;
+    }
+    const int cnt = __popc(keep);
+    int incl = cnt;  // inclusive warp scan
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    if (lane == 31) ctl->warp_cnt[warp - 4] = incl;
+    named_bar_sync(3, 128);
+    int wbase = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const int x = ctl->warp_cnt[w];
+      wbase += (w < warp - 4) ? x : 0;
+      total += x;
+    }
+    int pos = wbase + incl - cnt;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      if (keep & (1u << k)) {
+        list[pos] = vs[k];
+        list_shard[pos] = uint8_t(shards[k]);
+        ++pos;
+      }
+    }
+    if (d == 0) ctl->n_list = total;
+    if (err) atomicOr(&g_decode_error, err);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // peer barriers initialised before any remote arrive
+  tc_fence_after();
+
+  if (c == 0)
+    run_cta<0, kFused>(a, sm, ctl, t, split, peer);
+  else
+    run_cta<1, kFused>(a, sm, ctl, t, split, peer);
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peer no longer writes into this CTA's shared memory
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(ctl->tbase, kTmemCols);
+  }
+}
+
+// Split-K policy, a function of the shape alone: enough clusters to cover the
+// GB300's 76 SM pairs when there are few query rows, at least 256 top-k
+// entries per split, and at most kMaxList entries per split.
+constexpr int kClusterSlots = 76;
+
+int decode_splits(int32_t T, int32_t K) {
+  int s = (T > 0) ? kClusterSlots / T : 1;
+  s = min(s, (K + 255) / 256);
+  s = max(s, (K + kMaxList - 1) / kMaxList);
+  return max(s, 1);
+}
+
+struct WsLayout {
+  size_t o_off, ml_off, tick_off, total;
+};
+
+WsLayout ws_layout(int32_t T, int32_t H, int32_t K) {
+  WsLayout w{0, 0, 0, 0};
+  const int S = decode_splits(T, K);
+  if (S == 1 || T <= 0) return w;
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  w.o_off = 0;
+  w.ml_off = up(size_t(T) * S * H * SMLA_V_DIM * sizeof(float));
+  w.tick_off = w.ml_off + up(size_t(T) * S * 2 * 2 * H * sizeof(float));
+  w.total = w.tick_off + up(size_t(T) * 2 * sizeof(int32_t));
+  return w;
+}
+
+}  // namespace
+
+size_t decode_workspace_bytes(int32_t T, int32_t H, int32_t K) {
+  return ws_layout(T, H, K).total;
+}
+
+namespace {
+
+template <bool kFused>
+cudaError_t launch_impl(const DecodeArgs& args, cudaStream_t s) {
+  DecodeArgs a = args;
+  a.splits = decode_splits(a.T, a.K);
+  const WsLayout w = ws_layout(a.T, a.H, a.K);
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  a.ws_o = w.total ? reinterpret_cast<float*>(ws + w.o_off) : nullptr;
+  a.ws_ml = w.total ? reinterpret_cast<float*>(ws + w.ml_off) : nullptr;
+  a.ws_tick = w.total ? reinterpret_cast<int32_t*>(ws + w.tick_off) : nullptr;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static bool attr_done[64] = {};
+  if (dev < 64 && !attr_done[dev]) {
+    e = cudaFuncSetAttribute(sparse_mla_decode_kernel<kFused>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  const int64_t ctas = 2 * int64_t(a.T) * a.splits;
+  sparse_mla_decode_kernel<kFused><<<dim3(unsigned(ctas)), dim3(kThreads), kSmemBytes, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) { return launch_impl<false>(a, s); }
+
+cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s) {
+  return launch_impl<true>(a, s);
+}
+
+cudaError_t decode_error_word(uint32_t* flags, bool clear) {
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_decode_error, sizeof(v));
+  if (e != cudaSuccess) return e;
+  *flags |= v;
+  if (clear) {
+    v = 0;
+    e = cudaMemcpyToSymbol(g_decode_error, &v, sizeof(v));
+  }
+  return e;
+}
+
+}  // namespace smla

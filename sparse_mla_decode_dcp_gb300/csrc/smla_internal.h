@@ -20,6 +20,8 @@ struct IndexArgs {
   int32_t* valid_count;  // may be null
 };
 
+constexpr int kMaxMerge = 16;
+
 struct DecodeArgs {
   const uint16_t* q;  // bf16 [T, H, 576]
   const uint8_t* kv;  // [num_slots, 656]
@@ -31,9 +33,22 @@ struct DecodeArgs {
   float* lse;     // [T, H]
   void* workspace;
   size_t workspace_bytes;
+  // filled by the launcher from the workspace (split-K partials)
+  int32_t splits;
+  float* ws_o;       // [T, splits, H, 512] unnormalised partial O
+  float* ws_ml;      // [T, splits, 2 halves, 2, H]: log2-domain max, then sum
+  int32_t* ws_tick;  // [T, 2] arrival counters, left at zero by every call
+  // Fused DCP step only (D > 0): global top-k ids are converted per shard in
+  // the kernel prologue and all shards' keys share one softmax.
+  int32_t D, block_size, num_reqs;
+  const int32_t* req_id;
+  const int32_t* topk;
+  const uint8_t* pools[kMaxMerge];
+  int64_t pool_slots[kMaxMerge];
+  const int32_t* bts[kMaxMerge];
+  int64_t bt_stride[kMaxMerge];
+  int32_t bt_width[kMaxMerge];
 };
-
-constexpr int kMaxMerge = 16;
 
 struct MergeArgs {
   const uint16_t* outs[kMaxMerge];
@@ -45,6 +60,7 @@ struct MergeArgs {
 
 cudaError_t launch_filter_convert(const IndexArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s);
 size_t decode_workspace_bytes(int32_t T, int32_t H, int32_t K);
 

@@ -56,6 +56,14 @@ class DcpDecodeStep:
             out=self.part_out[d], lse=self.part_lse[d], workspace=self.workspace,
             stream=self.stream)
 
+    def run_fused(self):
+        """The same step in one launch (conversion, decode and merge fused)."""
+        wl = self.wl
+        return capi.dcp_sparse_mla_decode_fused(
+            self.q, self.req_id, self.topk, self.pools, self.block_tables,
+            wl.spec.block_size, wl.spec.sm_scale, bt_widths=self.bt_widths,
+            out=self.out, lse=self.lse, workspace=self.workspace, stream=self.stream)
+
     def run(self):
         for d in range(self.wl.D):
             self.run_shard(d)

@@ -32,6 +32,7 @@ def test_header_declares_the_three_path_calls():
     names = _declared_functions()
     for n in ("smla_dcp_filter_convert_index", "smla_sparse_mla_decode",
               "smla_dcp_lse_merge", "smla_decode_workspace_size",
+              "smla_dcp_sparse_mla_decode_fused",
               "smla_status_string", "smla_get_device_error"):
         assert n in names
 
@@ -139,6 +140,51 @@ def test_workspace_size_shape_only(lib):
     assert capi.decode_workspace_size(64, 128, 2048) == capi.decode_workspace_size(64, 128, 2048)
     # monotone in T
     assert capi.decode_workspace_size(128, 128, 2048) >= capi.decode_workspace_size(64, 128, 2048)
+
+
+def _fused(lib, D=2, **kw):
+    a = dict(q=FAKE, T=2, H=16, K=64, scale=0.07, req=FAKE, topk=FAKE, nreq=2, bs=16,
+             pools=[FAKE] * D, nslots=[100] * D, bts=[FAKE] * D, strides=[4] * D,
+             widths=[4] * D, out=FAKE, lse=FAKE, ws=None, wsb=0)
+    a.update(kw)
+    n = max(D, 1)
+    arr = lambda typ, xs: (typ * n)(*(list(xs) + [0] * (n - len(xs)))[:n])
+    return lib.smla_dcp_sparse_mla_decode_fused(
+        a["q"], a["T"], a["H"], a["K"], ctypes.c_float(a["scale"]), a["req"], a["topk"],
+        a["nreq"], D, a["bs"], arr(ctypes.c_void_p, a["pools"]), arr(ctypes.c_int64, a["nslots"]),
+        arr(ctypes.c_void_p, a["bts"]), arr(ctypes.c_int64, a["strides"]),
+        arr(ctypes.c_int32, a["widths"]), a["out"], a["lse"], a["ws"], a["wsb"], None)
+
+
+@pytest.mark.parametrize("D,kw,status", [
+    (0, {}, capi.SMLA_ERR_INVALID_ARG),
+    (17, {}, capi.SMLA_ERR_UNSUPPORTED),
+    (2, dict(H=129), capi.SMLA_ERR_UNSUPPORTED),
+    (2, dict(T=-1), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(K=0), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(bs=0), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(nreq=0), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(scale=float("nan")), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(q=None), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(topk=None), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(q=FAKE + 8), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(pools=[FAKE, None]), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(pools=[FAKE, FAKE + 4]), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(nslots=[100, -1]), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(bts=[None, FAKE]), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(widths=[0, 4]), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(strides=[4, 3]), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(T=0, q=None, topk=None, req=None, out=None, lse=None), capi.SMLA_OK),
+])
+def test_fused_argument_checks(lib, D, kw, status):
+    assert _fused(lib, D=D, **kw) == status
+
+
+def test_fused_workspace_checks(lib):
+    need = capi.decode_workspace_size(3, 128, 2048)
+    assert need > 0
+    assert _fused(lib, T=3, H=128, K=2048) == capi.SMLA_ERR_WORKSPACE
+    assert _fused(lib, T=3, H=128, K=2048, ws=FAKE, wsb=need - 1) == capi.SMLA_ERR_WORKSPACE
 
 
 def _merge(lib, D=2, T=3, H=4, outs=None, lses=None, out=FAKE, lse=FAKE):

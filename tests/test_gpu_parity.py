@@ -31,6 +31,12 @@ class Run:
         self.out, self.lse = self.step.run()
         torch.cuda.synchronize()
         self.deverr = capi.get_device_error(clear=True)
+        st = self.step
+        self.f_out, self.f_lse = capi.dcp_sparse_mla_decode_fused(
+            st.q, st.req_id, st.topk, st.pools, st.block_tables, self.wl.spec.block_size,
+            self.wl.spec.sm_scale, bt_widths=st.bt_widths)
+        torch.cuda.synchronize()
+        self.f_deverr = capi.get_device_error(clear=True)
         self._ref = None
 
     def ref(self):
@@ -82,6 +88,20 @@ def test_merged_matches_oracle(run):
     _, _, outs, lses = run.ref()
     ref_out, ref_lse = oracle.lse_merge(outs, lses)
     compare_out_lse(run.out, run.lse, ref_out, ref_lse, where=f"{run.wl.spec.name} merged")
+
+
+def test_fused_step_matches_oracle(run):
+    """Conversion, decode and merge of all shards in one launch."""
+    _, _, outs, lses = run.ref()
+    ref_out, ref_lse = oracle.lse_merge(outs, lses)
+    compare_out_lse(run.f_out, run.f_lse, ref_out, ref_lse, where=f"{run.wl.spec.name} fused")
+    assert run.f_deverr == 0
+
+
+def test_fused_step_agrees_with_pipeline(run):
+    assert torch.equal(torch.isneginf(run.f_lse), torch.isneginf(run.lse))
+    fin = torch.isfinite(run.lse)
+    assert (run.f_lse[fin] - run.lse[fin]).abs().max().item() < 2e-3
 
 
 def test_merge_kernel_alone_on_gpu_partials(run):
@@ -236,6 +256,72 @@ def test_zero_tokens_is_noop(cuda_device):
     assert ls.shape == (0, 8)
     o, l = capi.dcp_lse_merge([out, out], [lse, lse])
     assert o.shape == (0, 16, 512)
+
+
+def test_fused_bad_inputs_masked_and_flagged(cuda_device):
+    """Ids past a block table, unallocated blocks and bad request ids drop
+    out of the softmax and set device error bits; the rest matches the oracle."""
+    dev = cuda_device
+    D, bs = 2, 4
+    pools = [_small_pool(32, dev, seed=20 + d) for d in range(D)]
+    bts = [torch.tensor([[0, 1, -1], [2, 3, 4]], dtype=torch.int32, device=dev),
+           torch.tensor([[5, -1, -1], [1, 6, 7]], dtype=torch.int32, device=dev)]
+    req = torch.tensor([0, 9, 1], dtype=torch.int32, device=dev)
+    topk = torch.tensor([[0, 1, 2, 3, 50, 17, -1, 6],
+                         [0, 1, 2, 3, 4, 5, 6, 7],
+                         [0, 1, 9, 10, 20, 21, -1, 8]], dtype=torch.int32, device=dev)
+    g = torch.Generator(device=dev).manual_seed(21)
+    q = torch.randn((3, 16, 576), generator=g, device=dev).to(torch.bfloat16)
+    capi.get_device_error(clear=True)
+    out, lse = capi.dcp_sparse_mla_decode_fused(q, req, topk, pools, bts, bs, 0.07)
+    torch.cuda.synchronize()
+    err = capi.get_device_error(clear=True)
+    assert err & capi.DEVERR_BLOCK_TABLE and err & capi.DEVERR_REQ_ID
+    assert torch.isneginf(lse[1]).all() and torch.all(out[1].view(torch.int16) == 0)
+    # reference: drop the bad ids by hand (50 -> rank 0 local 25 -> column 6
+    # past the width; 17 -> rank 1 local 8 -> column 2 = -1 for request 0)
+    clean = torch.tensor([[0, 1, 2, 3, -1, -1, -1, 6], [-1] * 8,
+                          [0, 1, 9, 10, 20, 21, -1, 8]], dtype=torch.int32, device=dev)
+    q_bits = _q_bits(q)
+    outs, lses = [], []
+    for d in range(D):
+        sl, _ = oracle.dcp_filter_convert_index(np.array([0, 0, 1]), bts[d].cpu().numpy(),
+                                                clean.cpu().numpy(), D, d, bs)
+        sl[1] = -1
+        o, l = oracle.sparse_mla_decode(q_bits, pools[d].cpu().numpy(), sl, 0.07)
+        outs.append(o)
+        lses.append(l)
+    ref_out, ref_lse = oracle.lse_merge(outs, lses)
+    compare_out_lse(out, lse, ref_out, ref_lse, where="fused bad inputs")
+
+
+@pytest.mark.parametrize("K", [64, 2048, 4096])
+def test_fused_small_batches_split_k(cuda_device, K):
+    """Few query rows: the fused step splits each row over several clusters
+    and combines the splits in-kernel."""
+    dev = cuda_device
+    spec = inputs.WorkloadSpec(
+        name="fused_small", num_reqs=3, tokens_per_req=1, heads=128, topk=K, dcp=4,
+        block_size=64, ctx_kind="uniform", ctx_lo=K // 2, ctx_hi=3 * K)
+    wl = inputs.make_workload(spec, seed=K, device=dev)
+    step = DcpDecodeStep(wl, device=dev)
+    out, lse = step.run()
+    torch.cuda.synchronize()
+    f_out, f_lse = capi.dcp_sparse_mla_decode_fused(
+        step.q, step.req_id, step.topk, step.pools, step.block_tables, spec.block_size,
+        spec.sm_scale, bt_widths=step.bt_widths)
+    torch.cuda.synchronize()
+    q_bits = _q_bits(wl.q)
+    outs, lses = [], []
+    for d, s in enumerate(wl.shards):
+        sl, _ = oracle.dcp_filter_convert_index(wl.req_id, s.block_table, wl.topk, wl.D, d,
+                                                spec.block_size)
+        o, l = oracle.sparse_mla_decode(q_bits, s.pool.cpu().numpy(), sl, spec.sm_scale)
+        outs.append(o)
+        lses.append(l)
+    ref_out, ref_lse = oracle.lse_merge(outs, lses)
+    compare_out_lse(f_out, f_lse, ref_out, ref_lse, where=f"fused K={K}")
+    compare_out_lse(out, lse, ref_out, ref_lse, where=f"pipeline K={K}")
 
 
 # ---------------------------------------------------------- index edge cases
