@@ -47,7 +47,7 @@ DECODE_SOURCES = ["sparse_mla_decode_dcp_gb300/csrc/smla_decode.cu",
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--steps", type=int, default=3000)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
@@ -94,7 +94,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -407,29 +407,37 @@ def run_gpu(args):
 
 # ------------------------------------------------------------ reference arm
 def run_reference(args):
+    """The reference arm of this build: the float64 CPU oracle, timed as it
+    stands on this host's cores, on the same workload and metric.  Each step
+    is a bounded sample of the workload's query rows (all D shards' convert +
+    decode, then the merge), sized from a measured per-row time so that the
+    whole --steps/--warmup run stays within about two minutes."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    import torch
-
     from sparse_mla_decode_dcp_gb300 import inputs
     wl = inputs.make_workload(args.workload, seed=args.seed, device="cpu")
-    n = min(args.cpu_sample_tokens, wl.T)
+    probe = cpu_baseline(wl, 2)
+    per_row_s = 1.0 / probe["value"]
+    budget_s = 120.0
+    n = int(budget_s / (max(1, args.steps + args.warmup) * per_row_s))
+    n = max(1, min(wl.T, n))
     for _ in range(args.warmup):
-        cpu_baseline(wl, max(1, n // 4))
+        cpu_baseline(wl, n)
     times = []
+    b = None
     for _ in range(args.steps):
         b = cpu_baseline(wl, n)
         times.append(n / b["value"])
     value = n * len(times) / sum(times)
     b["value"] = value
     result = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": args.workload, "T": wl.T, "H": wl.H, "K": wl.K, "D": wl.D,
-                   "sample_tokens_per_step": n},
+                   "sample_rows_per_step": n},
         "cpu_baseline": b,
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

@@ -59,6 +59,8 @@ enum {
   SMLA_DEVERR_SLOT_RANGE = 4u,  /* local slot >= num_slots                     */
   SMLA_DEVERR_TIMEOUT = 8u      /* a bounded wait inside a kernel gave up      */
 };
+/* With SMLA_DEVERR_TIMEOUT, bits 8..31 of the word tell which of the decode
+ * kernel's internal waits gave up (a diagnostic bitmask, one bit per site). */
 
 /* Largest gathered head count the decode kernel takes [P3 implementation
  * breakdown step 4: heads pad to the 64/128 kernel envelope]. */
@@ -150,7 +152,8 @@ size_t smla_decode_workspace_size(int32_t T, int32_t H, int32_t K);
  *               zero-filled again); may be NULL when that size is 0.
  *               Calls that run concurrently need distinct workspaces.
  * Errors: INVALID_ARG for null pointers, T < 0, K < 1, H < 1, num_slots < 0,
- * misaligned q/kv_cache/out; UNSUPPORTED for H > SMLA_MAX_HEADS; WORKSPACE
+ * sm_scale not finite and positive, misaligned q/kv_cache/out; UNSUPPORTED
+ * for H > SMLA_MAX_HEADS; WORKSPACE
  * when the workspace is too small, NULL or misaligned.  A slot >= num_slots
  * is treated as -1 and sets SMLA_DEVERR_SLOT_RANGE.
  */

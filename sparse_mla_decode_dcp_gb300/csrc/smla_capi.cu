@@ -83,7 +83,8 @@ smla_status smla_sparse_mla_decode(
     const int32_t* local_slots, int32_t T, int32_t H, int32_t K,
     float sm_scale, uint16_t* out, float* lse, void* workspace,
     size_t workspace_bytes, void* stream) {
-  if (T < 0 || K < 1 || H < 1 || num_slots < 0 || !std::isfinite(sm_scale))
+  if (T < 0 || K < 1 || H < 1 || num_slots < 0 || !std::isfinite(sm_scale) ||
+      !(sm_scale > 0.f))
     return SMLA_ERR_INVALID_ARG;
   if (H > SMLA_MAX_HEADS) return SMLA_ERR_UNSUPPORTED;
   if (T == 0) return SMLA_OK;
@@ -119,7 +120,7 @@ smla_status smla_dcp_sparse_mla_decode_fused(
     const int64_t* bt_row_strides, const int32_t* bt_widths, uint16_t* out,
     float* lse, void* workspace, size_t workspace_bytes, void* stream) {
   if (T < 0 || K < 1 || H < 1 || D < 1 || block_size < 1 || num_reqs < 1 ||
-      !std::isfinite(sm_scale))
+      !std::isfinite(sm_scale) || !(sm_scale > 0.f))
     return SMLA_ERR_INVALID_ARG;
   if (H > SMLA_MAX_HEADS || D > SMLA_MAX_DCP) return SMLA_ERR_UNSUPPORTED;
   if (T == 0) return SMLA_OK;

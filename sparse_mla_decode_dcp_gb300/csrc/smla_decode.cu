@@ -58,13 +58,12 @@ constexpr int kTileN = 64;        // keys per tile (MMA N of QK^T, K of PV)
 constexpr int kThreads = 288;     // 9 warps
 constexpr int kMmaWarp = 8;
 constexpr int kMaxList = 2048;    // compacted slots one cluster handles
-constexpr uint32_t kSpinLimit = 1u << 22;
 
 // tensor-memory columns (512 allocated)
 constexpr uint32_t kOCol = 0;     // O half: 256 fp32 columns
 constexpr uint32_t kSCol = 256;   // S tile: 64 fp32 columns
 constexpr uint32_t kPCol = 320;   // P tile: 64 fp16 = 32 columns
-constexpr uint32_t kQCol = 352;   // Q half: up to 320 fp16 = 160 columns
+constexpr uint32_t kQCol = 352;   // Q part: 288 fp16 = 144 columns
 constexpr uint32_t kTmemCols = 512;
 
 // shared-memory layout (offsets from a 1024-byte aligned base)
@@ -94,11 +93,37 @@ static_assert(sizeof(Ctl) <= 256, "control block");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait sites, recorded in bits 8.. of the device error word when a wait
+// gives up (diagnostic).
+enum WaitSite : uint32_t {
+  kWsSFull = 0, kWsExchange, kWsPvDone, kWsPvLast, kWsFreed, kWsQReady, kWsFull, kWsSFree,
+  kWsPFull, kWsDrain
+};
+
+// Every wait is bounded in time (kWaitNs of the global timer); a wait that
+// gives up records TIMEOUT plus its site and raises the CTA's abort flag so
+// the other roles stop waiting too.
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+template <bool kCluster>
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                           uint32_t site) {
+  auto probe = [&]() {
+    return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (probe()) return true;
+  const uint64_t t0 = globaltimer_ns();
   uint32_t it = 0;
-  while (!mbar_try_wait(bar, parity)) {
-    if (*abort || ++it > kSpinLimit) {
-      atomicOr(&g_decode_error, SMLA_DEVERR_TIMEOUT);
+  while (!probe()) {
+    if (*abort) return false;
+    if ((++it & 63u) == 0 && globaltimer_ns() - t0 > kWaitNs) {
+      atomicOr(&g_decode_error, SMLA_DEVERR_TIMEOUT | (1u << (8 + site)));
       *abort = 1;
       return false;
     }
@@ -106,17 +131,14 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   return true;
 }
 
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                         uint32_t site) {
+  return wait_phase<false>(bar, parity, abort, site);
+}
+
 __device__ __forceinline__ bool wait_bar_cluster(uint64_t* bar, uint32_t parity,
-                                                 volatile int* abort) {
-  uint32_t it = 0;
-  while (!mbar_try_wait_cluster(bar, parity)) {
-    if (*abort || ++it > kSpinLimit) {
-      atomicOr(&g_decode_error, SMLA_DEVERR_TIMEOUT);
-      *abort = 1;
-      return false;
-    }
-  }
-  return true;
+                                                 volatile int* abort, uint32_t site) {
+  return wait_phase<true>(bar, parity, abort, site);
 }
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
@@ -132,7 +154,20 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// 8 e4m3 codes -> 8 fp16 values code * (hi + lo), one rounding
+// Two e4m3 codes (bytes `sel` picks) -> fp16x2 holding code * 2^-8, exactly,
+// on the integer pipe: the sign moves to fp16's sign bit and the 7 exponent /
+// mantissa bits drop in one position lower (4-bit exponent under fp16's
+// 5-bit field, bias 7 vs 15), which makes normal and subnormal codes alike
+// land on code * 2^-8.  (e4m3 NaN codes, which no quantiser emits, are not
+// special-cased.)
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled_down(uint32_t w, uint32_t sel) {
+  const uint32_t y = __byte_perm(w, 0u, sel);  // code a in bits 15:8, code b in 31:24
+  return (y & 0x80008000u) | ((y & 0x7F007F00u) >> 1);
+}
+
+// 8 e4m3 codes -> 8 fp16 values code * scale with one rounding: hi + lo is
+// the fp32 scale * 2^8 split into two fp16 parts, and fma(c, hi, c * lo)
+// rounds once.
 __device__ __forceinline__ uint4 e4m3x8_scaled(uint2 codes, __half2 hi, __half2 lo) {
   const uint32_t w[2] = {codes.x, codes.y};
   uint32_t o[4];
@@ -140,9 +175,8 @@ __device__ __forceinline__ uint4 e4m3x8_scaled(uint2 codes, __half2 hi, __half2 
   for (int k = 0; k < 2; ++k) {
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
-      const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(
-          static_cast<__nv_fp8x2_storage_t>((w[k] >> (16 * p)) & 0xffffu), __NV_E4M3);
-      const __half2 c = *reinterpret_cast<const __half2*>(&r);
+      const uint32_t bits = e4m3x2_to_f16x2_scaled_down(w[k], p == 0 ? 0x1404u : 0x3424u);
+      const __half2 c = *reinterpret_cast<const __half2*>(&bits);
       o[2 * k + p] = h2_bits(__hfma2(c, hi, __hmul2(c, lo)));
     }
   }
@@ -155,23 +189,31 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Per-CTA constants of the two halves of the pair.
+// Per-CTA constants of the two halves of the pair.  CTA 0 gathers latent
+// dims [0, 288) and contracts all of them; CTA 1 gathers latent dims
+// [256, 512) plus the rope dims and contracts key dims [288, 576).  Each
+// contracts 288 key dims (balanced), and each holds the 256 value dims of
+// its O half inside its tile.
 template <int C>
 struct Half {
-  static constexpr int kKDims = C == 0 ? 256 : 320;      // QK^T key dims
-  static constexpr int kKSteps = kKDims / 16;             // MMA K = 16
-  static constexpr int kQCols = kKDims / 2;
-  static constexpr int kRawChunks = C == 0 ? 17 : 25;     // 16-byte chunks per key
-  static constexpr int kOutChunks = kKDims / 8;           // fp16 chunks per key
-  static constexpr int kQDim0 = C == 0 ? 0 : 256;         // first q dim
+  static constexpr int kTileDims = C == 0 ? 288 : 320;    // key dims gathered
+  static constexpr int kDim0 = C == 0 ? 0 : 256;          // first gathered dim
+  static constexpr int kQkLocal0 = C == 0 ? 0 : 32;       // first contracted tile dim
+  static constexpr int kQkDims = 288;                     // contracted key dims
+  static constexpr int kKSteps = kQkDims / 16;            // MMA K = 16
+  static constexpr int kQDim0 = kDim0 + kQkLocal0;        // first q dim
+  static constexpr int kCodeChunks = C == 0 ? 18 : 16;    // 16-byte code chunks
+  static constexpr int kRawChunks = C == 0 ? 19 : 25;     // + scales (+ rope)
+  static constexpr int kScaleOff = kCodeChunks * 16;      // raw offset of the scales
+  static constexpr int kOutChunks = kTileDims / 8;        // fp16 chunks per key
 };
 
 // Source offset (bytes within the 656-byte row) of raw chunk `ch`.  The raw
-// row keeps codes at [0,256), the four scales at [256,272) and (CTA 1) the
-// rope values at [272,400).
+// row keeps this CTA's codes first, then the four scales, then (CTA 1) the
+// rope values.
 template <int C>
 __device__ __forceinline__ int raw_src_offset(int ch) {
-  if (C == 0) return ch < 16 ? ch * 16 : 512;
+  if (C == 0) return ch < 18 ? ch * 16 : 512;
   return 256 + ch * 16;
 }
 
@@ -200,26 +242,30 @@ __device__ void dequant_tile(const uint8_t* raw, uint8_t* op, int valid, int d) 
   const int oc1 = oc0 + HC::kOutChunks / 2;
   const uint8_t* row = raw + key * kRawStride;
   const bool live = key < valid;
-  __half2 hi[2], lo[2];
+  // this thread's latent chunks span at most two scale groups
+  const int g0 = (HC::kDim0 + oc0 * 8) >> 7;
+  const int g1 = (HC::kDim0 + (min(oc1, HC::kCodeChunks * 2) - 1) * 8) >> 7;
+  __half2 hi0 = __half2half2(__float2half_rn(0.f)), lo0 = hi0, hi1 = hi0, lo1 = hi0;
   if (live) {
-#pragma unroll
-    for (int g = 0; g < 2; ++g) {
-      const float s = *reinterpret_cast<const float*>(row + 256 + 4 * (2 * C + g));
-      const __half h = __float2half_rn(s);
-      const __half l = __float2half_rn(s - __half2float(h));
-      hi[g] = __half2half2(h);
-      lo[g] = __half2half2(l);
-    }
+    // scales carry the 2^8 the integer code decode leaves out
+    const float s0 = 256.f * *reinterpret_cast<const float*>(row + HC::kScaleOff + 4 * g0);
+    const float s1 = 256.f * *reinterpret_cast<const float*>(row + HC::kScaleOff + 4 * g1);
+    const __half h0 = __float2half_rn(s0), h1 = __float2half_rn(s1);
+    hi0 = __half2half2(h0);
+    lo0 = __half2half2(__float2half_rn(s0 - __half2float(h0)));
+    hi1 = __half2half2(h1);
+    lo1 = __half2half2(__float2half_rn(s1 - __half2float(h1)));
   }
   for (int oc = oc0; oc < oc1; ++oc) {
     uint4 v = make_uint4(0, 0, 0, 0);
     if (live) {
-      if (oc < 32) {
+      if (oc < HC::kCodeChunks * 2) {
         const uint2 codes = *reinterpret_cast<const uint2*>(row + oc * 8);
-        const int g = oc >> 4;
-        v = e4m3x8_scaled(codes, hi[g], lo[g]);
+        const bool first = ((HC::kDim0 + oc * 8) >> 7) == g0;
+        v = e4m3x8_scaled(codes, first ? hi0 : hi1, first ? lo0 : lo1);
       } else {
-        v = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(row + 272 + (oc - 32) * 16));
+        v = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(
+            row + HC::kScaleOff + 16 + (oc - HC::kCodeChunks * 2) * 16));
       }
     }
     const int kb = oc >> 3;
@@ -325,29 +371,34 @@ __device__ void split_epilogue(const DecodeArgs& a, Ctl* ctl, int64_t t, int spl
 template <int C>
 __device__ void load_q_to_tmem(const DecodeArgs& a, int64_t t, uint32_t tb, int warp, int h) {
   using HC = Half<C>;
-  constexpr int kChunks = HC::kQCols / 32;  // 32 TMEM columns = 64 dims each
+  constexpr int kVec = HC::kQkDims / 8;  // 16-byte loads per head row (36)
   const bool live = h < a.H;
   const uint4* qsrc = reinterpret_cast<const uint4*>(
       a.q + (t * a.H + (live ? h : 0)) * SMLA_QK_DIM + HC::kQDim0);
 #pragma unroll 1
-  for (int c0 = 0; c0 < kChunks; c0 += 2) {
+  for (int v0 = 0; v0 < kVec; v0 += 16) {
     uint4 raw[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k)
-      raw[k] = (live && c0 + (k >> 3) < kChunks) ? __ldg(qsrc + c0 * 8 + k) : make_uint4(0, 0, 0, 0);
+      raw[k] = (live && v0 + k < kVec) ? __ldg(qsrc + v0 + k) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-      if (c0 + cc < kChunks) {
+    for (int g = 0; g < 2; ++g) {  // 8 loads = 64 dims = 32 TMEM columns
+      const int vg = v0 + 8 * g;
+      if (vg < kVec) {
         uint32_t qr[32];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint4 v = bf16x8_to_f16x8(raw[cc * 8 + k]);
+          const uint4 v = bf16x8_to_f16x8(raw[8 * g + k]);
           qr[4 * k + 0] = v.x;
           qr[4 * k + 1] = v.y;
           qr[4 * k + 2] = v.z;
           qr[4 * k + 3] = v.w;
         }
-        tmem_st32(tmem_addr(tb, 32 * warp, kQCol + 32 * (c0 + cc)), qr);
+        const uint32_t addr = tmem_addr(tb, 32 * warp, kQCol + vg * 4);
+        if (vg + 8 <= kVec)
+          tmem_st32(addr, qr);
+        else
+          tmem_st16(addr, qr);  // trailing 32 dims
       }
     }
   }
@@ -378,7 +429,7 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, int64_t t, i
     const uint32_t peer_x0 = map_to_cta(smem_u32(xbase), peer);
     bool ok = true;
     for (int i = 0; i < ntiles && ok; ++i) {
-      ok = __all_sync(0xffffffffu, wait_bar(&ctl->s_full, i & 1, abort));
+      ok = __all_sync(0xffffffffu, wait_bar(&ctl->s_full, i & 1, abort, kWsSFull));
       if (!ok) break;
       tc_fence_after();
       float s[64];
@@ -403,7 +454,7 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, int64_t t, i
         st_cluster_v4(px + (j4 * 128 + h) * 16, s[4 * j4], s[4 * j4 + 1], s[4 * j4 + 2],
                       s[4 * j4 + 3]);
       mbar_arrive_remote(&ctl->x[b], peer);
-      ok = __all_sync(0xffffffffu, wait_bar_cluster(&ctl->x[b], (i >> 1) & 1, abort));
+      ok = __all_sync(0xffffffffu, wait_bar_cluster(&ctl->x[b], (i >> 1) & 1, abort, kWsExchange));
       if (!ok) break;
       const float4* mine = reinterpret_cast<const float4*>(xbase + b * kXBytes);
 #pragma unroll
@@ -414,35 +465,45 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, int64_t t, i
         s[4 * j4 + 2] += v.z;
         s[4 * j4 + 3] += v.w;
       }
+      // raw-score maximum (sm_scale > 0, so it commutes with the scaling)
       const int valid = min(kTileN, n - i * kTileN);
       float mx = -INFINITY;
+      if (valid == kTileN) {
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        s[j] = (j < valid) ? s[j] * scale_log2 : -INFINITY;
-        mx = fmaxf(mx, s[j]);
+        for (int j = 0; j < 64; ++j) mx = fmaxf(mx, s[j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          s[j] = (j < valid) ? s[j] : -INFINITY;
+          mx = fmaxf(mx, s[j]);
+        }
       }
-      float alpha = 1.f;
+      mx *= scale_log2;
+      float alpha = 1.f;  // this row's rescale factor for O and l
       bool rescale = false;
       if (mx > m_ref + 8.f) {
         alpha = ex2(m_ref - mx);  // 0 on the first tile
         m_ref = mx;
         rescale = (i > 0);
       }
-      float sum = 0.f;
+      const float neg_m = -m_ref;
+      float sums[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const float p0 = ex2(s[2 * j] - m_ref);
-        const float p1 = ex2(s[2 * j + 1] - m_ref);
-        sum += p0 + p1;
+        const float p0 = ex2(fmaf(s[2 * j], scale_log2, neg_m));
+        const float p1 = ex2(fmaf(s[2 * j + 1], scale_log2, neg_m));
+        sums[j & 3] += p0 + p1;
         pk[j] = h2_bits(__floats2half2_rn(p0, p1));
       }
-      l = l * alpha + sum;
+      l = l * alpha + ((sums[0] + sums[1]) + (sums[2] + sums[3]));
       if (i > 0) {
-        ok = __all_sync(0xffffffffu, wait_bar(&ctl->pv_done, (i - 1) & 1, abort));
+        ok = __all_sync(0xffffffffu, wait_bar(&ctl->pv_done, (i - 1) & 1, abort, kWsPvDone));
         if (!ok) break;
         tc_fence_after();
-        if (rescale) {
+        // tcgen05.ld/st are warp-collective: the warp rescales together when
+        // any of its rows needs it, each lane by its own factor (1 if none)
+        if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
           for (int cc = 0; cc < 8; ++cc) {
             uint32_t r[32];
@@ -450,7 +511,7 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, int64_t t, i
             tmem_ld32(addr, r);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+            for (int jj = 0; jj < 32; ++jj) r[jj] = __float_as_uint(__uint_as_float(r[jj]) * alpha);
             tmem_st32(addr, r);
           }
         }
@@ -462,9 +523,12 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, int64_t t, i
     }
     // epilogue
     if (ok && ntiles > 0) {
-      ok = __all_sync(0xffffffffu, wait_bar(&ctl->pv_done, (ntiles - 1) & 1, abort));
+      ok = __all_sync(0xffffffffu, wait_bar(&ctl->pv_done, (ntiles - 1) & 1, abort, kWsPvLast));
       tc_fence_after();
     }
+    // one decision for all four softmax warps (the split epilogue below uses a
+    // 128-thread named barrier)
+    ok = !named_bar_or(4, 128, !ok);
     if (ok && a.splits == 1) {
       // tcgen05.ld is warp-collective: every lane loads, only live heads store
       const bool live = h < a.H;
@@ -519,7 +583,7 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, int64_t t, i
       } else {
         cp_async_wait<0>();
       }
-      bool bad = (i >= 2) && !wait_bar(&ctl->freed[i & 1], ((i - 2) >> 1) & 1, abort);
+      bool bad = (i >= 2) && !wait_bar(&ctl->freed[i & 1], ((i - 2) >> 1) & 1, abort, kWsFreed);
       if (named_bar_or(1, 128, bad || *abort)) break;  // raw tile i landed for all
       dequant_tile<C>(raw + (i & 1) * kRawBytes, op + (i & 1) * kOpTileBytes,
                       min(kTileN, n - i * kTileN), d);
@@ -533,24 +597,26 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, int64_t t, i
     constexpr uint32_t idesc_qk = idesc_f16_f32(128, kTileN, false, false);
     constexpr uint32_t idesc_pv = idesc_f16_f32(128, 256, false, true);
     const uint32_t op0 = smem_u32(sm + kOffOp);
-    bool ok = wait_bar(&ctl->q_ready, 0, abort);
+    bool ok = wait_bar(&ctl->q_ready, 0, abort, kWsQReady);
     tc_fence_after();
     for (int i = 0; ok && i <= ntiles; ++i) {
       if (i < ntiles) {
-        if (!wait_bar(&ctl->full[i & 1], (i >> 1) & 1, abort)) break;
-        if (i > 0 && !wait_bar(&ctl->s_free, (i - 1) & 1, abort)) break;
+        if (!wait_bar(&ctl->full[i & 1], (i >> 1) & 1, abort, kWsFull)) break;
+        if (i > 0 && !wait_bar(&ctl->s_free, (i - 1) & 1, abort, kWsSFree)) break;
         tc_fence_after();
         const uint32_t base = op0 + (i & 1) * kOpTileBytes;
 #pragma unroll
         for (int k = 0; k < HC::kKSteps; ++k) {
-          const uint64_t bd = sdesc_sw128(base + (k >> 2) * kKBlockBytes + (k & 3) * 32, 16, 1024);
+          const int ldim = HC::kQkLocal0 + 16 * k;  // first tile dim of this K step
+          const uint64_t bd =
+              sdesc_sw128(base + (ldim >> 6) * kKBlockBytes + (ldim & 63) * 2, 16, 1024);
           mma_ts(tb + kSCol, tb + kQCol + 8 * k, bd, idesc_qk, k > 0);
         }
         mma_commit(&ctl->s_full);
       }
       if (i > 0) {
         const int j = i - 1;
-        if (!wait_bar(&ctl->p_full, j & 1, abort)) break;
+        if (!wait_bar(&ctl->p_full, j & 1, abort, kWsPFull)) break;
         tc_fence_after();
         const uint32_t base = op0 + (j & 1) * kOpTileBytes;
 #pragma unroll
@@ -563,10 +629,13 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, int64_t t, i
       }
     }
     // drain: every MMA issued above has completed before TMEM is released
-    // (waited on even after an abort, with its own bound)
-    mma_commit(&ctl->end);
-    int no_abort = 0;
-    wait_bar(&ctl->end, 0, &no_abort);
+    // (waited on even after an abort, with its own bound).  A CTA whose row
+    // has no valid slot issued no MMA and has nothing to drain.
+    if (ntiles > 0) {
+      mma_commit(&ctl->end);
+      int no_abort = 0;
+      wait_bar(&ctl->end, 0, &no_abort, kWsDrain);
+    }
   }
 }
 

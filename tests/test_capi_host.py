@@ -107,6 +107,8 @@ def _decode(lib, **kw):
     (dict(ns=-1), capi.SMLA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), capi.SMLA_ERR_INVALID_ARG),
     (dict(scale=float("inf")), capi.SMLA_ERR_INVALID_ARG),
+    (dict(scale=0.0), capi.SMLA_ERR_INVALID_ARG),
+    (dict(scale=-0.07), capi.SMLA_ERR_INVALID_ARG),
     (dict(q=None), capi.SMLA_ERR_INVALID_ARG),
     (dict(kv=None), capi.SMLA_ERR_INVALID_ARG),
     (dict(slots=None), capi.SMLA_ERR_INVALID_ARG),
@@ -165,6 +167,7 @@ def _fused(lib, D=2, **kw):
     (2, dict(bs=0), capi.SMLA_ERR_INVALID_ARG),
     (2, dict(nreq=0), capi.SMLA_ERR_INVALID_ARG),
     (2, dict(scale=float("nan")), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(scale=-1.0), capi.SMLA_ERR_INVALID_ARG),
     (2, dict(q=None), capi.SMLA_ERR_INVALID_ARG),
     (2, dict(topk=None), capi.SMLA_ERR_INVALID_ARG),
     (2, dict(q=FAKE + 8), capi.SMLA_ERR_INVALID_ARG),

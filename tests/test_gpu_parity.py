@@ -458,3 +458,70 @@ def test_spec_decode_rows_equal_single_token_calls(cuda_device):
                                           step.local_slots[d][i:i + 1], spec.sm_scale)
             assert (o[0].float() - step.part_out[d][i].float()).abs().max().item() < 2e-2
             assert (l[0] - step.part_lse[d][i]).abs().max().item() < 2e-3
+
+
+# ------------------------------------------------------- workspace and graphs
+def test_split_k_workspace_reused_across_calls(cuda_device):
+    """Split-K arrival counters return to zero after every call, so one
+    workspace serves any number of calls and results repeat bit for bit."""
+    dev = cuda_device
+    pool = _small_pool(3000, dev, seed=31)
+    g = torch.Generator(device=dev).manual_seed(31)
+    T, H, K = 4, 128, 2048
+    assert capi.decode_workspace_size(T, H, K) > 0
+    q = torch.randn((T, H, 576), generator=g, device=dev).to(torch.bfloat16)
+    rng = np.random.default_rng(31)
+    s = torch.from_numpy(np.stack([rng.choice(3000, K, replace=False)
+                                   for _ in range(T)]).astype(np.int32)).to(dev)
+    ws = capi.alloc_decode_workspace(T, H, K, dev)
+    first = capi.sparse_mla_decode(q, pool, s, 0.07, workspace=ws)
+    first = (first[0].clone(), first[1].clone())
+    for _ in range(3):
+        o, l = capi.sparse_mla_decode(q, pool, s, 0.07, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(o, first[0]) and torch.equal(l, first[1])
+    tick = ws[-256:]  # the counters sit in the last 256-byte block
+    assert torch.count_nonzero(tick).item() == 0
+
+
+@pytest.mark.parametrize("path", ["fused", "pipeline"])
+def test_step_replays_in_cuda_graph(cuda_device, path):
+    dev = cuda_device
+    wl = inputs.make_workload("tiny", seed=5, device=dev)
+    step = DcpDecodeStep(wl, device=dev)
+    fn = step.run_fused if path == "fused" else step.run
+    fn()
+    torch.cuda.synchronize()
+    ref_out, ref_lse = step.out.clone(), step.lse.clone()
+    step.out.zero_()
+    s = torch.cuda.Stream(dev)
+    with torch.cuda.stream(s):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            fn()
+    for _ in range(2):
+        step.out.fill_(7)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(step.out, ref_out) and torch.equal(step.lse, ref_lse)
+
+
+def test_decode_forced_rescale(cuda_device):
+    """Later tiles with ~10x larger latents push the running maximum up by far
+    more than 2^8 for most (but not all) head rows, exercising the O rescale
+    (and rows of one warp disagreeing about it)."""
+    dev = cuda_device
+    n = 512
+    pool = _small_pool(n, dev, seed=41)
+    scales = pool[:, 512:528].clone().view(torch.float32)
+    scales[64:] *= 10.0  # rows past the first tile
+    pool[:, 512:528] = scales.view(torch.uint8)
+    g = torch.Generator(device=dev).manual_seed(41)
+    T, H = 3, 128
+    q = torch.randn((T, H, 576), generator=g, device=dev).to(torch.bfloat16)
+    s = torch.arange(n, dtype=torch.int32, device=dev).repeat(T, 1)  # tile 0 = small rows
+    s[1] = torch.flip(s[1], dims=[0])  # large rows first: no rescale needed
+    s[2, 100:300] = -1
+    capi.get_device_error(clear=True)
+    _decode_vs_oracle(q, pool, s, 1 / math.sqrt(192), "forced rescale")
+    assert capi.get_device_error(clear=True) == 0
