@@ -29,8 +29,11 @@
 //     3 more mantissa bits than bf16, which keeps score errors well inside
 //     the LSE tolerance even for rows with a single valid slot.
 //   * Valid slots are compacted in order in the prologue (-1 never costs a
-//     load or an MMA); rows are gathered with 16-byte cp.async into a
-//     two-stage raw buffer, so the gather of tile i+1 overlaps tile i.
+//     load or an MMA).  Each gather thread loads its fixed share of every key
+//     row straight into registers one tile ahead and converts it from there;
+//     three operand tiles are in flight.
+//   * The partial score tiles travel as asynchronous remote stores counted on
+//     the receiving CTA's mbarrier (st.async + expect_tx).
 //   * Softmax in the log2 domain with a lazily moved reference maximum: the
 //     O accumulator in TMEM is rescaled only when the row maximum grows by
 //     more than 2^8.
@@ -56,6 +59,7 @@ __device__ unsigned int g_decode_error;
 
 constexpr int kTileN = 64;        // keys per tile (MMA N of QK^T, K of PV)
 constexpr int kThreads = 288;     // 9 warps
+constexpr int kStages = 3;        // operand tiles in flight
 constexpr int kMmaWarp = 8;
 constexpr int kMaxList = 2048;    // compacted slots one cluster handles
 
@@ -69,26 +73,29 @@ constexpr uint32_t kTmemCols = 512;
 // shared-memory layout (offsets from a 1024-byte aligned base)
 constexpr int kKBlockBytes = kTileN * 128;          // 64 keys x 64 fp16
 constexpr int kOpTileBytes = 5 * kKBlockBytes;      // up to 320 key dims
-constexpr int kRawStride = 400;                     // raw bytes per key
-constexpr int kRawBytes = kTileN * kRawStride;
 constexpr int kXBytes = 128 * kTileN * 4;           // fp32 partial S tile
 constexpr int kOffOp = 0;
-constexpr int kOffRaw = kOffOp + 2 * kOpTileBytes;
-constexpr int kOffX = kOffRaw + 2 * kRawBytes;
+constexpr int kOffX = kOffOp + kStages * kOpTileBytes;
 constexpr int kOffList = kOffX + 2 * kXBytes;
 constexpr int kOffListShard = kOffList + kMaxList * 4;  // fused step: shard of each key
 constexpr int kOffCtl = kOffListShard + kMaxList;
-constexpr int kSmemBytes = kOffCtl + 256 + 1024;    // + control block + alignment slack
+constexpr int kCtlBytes = 1024;
+constexpr int kSmemBytes = kOffCtl + kCtlBytes + 1024;  // + control block + alignment slack
 
 struct Ctl {
-  uint64_t q_ready, full[2], freed[2], s_full, s_free, p_full, pv_done, x[2], end;
+  uint64_t q_ready, full[kStages], freed[kStages], s_full, s_free, p_full, pv_done, x[2], end;
   uint32_t tbase;
   int n_list;
   int abort;
   int is_last;
   int warp_cnt[8];
+  // fused step: per shard, its pool and this row's request row of its table
+  const uint8_t* pool[kMaxMerge];
+  const int32_t* bt_row[kMaxMerge];
+  int64_t pool_slots[kMaxMerge];
+  int32_t bt_width[kMaxMerge];
 };
-static_assert(sizeof(Ctl) <= 256, "control block");
+static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -189,95 +196,141 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Per-CTA constants of the two halves of the pair.  CTA 0 gathers latent
-// dims [0, 288) and contracts all of them; CTA 1 gathers latent dims
-// [256, 512) plus the rope dims and contracts key dims [288, 576).  Each
-// contracts 288 key dims (balanced), and each holds the 256 value dims of
-// its O half inside its tile.
-template <int C>
-struct Half {
-  static constexpr int kTileDims = C == 0 ? 288 : 320;    // key dims gathered
-  static constexpr int kDim0 = C == 0 ? 0 : 256;          // first gathered dim
-  static constexpr int kQkLocal0 = C == 0 ? 0 : 32;       // first contracted tile dim
-  static constexpr int kQkDims = 288;                     // contracted key dims
-  static constexpr int kKSteps = kQkDims / 16;            // MMA K = 16
-  static constexpr int kQDim0 = kDim0 + kQkLocal0;        // first q dim
-  static constexpr int kCodeChunks = C == 0 ? 18 : 16;    // 16-byte code chunks
-  static constexpr int kRawChunks = C == 0 ? 19 : 25;     // + scales (+ rope)
-  static constexpr int kScaleOff = kCodeChunks * 16;      // raw offset of the scales
-  static constexpr int kOutChunks = kTileDims / 8;        // fp16 chunks per key
+// The two CTAs of a pair split the work by key dimension.  CTA 0 gathers
+// latent dims [0, 288) and contracts all of them; CTA 1 gathers latent dims
+// [256, 512) plus the 64 rope dims and contracts key dims [288, 576).  Each
+// contracts 288 key dims (balanced) and holds the 256 value dims of its O
+// half inside its tile.  All of it is runtime data of the CTA's rank, so the
+// two CTAs share one instruction stream (half the code, for the i-cache).
+constexpr int kQkDims = 288;
+constexpr int kKSteps = kQkDims / 16;  // MMA K = 16
+constexpr int kChunksPerThread = 12;   // 16-byte source chunks per gather thread and key
+
+struct HalfRt {
+  int c;           // CTA rank in the pair
+  int qk_local0;   // first contracted tile dim (0 or 32)
+  int q_dim0;      // first q dim (0 or 288)
 };
 
-// Source offset (bytes within the 656-byte row) of raw chunk `ch`.  The raw
-// row keeps this CTA's codes first, then the four scales, then (CTA 1) the
-// rope values.
-template <int C>
-__device__ __forceinline__ int raw_src_offset(int ch) {
-  if (C == 0) return ch < 18 ? ch * 16 : 512;
-  return 256 + ch * 16;
+__device__ __forceinline__ HalfRt half_of(uint32_t c) {
+  HalfRt r;
+  r.c = int(c);
+  r.qk_local0 = c ? 32 : 0;
+  r.q_dim0 = c ? 288 : 0;
+  return r;
 }
 
-template <int C, bool kFused>
-__device__ void issue_tile_loads(const DecodeArgs& a, const int* list, const uint8_t* shard,
-                                 int n, int tile, uint8_t* raw, int d) {
-  using HC = Half<C>;
-  const int k0 = tile * kTileN;
-  for (int q = d; q < kTileN * HC::kRawChunks; q += 128) {
-    const int key = q / HC::kRawChunks;
-    const int ch = q - key * HC::kRawChunks;
-    if (k0 + key < n) {
-      const uint8_t* pool = kFused ? a.pools[shard[k0 + key]] : a.kv;
-      const uint8_t* src = pool + int64_t(list[k0 + key]) * SMLA_ROW_BYTES + raw_src_offset<C>(ch);
-      cp_async_16(smem_u32(raw + key * kRawStride + ch * 16), src);
+// Gather thread (key, part) of CTA c owns up to 12 source chunks of 16 bytes
+// of every key row.  Chunk k: its byte offset in the 656-byte row, the first
+// tile dim it fills, whether it holds 16 e4m3 codes (two 8-dim output chunks,
+// scale group `group`) or 8 bf16 rope values (one output chunk).
+//   CTA 0: codes [0, 288) = 18 code chunks, 9 per part
+//   CTA 1: codes [256, 512) = 16 code chunks + 8 rope chunks; part 0 takes
+//          code chunks 0..11, part 1 code chunks 12..15 and the rope chunks
+__device__ __forceinline__ void chunk_at(int c, int part, int k, int& src, int& ldim, bool& code,
+                                         int& group) {
+  if (c == 0) {
+    const int ci = 9 * part + k;
+    src = 16 * ci;
+    ldim = 16 * ci;
+    code = true;
+    group = ci >> 3;
+  } else if (part == 0 || k < 4) {
+    const int ci = 12 * part + k;
+    src = 256 + 16 * ci;
+    ldim = 16 * ci;
+    code = true;
+    group = 2 + (ci >> 3);
+  } else {
+    const int r = k - 4;
+    src = 528 + 16 * r;
+    ldim = 256 + 8 * r;
+    code = false;
+    group = 0;
+  }
+}
+
+__device__ __forceinline__ int chunks_of(int c) { return c == 0 ? 9 : 12; }
+
+// Registers one thread holds for one key of one tile.
+struct RowRegs {
+  uint4 chunk[kChunksPerThread];
+  float4 scales;
+};
+
+template <bool kFused>
+__device__ __forceinline__ void load_row_regs(const DecodeArgs& a, const Ctl* ctl, const int* list,
+                                              const uint8_t* shard, int n, int tile, int key,
+                                              int c, int part, RowRegs& r) {
+  const int idx = tile * kTileN + key;
+  if (idx >= n) return;
+  const uint8_t* pool = kFused ? ctl->pool[shard[idx]] : a.kv;
+  const uint8_t* row = pool + int64_t(list[idx]) * SMLA_ROW_BYTES;
+  r.scales = __ldg(reinterpret_cast<const float4*>(row + 512));
+  const int nch = chunks_of(c);
+#pragma unroll
+  for (int k = 0; k < kChunksPerThread; ++k) {
+    if (k < nch) {
+      int src, ldim, group;
+      bool code;
+      chunk_at(c, part, k, src, ldim, code, group);
+      r.chunk[k] = __ldg(reinterpret_cast<const uint4*>(row + src));
     }
   }
 }
 
-template <int C>
-__device__ void dequant_tile(const uint8_t* raw, uint8_t* op, int valid, int d) {
-  using HC = Half<C>;
-  const int key = d >> 1;
-  const int part = d & 1;
-  const int oc0 = part * (HC::kOutChunks / 2);
-  const int oc1 = oc0 + HC::kOutChunks / 2;
-  const uint8_t* row = raw + key * kRawStride;
-  const bool live = key < valid;
-  // this thread's latent chunks span at most two scale groups
-  const int g0 = (HC::kDim0 + oc0 * 8) >> 7;
-  const int g1 = (HC::kDim0 + (min(oc1, HC::kCodeChunks * 2) - 1) * 8) >> 7;
-  __half2 hi0 = __half2half2(__float2half_rn(0.f)), lo0 = hi0, hi1 = hi0, lo1 = hi0;
+__device__ __forceinline__ void split_scale(float s, __half2& hi, __half2& lo) {
+  const float x = 256.f * s;  // the integer code decode leaves a factor 2^-8 out
+  const __half h = __float2half_rn(x);
+  hi = __half2half2(h);
+  lo = __half2half2(__float2half_rn(x - __half2float(h)));
+}
+
+// Convert this thread's chunks of one key into the swizzled fp16 tile (zeros
+// for a key past the row's valid count).
+__device__ __forceinline__ void store_row_regs(const RowRegs& r, uint8_t* op, int key, bool live,
+                                               int c, int part) {
+  __half2 hi[4], lo[4];
+  const __half2 z = __half2half2(__float2half_rn(0.f));
+#pragma unroll
+  for (int g = 0; g < 4; ++g) hi[g] = lo[g] = z;
   if (live) {
-    // scales carry the 2^8 the integer code decode leaves out
-    const float s0 = 256.f * *reinterpret_cast<const float*>(row + HC::kScaleOff + 4 * g0);
-    const float s1 = 256.f * *reinterpret_cast<const float*>(row + HC::kScaleOff + 4 * g1);
-    const __half h0 = __float2half_rn(s0), h1 = __float2half_rn(s1);
-    hi0 = __half2half2(h0);
-    lo0 = __half2half2(__float2half_rn(s0 - __half2float(h0)));
-    hi1 = __half2half2(h1);
-    lo1 = __half2half2(__float2half_rn(s1 - __half2float(h1)));
+    split_scale(r.scales.x, hi[0], lo[0]);
+    split_scale(r.scales.y, hi[1], lo[1]);
+    split_scale(r.scales.z, hi[2], lo[2]);
+    split_scale(r.scales.w, hi[3], lo[3]);
   }
-  for (int oc = oc0; oc < oc1; ++oc) {
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (live) {
-      if (oc < HC::kCodeChunks * 2) {
-        const uint2 codes = *reinterpret_cast<const uint2*>(row + oc * 8);
-        const bool first = ((HC::kDim0 + oc * 8) >> 7) == g0;
-        v = e4m3x8_scaled(codes, first ? hi0 : hi1, first ? lo0 : lo1);
-      } else {
-        v = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(
-            row + HC::kScaleOff + 16 + (oc - HC::kCodeChunks * 2) * 16));
+  const int nch = chunks_of(c);
+#pragma unroll
+  for (int k = 0; k < kChunksPerThread; ++k) {
+    if (k < nch) {
+      int src, ldim, group;
+      bool code;
+      chunk_at(c, part, k, src, ldim, code, group);
+      uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+      if (live) {
+        if (code) {
+          const __half2 hh = group == 0 ? hi[0] : group == 1 ? hi[1] : group == 2 ? hi[2] : hi[3];
+          const __half2 ll = group == 0 ? lo[0] : group == 1 ? lo[1] : group == 2 ? lo[2] : lo[3];
+          v0 = e4m3x8_scaled(make_uint2(r.chunk[k].x, r.chunk[k].y), hh, ll);
+          v1 = e4m3x8_scaled(make_uint2(r.chunk[k].z, r.chunk[k].w), hh, ll);
+        } else {
+          v0 = bf16x8_to_f16x8(r.chunk[k]);
+        }
       }
+      *reinterpret_cast<uint4*>(op + (ldim >> 6) * kKBlockBytes +
+                                sw128_offset(key, (ldim & 63) >> 3)) = v0;
+      if (code)
+        *reinterpret_cast<uint4*>(op + ((ldim + 8) >> 6) * kKBlockBytes +
+                                  sw128_offset(key, ((ldim + 8) & 63) >> 3)) = v1;
     }
-    const int kb = oc >> 3;
-    *reinterpret_cast<uint4*>(op + kb * kKBlockBytes + sw128_offset(key, oc & 7)) = v;
   }
 }
 
 // Split-K epilogue: write this split's unnormalised O half, its log2-domain
 // reference maximum and its sum; the last split of the row to arrive (per
 // value half) combines all of them and resets the row's arrival counter.
-template <int C>
-__device__ void split_epilogue(const DecodeArgs& a, Ctl* ctl, int64_t t, int split, int ntiles,
+__device__ void split_epilogue(const DecodeArgs& a, Ctl* ctl, int C, int64_t t, int split, int ntiles,
                                float m_ref, float l, uint32_t tb, int warp, int h) {
   const int S = a.splits;
   const bool live = h < a.H;
@@ -365,50 +418,66 @@ __device__ void split_epilogue(const DecodeArgs& a, Ctl* ctl, int64_t t, int spl
   if (h == 0) a.ws_tick[t * 2 + C] = 0;
 }
 
-// Load this CTA's half of q[t, h, :] (bf16) into tensor memory as fp16
-// pairs (the A operand of QK^T), one head row per thread, two 64-dim chunks
-// of loads in flight at a time.
-template <int C>
-__device__ void load_q_to_tmem(const DecodeArgs& a, int64_t t, uint32_t tb, int warp, int h) {
-  using HC = Half<C>;
-  constexpr int kVec = HC::kQkDims / 8;  // 16-byte loads per head row (36)
+// This CTA's 288 q dims of head row h (bf16), as 16-byte loads.
+__device__ __forceinline__ const uint4* q_src(const DecodeArgs& a, int64_t t, int h, int q_dim0) {
   const bool live = h < a.H;
-  const uint4* qsrc = reinterpret_cast<const uint4*>(
-      a.q + (t * a.H + (live ? h : 0)) * SMLA_QK_DIM + HC::kQDim0);
-#pragma unroll 1
-  for (int v0 = 0; v0 < kVec; v0 += 16) {
-    uint4 raw[16];
+  return reinterpret_cast<const uint4*>(a.q + (t * a.H + (live ? h : 0)) * SMLA_QK_DIM + q_dim0);
+}
+
+// First 16 loads of the q row, issued before the CTA's set-up barrier.
+__device__ __forceinline__ void q_prefetch(const DecodeArgs& a, int64_t t, int h, int q_dim0,
+                                           uint4* pre) {
+  const uint4* src = q_src(a, t, h, q_dim0);
+  const bool live = h < a.H;
 #pragma unroll
-    for (int k = 0; k < 16; ++k)
-      raw[k] = (live && v0 + k < kVec) ? __ldg(qsrc + v0 + k) : make_uint4(0, 0, 0, 0);
+  for (int k = 0; k < 16; ++k) pre[k] = live ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
+}
+
+// Store 8 q loads (64 dims) as fp16 pairs into 32 (or 16) TMEM columns.
+__device__ __forceinline__ void q_store_group(const uint4* raw, uint32_t addr, bool full) {
+  uint32_t qr[32];
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {  // 8 loads = 64 dims = 32 TMEM columns
-      const int vg = v0 + 8 * g;
-      if (vg < kVec) {
-        uint32_t qr[32];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint4 v = bf16x8_to_f16x8(raw[8 * g + k]);
-          qr[4 * k + 0] = v.x;
-          qr[4 * k + 1] = v.y;
-          qr[4 * k + 2] = v.z;
-          qr[4 * k + 3] = v.w;
-        }
-        const uint32_t addr = tmem_addr(tb, 32 * warp, kQCol + vg * 4);
-        if (vg + 8 <= kVec)
-          tmem_st32(addr, qr);
-        else
-          tmem_st16(addr, qr);  // trailing 32 dims
-      }
-    }
+  for (int k = 0; k < 8; ++k) {
+    const uint4 v = bf16x8_to_f16x8(raw[k]);
+    qr[4 * k + 0] = v.x;
+    qr[4 * k + 1] = v.y;
+    qr[4 * k + 2] = v.z;
+    qr[4 * k + 3] = v.w;
   }
+  if (full)
+    tmem_st32(addr, qr);
+  else
+    tmem_st16(addr, qr);  // trailing 32 dims
+}
+
+// Load this CTA's 288 q dims of q[t, h, :] into tensor memory as fp16 pairs
+// (the A operand of QK^T), one head row per thread; `pre` holds the first 16
+// loads.
+__device__ void load_q_to_tmem(const DecodeArgs& a, int64_t t, uint32_t tb, int warp, int h,
+                               int q_dim0, const uint4* pre) {
+  constexpr int kVec = kQkDims / 8;  // 36 loads per head row
+  const uint4* src = q_src(a, t, h, q_dim0);
+  const bool live = h < a.H;
+  uint4 rest[kVec - 16];
+#pragma unroll
+  for (int k = 0; k < kVec - 16; ++k)
+    rest[k] = live ? __ldg(src + 16 + k) : make_uint4(0, 0, 0, 0);
+  const uint32_t base = tmem_addr(tb, 32 * warp, kQCol);
+  q_store_group(pre, base, true);
+  q_store_group(pre + 8, base + 32, true);
+  q_store_group(rest, base + 64, true);
+  q_store_group(rest + 8, base + 96, true);
+  uint4 tail[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) tail[k] = (k < kVec - 32) ? rest[16 + k] : make_uint4(0, 0, 0, 0);
+  q_store_group(tail, base + 128, false);
   tmem_st_wait();
 }
 
-template <int C, bool kFused>
-__device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, int64_t t, int split,
-                        uint32_t peer) {
-  using HC = Half<C>;
+template <bool kFused>
+__device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt& hr, int64_t t,
+                        int split, uint32_t peer) {
+  const int C = hr.c;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -427,6 +496,13 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, int64_t t, i
     float l = 0.f;
     uint8_t* xbase = sm + kOffX;
     const uint32_t peer_x0 = map_to_cta(smem_u32(xbase), peer);
+    const uint32_t peer_bar0 = map_to_cta(smem_u32(&ctl->x[0]), peer);
+    const uint32_t peer_bar1 = map_to_cta(smem_u32(&ctl->x[1]), peer);
+    // this CTA expects the peer's partial score tiles of tiles 0 and 1
+    if (h == 0) {
+      if (ntiles > 0) mbar_arrive_expect_tx(&ctl->x[0], kXBytes);
+      if (ntiles > 1) mbar_arrive_expect_tx(&ctl->x[1], kXBytes);
+    }
     bool ok = true;
     for (int i = 0; i < ntiles && ok; ++i) {
       ok = __all_sync(0xffffffffu, wait_bar(&ctl->s_full, i & 1, abort, kWsSFull));
@@ -446,14 +522,15 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, int64_t t, i
       }
       tc_fence_before();
       mbar_arrive(&ctl->s_free);
-      // exchange partial scores with the peer CTA
+      // exchange partial scores with the peer CTA: asynchronous remote stores
+      // counted on the peer's barrier; then wait for the peer's tile on ours
       const int b = i & 1;
       const uint32_t px = peer_x0 + b * kXBytes;
+      const uint32_t pbar = b ? peer_bar1 : peer_bar0;
 #pragma unroll
       for (int j4 = 0; j4 < 16; ++j4)
-        st_cluster_v4(px + (j4 * 128 + h) * 16, s[4 * j4], s[4 * j4 + 1], s[4 * j4 + 2],
-                      s[4 * j4 + 3]);
-      mbar_arrive_remote(&ctl->x[b], peer);
+        st_async_v4(px + (j4 * 128 + h) * 16, s[4 * j4], s[4 * j4 + 1], s[4 * j4 + 2],
+                    s[4 * j4 + 3], pbar);
       ok = __all_sync(0xffffffffu, wait_bar_cluster(&ctl->x[b], (i >> 1) & 1, abort, kWsExchange));
       if (!ok) break;
       const float4* mine = reinterpret_cast<const float4*>(xbase + b * kXBytes);
@@ -465,19 +542,20 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, int64_t t, i
         s[4 * j4 + 2] += v.z;
         s[4 * j4 + 3] += v.w;
       }
-      // raw-score maximum (sm_scale > 0, so it commutes with the scaling)
+      // the buffer is read; it receives tile i + 2 next
+      if (h == 0 && i + 2 < ntiles) mbar_arrive_expect_tx(&ctl->x[b], kXBytes);
       const int valid = min(kTileN, n - i * kTileN);
-      float mx = -INFINITY;
-      if (valid == kTileN) {
+      if (valid < kTileN) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) mx = fmaxf(mx, s[j]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          s[j] = (j < valid) ? s[j] : -INFINITY;
-          mx = fmaxf(mx, s[j]);
-        }
+        for (int j = 0; j < 64; ++j) s[j] = (j < valid) ? s[j] : -INFINITY;
       }
+      float mq[8];  // tree-shaped maximum: 8 independent chains, then 3 levels
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mq[k] = s[k];
+#pragma unroll
+      for (int j = 8; j < 64; ++j) mq[j & 7] = fmaxf(mq[j & 7], s[j]);
+      float mx = fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])),
+                       fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7])));
       mx *= scale_log2;
       float alpha = 1.f;  // this row's rescale factor for O and l
       bool rescale = false;
@@ -563,35 +641,36 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, int64_t t, i
       if (C == 0 && live)
         a.lse[t * a.H + h] = (ntiles == 0) ? -INFINITY : (m_ref + log2f(l)) * kLn2;
     } else if (ok) {
-      split_epilogue<C>(a, ctl, t, split, ntiles, m_ref, l, tb, warp, h);
+      split_epilogue(a, ctl, C, t, split, ntiles, m_ref, l, tb, warp, h);
     }
   } else if (warp < 8) {
     // ------------------------------------------------ gather + dequantise
+    // Thread d owns key d/2 of every tile and its half `part` of the key's
+    // chunks; it loads tile i+1's bytes into registers while it converts
+    // tile i, so no staging buffer sits between HBM and the operand tiles.
     const int d = tid - 128;
-    uint8_t* raw = sm + kOffRaw;
+    const int key = d >> 1;
+    const int part = d & 1;
     uint8_t* op = sm + kOffOp;
-    if (ntiles > 0) {
-      issue_tile_loads<C, kFused>(a, list, list_shard, n, 0, raw, d);
-      cp_async_commit();
-    }
-    for (int i = 0; i < ntiles; ++i) {
-      if (i + 1 < ntiles) {
-        issue_tile_loads<C, kFused>(a, list, list_shard, n, i + 1,
-                                    raw + ((i + 1) & 1) * kRawBytes, d);
-        cp_async_commit();
-        cp_async_wait<1>();
-      } else {
-        cp_async_wait<0>();
-      }
-      bool bad = (i >= 2) && !wait_bar(&ctl->freed[i & 1], ((i - 2) >> 1) & 1, abort, kWsFreed);
-      if (named_bar_or(1, 128, bad || *abort)) break;  // raw tile i landed for all
-      dequant_tile<C>(raw + (i & 1) * kRawBytes, op + (i & 1) * kOpTileBytes,
-                      min(kTileN, n - i * kTileN), d);
+    RowRegs ra, rb;
+    auto convert = [&](const RowRegs& r, int i) -> bool {
+      if (i >= kStages &&
+          !wait_bar(&ctl->freed[i % kStages], ((i - kStages) / kStages) & 1, abort, kWsFreed))
+        return false;
+      store_row_regs(r, op + (i % kStages) * kOpTileBytes, key, key < n - i * kTileN, C, part);
       fence_async_shared();
-      mbar_arrive(&ctl->full[i & 1]);
-      if (named_bar_or(1, 128, *abort != 0)) break;  // raw stage free for reuse
+      mbar_arrive(&ctl->full[i % kStages]);
+      return true;
+    };
+    if (ntiles > 0) load_row_regs<kFused>(a, ctl, list, list_shard, n, 0, key, C, part, ra);
+    for (int i = 0; i < ntiles; i += 2) {
+      if (i + 1 < ntiles)
+        load_row_regs<kFused>(a, ctl, list, list_shard, n, i + 1, key, C, part, rb);
+      if (!convert(ra, i) || i + 1 >= ntiles) break;
+      if (i + 2 < ntiles)
+        load_row_regs<kFused>(a, ctl, list, list_shard, n, i + 2, key, C, part, ra);
+      if (!convert(rb, i + 1)) break;
     }
-    cp_async_wait<0>();
   } else if (lane == 0) {
     // ------------------------------------------------ MMA issue (one thread)
     constexpr uint32_t idesc_qk = idesc_f16_f32(128, kTileN, false, false);
@@ -601,13 +680,13 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, int64_t t, i
     tc_fence_after();
     for (int i = 0; ok && i <= ntiles; ++i) {
       if (i < ntiles) {
-        if (!wait_bar(&ctl->full[i & 1], (i >> 1) & 1, abort, kWsFull)) break;
+        if (!wait_bar(&ctl->full[i % kStages], (i / kStages) & 1, abort, kWsFull)) break;
         if (i > 0 && !wait_bar(&ctl->s_free, (i - 1) & 1, abort, kWsSFree)) break;
         tc_fence_after();
-        const uint32_t base = op0 + (i & 1) * kOpTileBytes;
+        const uint32_t base = op0 + (i % kStages) * kOpTileBytes;
 #pragma unroll
-        for (int k = 0; k < HC::kKSteps; ++k) {
-          const int ldim = HC::kQkLocal0 + 16 * k;  // first tile dim of this K step
+        for (int k = 0; k < kKSteps; ++k) {
+          const int ldim = hr.qk_local0 + 16 * k;  // first tile dim of this K step
           const uint64_t bd =
               sdesc_sw128(base + (ldim >> 6) * kKBlockBytes + (ldim & 63) * 2, 16, 1024);
           mma_ts(tb + kSCol, tb + kQCol + 8 * k, bd, idesc_qk, k > 0);
@@ -618,14 +697,14 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, int64_t t, i
         const int j = i - 1;
         if (!wait_bar(&ctl->p_full, j & 1, abort, kWsPFull)) break;
         tc_fence_after();
-        const uint32_t base = op0 + (j & 1) * kOpTileBytes;
+        const uint32_t base = op0 + (j % kStages) * kOpTileBytes;
 #pragma unroll
         for (int k = 0; k < kTileN / 16; ++k) {
           const uint64_t bd = sdesc_sw128(base + k * 2048, kKBlockBytes, 1024);
           mma_ts(tb + kOCol, tb + kPCol + 8 * k, bd, idesc_pv, (j > 0 || k > 0));
         }
         mma_commit(&ctl->pv_done);
-        mma_commit(&ctl->freed[j & 1]);
+        mma_commit(&ctl->freed[j % kStages]);
       }
     }
     // drain: every MMA issued above has completed before TMEM is released
@@ -642,11 +721,13 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, int64_t t, i
 // Resolve entry j of row `row` to (slot, shard).  Per-shard launch: the
 // entry already is a local slot.  Fused DCP step: the entry is a global
 // position t, owned by shard t mod D at local position t div D (interleave
-// 1), then mapped through that shard's block table.  Returns false for -1 /
-// foreign / invalid entries (recording input errors in `err`).
+// 1), then mapped through that shard's block-table row for this request
+// (cached in the control block).  Returns false for -1 / foreign / invalid
+// entries, recording input errors in `err`.
 template <bool kFused>
-__device__ __forceinline__ bool resolve_entry(const DecodeArgs& a, int64_t row, int32_t req,
-                                              int j, int32_t& slot, int& shard, unsigned& err) {
+__device__ __forceinline__ bool resolve_entry(const DecodeArgs& a, const Ctl* ctl, int64_t row,
+                                              bool req_ok, int j, int32_t& slot, int& shard,
+                                              unsigned& err) {
   if (!kFused) {
     const int32_t v = a.slots[row * a.K + j];
     if (v >= a.num_slots) {
@@ -658,21 +739,21 @@ __device__ __forceinline__ bool resolve_entry(const DecodeArgs& a, int64_t row, 
     return v >= 0;
   }
   const int32_t tk = a.topk[row * a.K + j];
-  if (tk < 0 || req < 0) return false;
+  if (tk < 0 || !req_ok) return false;
   const int d = tk % a.D;
   const int32_t lp = tk / a.D;
   const int32_t col = lp / a.block_size;
-  if (col >= a.bt_width[d]) {
+  if (col >= ctl->bt_width[d]) {
     err |= SMLA_DEVERR_BLOCK_TABLE;
     return false;
   }
-  const int32_t blk = __ldg(a.bts[d] + req * a.bt_stride[d] + col);
+  const int32_t blk = __ldg(ctl->bt_row[d] + col);
   if (blk < 0) {
     err |= SMLA_DEVERR_BLOCK_TABLE;
     return false;
   }
   const int64_t s64 = int64_t(blk) * a.block_size + (lp - col * a.block_size);
-  if (s64 >= a.pool_slots[d]) {
+  if (s64 >= ctl->pool_slots[d]) {
     err |= SMLA_DEVERR_SLOT_RANGE;
     return false;
   }
@@ -700,25 +781,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int e_begin = split * per_split;
   const int e_end = min(a.K, e_begin + per_split);
 
+  const HalfRt hr = half_of(c);
+  uint4 qpre[16];
+  if (warp < 4) q_prefetch(a, t, tid, hr.q_dim0, qpre);  // in flight during set-up
   if (warp == kMmaWarp) {
     tmem_alloc(&ctl->tbase, kTmemCols);
     tmem_relinquish();
   }
   if (tid == 0) {
     mbar_init(&ctl->q_ready, 128);
-    mbar_init(&ctl->full[0], 128);
-    mbar_init(&ctl->full[1], 128);
-    mbar_init(&ctl->freed[0], 1);
-    mbar_init(&ctl->freed[1], 1);
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(&ctl->full[st], 128);
+      mbar_init(&ctl->freed[st], 1);
+    }
     mbar_init(&ctl->s_full, 1);
     mbar_init(&ctl->s_free, 128);
     mbar_init(&ctl->p_full, 128);
     mbar_init(&ctl->pv_done, 1);
-    mbar_init(&ctl->x[0], 128);
-    mbar_init(&ctl->x[1], 128);
+    mbar_init(&ctl->x[0], 1);  // one expect_tx arrival per phase
+    mbar_init(&ctl->x[1], 1);
     mbar_init(&ctl->end, 1);
     ctl->abort = 0;
     fence_mbar_init_cluster();
+  }
+  if (kFused && tid < a.D) {
+    // per-shard pointers of this row's request, read once
+    const int32_t r = a.req_id[t];
+    const bool ok = r >= 0 && r < a.num_reqs;
+    ctl->pool[tid] = a.pools[tid];
+    ctl->bt_row[tid] = a.bts[tid] + (ok ? int64_t(r) * a.bt_stride[tid] : 0);
+    ctl->pool_slots[tid] = a.pool_slots[tid];
+    ctl->bt_width[tid] = a.bt_width[tid];
   }
   tc_fence_before();
   __syncthreads();
@@ -726,10 +819,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     // Q half -> TMEM, overlapping the compaction below
-    if (c == 0)
-      load_q_to_tmem<0>(a, t, ctl->tbase, warp, tid);
-    else
-      load_q_to_tmem<1>(a, t, ctl->tbase, warp, tid);
+    load_q_to_tmem(a, t, ctl->tbase, warp, tid, hr.q_dim0, qpre);
     tc_fence_before();
     mbar_arrive(&ctl->q_ready);
   } else if (warp < 8) {
@@ -743,13 +833,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint8_t* list_shard = sm + kOffListShard;
     constexpr int kPer = kMaxList / 128;
     unsigned err = 0;
-    int32_t req = 0;
+    bool req_ok = true;
     if (kFused) {
-      req = a.req_id[t];
-      if (req < 0 || req >= a.num_reqs) {
-        if (d == 0) err |= SMLA_DEVERR_REQ_ID;
-        req = -1;
-      }
+      const int32_t r = a.req_id[t];
+      req_ok = r >= 0 && r < a.num_reqs;
+      if (!req_ok && d == 0) err |= SMLA_DEVERR_REQ_ID;
     }
     const int j0 = e_begin + d * kPer;
     int32_t vs[kPer];
@@ -759,7 +847,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int k = 0; k < kPer; ++k) {
       vs[k] = -1;
       shards[k] = 0;
-      if (j0 + k < e_end && resolve_entry<kFused>(a, t, req, j0 + k, vs[k], shards[k], err))
+      if (j0 + k < e_end && resolve_entry<kFused>(a, ctl, t, req_ok, j0 + k, vs[k], shards[k], err))
         keep |= 1u << k;
     }
     const int cnt = __popc(keep);
@@ -795,10 +883,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();  // peer barriers initialised before any remote arrive
   tc_fence_after();
 
-  if (c == 0)
-    run_cta<0, kFused>(a, sm, ctl, t, split, peer);
-  else
-    run_cta<1, kFused>(a, sm, ctl, t, split, peer);
+  run_cta<kFused>(a, sm, ctl, hr, t, split, peer);
 
   tc_fence_before();
   __syncthreads();

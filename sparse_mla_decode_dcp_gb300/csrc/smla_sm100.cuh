@@ -41,6 +41,18 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
                :: "r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
+// Asynchronous 16-byte store into another CTA's shared memory (`addr` and
+// `remote_bar` are shared::cluster addresses in that CTA).  Its completion is
+// counted as 16 transaction bytes on that CTA's mbarrier, so the receiver
+// learns the data has landed by waiting on its own barrier, with no fence or
+// arrive on the sending side.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d,
+                                            uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+      :: "r"(addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar) : "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count)
@@ -49,6 +61,13 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 
 __device__ __forceinline__ void fence_mbar_init_cluster() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Arrive once and add `bytes` to the transaction count the current phase
+// waits for.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(smem_u32(bar)),
+               "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
