@@ -164,6 +164,34 @@ smla_status smla_sparse_mla_decode(
     size_t workspace_bytes, void* stream);
 
 /*
+ * Step 2 without caller scratch.  The pages have no counterpart to this call:
+ * it exists for callers that cannot allocate device memory -- code that runs
+ * inside CUDA stream capture, where cudaMalloc is not allowed, or hosts that
+ * forbid device allocation after start-up -- and so cannot provide the
+ * workspace smla_sparse_mla_decode wants.
+ *
+ * Same arguments, semantics and errors as smla_sparse_mla_decode minus the
+ * workspace: the split-K scratch is a library-owned array of
+ * SMLA_NOALLOC_SCRATCH_BYTES in device memory, which every GPU that loads the
+ * library holds until the process exits.  A shape whose scratch need
+ * (smla_decode_workspace_size) exceeds that size returns SMLA_ERR_WORKSPACE
+ * and launches nothing.  The call allocates nothing (no cudaMalloc, no
+ * cudaFree, no allocating library routine); it clears the scratch's arrival
+ * counters with cudaMemsetAsync on `stream` before each launch.
+ *
+ * The first call on a device looks up the array's device address there (with
+ * that device current); make that first call before any stream capture.
+ * Every call on a device shares the one array and it keeps the last call's
+ * contents, so calls that overlap on the GPU (e.g. on two streams at once)
+ * race and must be serialised by the caller.
+ */
+#define SMLA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+smla_status smla_sparse_mla_decode_noalloc(
+    const uint16_t* q, const uint8_t* kv_cache, int64_t num_slots,
+    const int32_t* local_slots, int32_t T, int32_t H, int32_t K,
+    float sm_scale, uint16_t* out, float* lse, void* stream);
+
+/*
  * Steps 1-3 in one launch (fused DCP step for D shards held by one GPU).
  *
  * Computes exactly what the three calls above compute for D shard pools --

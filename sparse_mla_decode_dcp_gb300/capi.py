@@ -46,6 +46,9 @@ SIGNATURES = {
     "smla_sparse_mla_decode": (ctypes.c_int, [
         _c_vp, _c_vp, _c_i64, _c_vp, _c_i32, _c_i32, _c_i32, ctypes.c_float, _c_vp,
         _c_vp, _c_vp, _c_sz, _c_vp]),
+    "smla_sparse_mla_decode_noalloc": (ctypes.c_int, [
+        _c_vp, _c_vp, _c_i64, _c_vp, _c_i32, _c_i32, _c_i32, ctypes.c_float, _c_vp, _c_vp,
+        _c_vp]),
     "smla_dcp_sparse_mla_decode_fused": (ctypes.c_int, [
         _c_vp, _c_i32, _c_i32, _c_i32, ctypes.c_float, _c_vp, _c_vp, _c_i32, _c_i32, _c_i32,
         _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]),
@@ -188,6 +191,41 @@ def sparse_mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, local_slots: torc
         T, H, K, float(sm_scale), out.data_ptr(), lse.data_ptr(), ws_ptr, ws_bytes,
         _stream_ptr(stream, dev))
     _check("smla_sparse_mla_decode", st)
+    return out, lse
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def sparse_mla_decode_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, local_slots: torch.Tensor,
+                              sm_scale: float, *, out: Optional[torch.Tensor] = None,
+                              lse: Optional[torch.Tensor] = None,
+                              stream: Optional[torch.cuda.Stream] = None
+                              ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """smla_sparse_mla_decode without a workspace argument: the split-K scratch
+    is the library's own device array, for callers that cannot allocate device
+    memory (see include/smla.h).  Such callers pass `out` and `lse`; when
+    omitted they are allocated here for convenience."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev)
+    _need(kv_cache, "kv_cache", torch.uint8, dev)
+    _need(local_slots, "local_slots", torch.int32, dev)
+    T, H, Dq = q.shape
+    K = local_slots.shape[1]
+    if Dq != QK_DIM or local_slots.shape[0] != T:
+        raise ValueError("q must be [T, H, 576] and local_slots [T, K]")
+    if kv_cache.dim() != 2 or kv_cache.shape[1] != ROW_BYTES:
+        raise ValueError(f"kv_cache must be [num_slots, {ROW_BYTES}] uint8")
+    if out is None:
+        out = torch.empty((T, H, V_DIM), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, dev)
+    _need(lse, "lse", torch.float32, dev)
+    st = load().smla_sparse_mla_decode_noalloc(
+        q.data_ptr(), kv_cache.data_ptr(), kv_cache.shape[0], local_slots.data_ptr(),
+        T, H, K, float(sm_scale), out.data_ptr(), lse.data_ptr(), _stream_ptr(stream, dev))
+    _check("smla_sparse_mla_decode_noalloc", st)
     return out, lse
 
 

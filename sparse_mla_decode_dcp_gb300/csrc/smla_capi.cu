@@ -19,6 +19,9 @@ inline smla_status from_cuda(cudaError_t e) {
 
 }  // namespace
 
+static_assert(SMLA_NOALLOC_SCRATCH_BYTES == smla::kNoAllocScratchBytes,
+              "header and library agree on the scratch size");
+
 extern "C" {
 
 const char* smla_status_string(smla_status status) {
@@ -110,6 +113,35 @@ smla_status smla_sparse_mla_decode(
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
   return from_cuda(smla::launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+smla_status smla_sparse_mla_decode_noalloc(
+    const uint16_t* q, const uint8_t* kv_cache, int64_t num_slots,
+    const int32_t* local_slots, int32_t T, int32_t H, int32_t K,
+    float sm_scale, uint16_t* out, float* lse, void* stream) {
+  if (T < 0 || K < 1 || H < 1 || num_slots < 0 || !std::isfinite(sm_scale) ||
+      !(sm_scale > 0.f))
+    return SMLA_ERR_INVALID_ARG;
+  if (H > SMLA_MAX_HEADS) return SMLA_ERR_UNSUPPORTED;
+  if (T == 0) return SMLA_OK;
+  if (!q || !kv_cache || !local_slots || !out || !lse) return SMLA_ERR_INVALID_ARG;
+  if (misaligned(q, 16) || misaligned(kv_cache, 16) || misaligned(out, 16) ||
+      misaligned(local_slots, 4) || misaligned(lse, 4))
+    return SMLA_ERR_INVALID_ARG;
+  if (smla::decode_workspace_bytes(T, H, K) > SMLA_NOALLOC_SCRATCH_BYTES)
+    return SMLA_ERR_WORKSPACE;
+  smla::DecodeArgs a{};
+  a.q = q;
+  a.kv = kv_cache;
+  a.num_slots = num_slots;
+  a.slots = local_slots;
+  a.T = T;
+  a.H = H;
+  a.K = K;
+  a.sm_scale = sm_scale;
+  a.out = out;
+  a.lse = lse;
+  return from_cuda(smla::launch_decode_noalloc(a, static_cast<cudaStream_t>(stream)));
 }
 
 smla_status smla_dcp_sparse_mla_decode_fused(

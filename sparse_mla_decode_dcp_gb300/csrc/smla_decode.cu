@@ -46,6 +46,8 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#include <mutex>
+
 #include "../../include/smla.h"
 #include "smla_internal.h"
 #include "smla_sm100.cuh"
@@ -960,6 +962,59 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) { return launch_i
 
 cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s) {
   return launch_impl<true>(a, s);
+}
+
+// ---------------------------------------------------------------------------
+// Decode with library-owned scratch, for callers that cannot allocate device
+// memory themselves.  The split-K scratch lives in this file-scope array; every
+// GPU that loads the library holds it until the process exits.  Host code
+// must not pass the array's name to a kernel (on the host it names a stand-in,
+// not device memory): its device address is looked up once per device with
+// cudaGetSymbolAddress, with that device current, on the first call there.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+cudaError_t noalloc_scratch_ptr(void** ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = p;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_decode_noalloc(const DecodeArgs& args, cudaStream_t s) {
+  const WsLayout w = ws_layout(args.T, args.H, args.K);
+  if (w.total > kNoAllocScratchBytes) return cudaErrorInvalidValue;  // caller checks first
+  DecodeArgs a = args;
+  a.workspace = nullptr;
+  a.workspace_bytes = 0;
+  if (w.total > 0) {
+    void* scratch = nullptr;
+    cudaError_t e = noalloc_scratch_ptr(&scratch);
+    if (e != cudaSuccess) return e;
+    // the arrival counters must start at zero; a call that gave up part-way
+    // could have left them otherwise
+    e = cudaMemsetAsync(static_cast<uint8_t*>(scratch) + w.tick_off, 0, w.total - w.tick_off, s);
+    if (e != cudaSuccess) return e;
+    a.workspace = scratch;
+    a.workspace_bytes = w.total;
+  }
+  return launch_impl<false>(a, s);
 }
 
 cudaError_t decode_error_word(uint32_t* flags, bool clear) {

@@ -61,6 +61,9 @@ struct MergeArgs {
 cudaError_t launch_filter_convert(const IndexArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s);
+// Library-owned split-K scratch (no allocation by anyone at call time).
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+cudaError_t launch_decode_noalloc(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s);
 size_t decode_workspace_bytes(int32_t T, int32_t H, int32_t K);
 
