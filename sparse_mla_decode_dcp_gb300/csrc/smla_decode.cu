@@ -14,11 +14,13 @@
 //     so the 576-wide latent keys are shared by all heads (MQA-style).
 //   * The fp32 accumulator O[128 x 512] alone fills a whole SM's tensor
 //     memory, so CTA c of the pair owns value dims [256c, 256c + 256).  The
-//     QK^T contraction is split by key dimension the same way: CTA 0 does
-//     latent dims 0..255, CTA 1 latent dims 256..511 plus the 64 rope dims.
-//     The two fp32 partial score tiles are exchanged through distributed
-//     shared memory each tile, so no FLOP is recomputed and every cache byte
-//     is read once.  Both CTAs then run the identical online softmax.
+//     QK^T contraction is split by key dimension into equal halves of 288:
+//     CTA 0 does latent dims 0..287, CTA 1 latent dims 288..511 plus the 64
+//     rope dims.  Each CTA gathers the dims it contracts plus its value half
+//     (CTA 0 latent 0..287, CTA 1 latent 256..511 + rope), so only latent
+//     dims 256..287 are fetched twice.  The two fp32 partial score tiles are
+//     exchanged through distributed shared memory each tile, so no FLOP is
+//     recomputed.  Both CTAs then run the identical online softmax.
 //   * Q (this CTA's key-dim half) and P live in tensor memory as the A
 //     operand; K/V tiles are the B operand in shared memory (128-byte
 //     swizzle): one buffer serves as K (K-major) for QK^T and as V
