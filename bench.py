@@ -55,6 +55,9 @@ def parse_args(argv=None):
                    help="fused: one launch per step; pipeline: D x convert + D x decode + merge")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-aux", action="store_true",
+                   help="time the chosen path only: no warm-up or timing of the other path, "
+                        "per-launch decode times, e2e or CPU baseline (profiling runs)")
     p.add_argument("--cpu-sample-tokens", type=int, default=64)
     return p.parse_args(argv)
 
@@ -164,30 +167,37 @@ def profile_traffic(kernel: str, workload: str):
         return None
 
 
-def cpu_baseline(wl, sample_tokens: int):
+def cpu_baseline(wl, sample_tokens: int, min_seconds: float = 10.0, max_passes: int = 200):
     """The float64 oracle as it stands, timed on this host on a bounded sample
     of the same workload: the first `sample_tokens` query rows, every shard's
-    convert + decode, then the merge."""
+    convert + decode, then the merge -- repeated until at least `min_seconds`
+    of CPU work have been timed (one pass of the full workload takes well
+    under a second)."""
     import oracle
     import torch
     n = min(sample_tokens, wl.T)
     q_bits = wl.q[:n].detach().cpu().contiguous().view(torch.int16).numpy().astype(np.uint16)
     pools = [s.pool.cpu().numpy() for s in wl.shards]
+    passes = 0
     t0 = time.perf_counter()
-    outs, lses = [], []
-    for d, s in enumerate(wl.shards):
-        sl, _ = oracle.dcp_filter_convert_index(wl.req_id[:n], s.block_table, wl.topk[:n],
-                                                wl.D, d, wl.spec.block_size)
-        o, l = oracle.sparse_mla_decode(q_bits, pools[d], sl, wl.spec.sm_scale)
-        outs.append(o)
-        lses.append(l)
-    oracle.lse_merge(outs, lses)
-    dt = time.perf_counter() - t0
+    while True:
+        outs, lses = [], []
+        for d, s in enumerate(wl.shards):
+            sl, _ = oracle.dcp_filter_convert_index(wl.req_id[:n], s.block_table, wl.topk[:n],
+                                                    wl.D, d, wl.spec.block_size)
+            o, l = oracle.sparse_mla_decode(q_bits, pools[d], sl, wl.spec.sm_scale)
+            outs.append(o)
+            lses.append(l)
+        oracle.lse_merge(outs, lses)
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds or passes >= max_passes:
+            break
     cores = int(os.environ.get("OMP_NUM_THREADS", os.environ.get("OPENBLAS_NUM_THREADS",
                                                                   os.cpu_count() or 1)))
-    return {"value": n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+    return {"value": passes * n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"first {n} of {wl.T} query rows of {wl.spec.name}, all {wl.D} shards "
-                      f"(convert + decode) + merge, float64 numpy; {dt:.2f} s"}
+                      f"(convert + decode) + merge, float64 numpy, {passes} passes; {dt:.2f} s"}
 
 
 # ------------------------------------------------------------ multi-rank
@@ -309,8 +319,9 @@ def run_gpu(args):
     for _ in range(max(args.warmup, 3)):
         flush.fill_(1)
         main_fn()
-        flush.fill_(1)
-        alt_fn()
+        if not args.no_aux:
+            flush.fill_(1)
+            alt_fn()
     torch.cuda.synchronize()
 
     # Timed region: exactly `steps` steps of the reported path.
@@ -328,12 +339,33 @@ def run_gpu(args):
     clocks = sampler.stop()
     value, ms_per_step = aggregate_throughput(T, args.steps, float(sum(step_ms)), world, dev)
 
+    total_keys = sum(units)
+    peaks = load_peaks()
+    roofline_us = max(
+        2.0 * H * (QK_DIM + V_DIM) * total_keys / (peaks["bf16_tflops"] * 1e12),
+        ROW_BYTES * total_keys / (peaks["hbm_gbs"] * 1e9)) * 1e6
+    if args.no_aux:
+        # profiling run: the chosen path only, one reduced line
+        roof = _roofline("smla_dcp_sparse_mla_decode_fused" if args.path == "fused" else
+                         "smla_sparse_mla_decode", ms_per_step / (1 if args.path == "fused" else D),
+                         total_keys / (1 if args.path == "fused" else D), H, peaks, args.workload)
+        roof["roofline_us_per_step"] = roofline_us
+        if rank == 0:
+            print(json.dumps({
+                "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
+                "higher_is_better": True, "config": {"workload": args.workload, "path": args.path},
+                "roofline": roof, "aux": "skipped (--no-aux)",
+                "gpu_launches": args.steps * main_launches, "clocks": clocks}), flush=True)
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
     # The other form of the same step, and per-launch decode times.
     n_aux = max(10, min(args.steps, 50))
     alt_ms = float(np.mean(_timed_steps(alt_fn, n_aux, flush, stream)))
     dec_ms = _pipeline_decode_ms(step, wl, n_aux, flush, stream)
-    total_keys = sum(units)
-    peaks = load_peaks()
     if args.path == "fused":
         roof = _roofline("smla_dcp_sparse_mla_decode_fused", ms_per_step, total_keys, H, peaks,
                          args.workload)
@@ -343,9 +375,7 @@ def run_gpu(args):
                          args.workload)
         roof["launches_per_step"] = D
     roof["valid_slots_per_shard"] = units
-    roof["roofline_us_per_step"] = max(
-        2.0 * H * (QK_DIM + V_DIM) * total_keys / (peaks["bf16_tflops"] * 1e12),
-        ROW_BYTES * total_keys / (peaks["hbm_gbs"] * 1e9)) * 1e6
+    roof["roofline_us_per_step"] = roofline_us
     pipeline_ms = alt_ms if args.path == "fused" else ms_per_step
     fused_ms = ms_per_step if args.path == "fused" else alt_ms
     per_shard_roof = _roofline("smla_sparse_mla_decode", float(dec_ms.mean()), total_keys / D, H,

@@ -63,7 +63,8 @@ __device__ unsigned int g_decode_error;
 
 constexpr int kTileN = 64;        // keys per tile (MMA N of QK^T, K of PV)
 constexpr int kThreads = 288;     // 9 warps
-constexpr int kStages = 3;        // operand tiles in flight
+constexpr int kStages = 2;        // fp16 operand tiles in flight
+constexpr int kRawStages = 3;     // raw cache-row tiles in flight
 constexpr int kMmaWarp = 8;
 constexpr int kMaxList = 2048;    // compacted slots one cluster handles
 
@@ -77,17 +78,21 @@ constexpr uint32_t kTmemCols = 512;
 // shared-memory layout (offsets from a 1024-byte aligned base)
 constexpr int kKBlockBytes = kTileN * 128;          // 64 keys x 64 fp16
 constexpr int kOpTileBytes = 5 * kKBlockBytes;      // up to 320 key dims
+constexpr int kRawChunks = 13;                      // staged 16-byte chunks per converter
+constexpr int kRawTileBytes = kRawChunks * 128 * 16;  // one tile, all 128 converters
 constexpr int kXBytes = 128 * kTileN * 4;           // fp32 partial S tile
 constexpr int kOffOp = 0;
-constexpr int kOffX = kOffOp + kStages * kOpTileBytes;
-constexpr int kOffList = kOffX + 2 * kXBytes;
+constexpr int kOffRaw = kOffOp + kStages * kOpTileBytes;
+constexpr int kOffX = kOffRaw + kRawStages * kRawTileBytes;
+constexpr int kOffList = kOffX + kXBytes;
 constexpr int kOffListShard = kOffList + kMaxList * 4;  // fused step: shard of each key
 constexpr int kOffCtl = kOffListShard + kMaxList;
 constexpr int kCtlBytes = 1024;
 constexpr int kSmemBytes = kOffCtl + kCtlBytes + 1024;  // + control block + alignment slack
 
 struct Ctl {
-  uint64_t q_ready, full[kStages], freed[kStages], s_full, s_free, p_full, pv_done, x[2], end;
+  uint64_t q_ready, full[kStages], freed[kStages], s_full, s_free, p_full, pv_done, x, x_free,
+      end;
   uint32_t tbase;
   int n_list;
   int abort;
@@ -100,6 +105,7 @@ struct Ctl {
   int32_t bt_width[kMaxMerge];
 };
 static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -114,7 +120,7 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // gives up (diagnostic).
 enum WaitSite : uint32_t {
   kWsSFull = 0, kWsExchange, kWsPvDone, kWsPvLast, kWsFreed, kWsQReady, kWsFull, kWsSFree,
-  kWsPFull, kWsDrain
+  kWsPFull, kWsDrain, kWsXFree
 };
 
 // Every wait is bounded in time (kWaitNs of the global timer); a wait that
@@ -194,9 +200,11 @@ __device__ __forceinline__ uint4 e4m3x8_scaled(uint2 codes, __half2 hi, __half2 
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// 2^x; results below 2^-126 flush to zero (a softmax weight that small is
+// zero in the fp16 P tile anyway)
 __device__ __forceinline__ float ex2(float x) {
   float y;
-  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
@@ -208,7 +216,6 @@ __device__ __forceinline__ float ex2(float x) {
 // two CTAs share one instruction stream (half the code, for the i-cache).
 constexpr int kQkDims = 288;
 constexpr int kKSteps = kQkDims / 16;  // MMA K = 16
-constexpr int kChunksPerThread = 12;   // 16-byte source chunks per gather thread and key
 
 struct HalfRt {
   int c;           // CTA rank in the pair
@@ -224,63 +231,57 @@ __device__ __forceinline__ HalfRt half_of(uint32_t c) {
   return r;
 }
 
-// Gather thread (key, part) of CTA c owns up to 12 source chunks of 16 bytes
-// of every key row.  Chunk k: its byte offset in the 656-byte row, the first
-// tile dim it fills, whether it holds 16 e4m3 codes (two 8-dim output chunks,
-// scale group `group`) or 8 bf16 rope values (one output chunk).
-//   CTA 0: codes [0, 288) = 18 code chunks, 9 per part
-//   CTA 1: codes [256, 512) = 16 code chunks + 8 rope chunks; part 0 takes
-//          code chunks 0..11, part 1 code chunks 12..15 and the rope chunks
-__device__ __forceinline__ void chunk_at(int c, int part, int k, int& src, int& ldim, bool& code,
-                                         int& group) {
-  if (c == 0) {
-    const int ci = 9 * part + k;
-    src = 16 * ci;
-    ldim = 16 * ci;
-    code = true;
-    group = ci >> 3;
-  } else if (part == 0 || k < 4) {
-    const int ci = 12 * part + k;
-    src = 256 + 16 * ci;
-    ldim = 16 * ci;
-    code = true;
-    group = 2 + (ci >> 3);
-  } else {
-    const int r = k - 4;
-    src = 528 + 16 * r;
-    ldim = 256 + 8 * r;
-    code = false;
-    group = 0;
-  }
-}
-
-__device__ __forceinline__ int chunks_of(int c) { return c == 0 ? 9 : 12; }
-
-// Registers one thread holds for one key of one tile.
-struct RowRegs {
-  uint4 chunk[kChunksPerThread];
-  float4 scales;
+// Converter thread (key, part) of CTA c stages and converts up to 12 chunks
+// of 16 bytes of its key's cache row, plus the row's 16 bytes of scales:
+// first `n_code` chunks of 16 e4m3 codes, consecutive in the row from byte
+// `src0` and in the operand tile from dim `ldim0`, then `n_rope` chunks of 8
+// bf16 rope values (row bytes 528 + 16r, tile dims 256 + 8r).
+//   CTA 0: codes [0, 288) = 18 chunks, 9 per part
+//   CTA 1: codes [256, 512) = 16 chunks + 8 rope chunks; part 0 takes code
+//          chunks 0..11, part 1 code chunks 12..15 and the rope chunks
+struct ChunkPlan {
+  int n_code, n_rope, src0, ldim0;
 };
 
-template <bool kFused>
-__device__ __forceinline__ void load_row_regs(const DecodeArgs& a, const Ctl* ctl, const int* list,
-                                              const uint8_t* shard, int n, int tile, int key,
-                                              int c, int part, RowRegs& r) {
-  const int idx = tile * kTileN + key;
-  if (idx >= n) return;
-  const uint8_t* pool = kFused ? ctl->pool[shard[idx]] : a.kv;
-  const uint8_t* row = pool + int64_t(list[idx]) * SMLA_ROW_BYTES;
-  r.scales = __ldg(reinterpret_cast<const float4*>(row + 512));
-  const int nch = chunks_of(c);
-#pragma unroll
-  for (int k = 0; k < kChunksPerThread; ++k) {
-    if (k < nch) {
-      int src, ldim, group;
-      bool code;
-      chunk_at(c, part, k, src, ldim, code, group);
-      r.chunk[k] = __ldg(reinterpret_cast<const uint4*>(row + src));
-    }
+__device__ __forceinline__ ChunkPlan chunk_plan(int c, int part) {
+  ChunkPlan p;
+  if (c == 0) {
+    p.n_code = 9;
+    p.n_rope = 0;
+    p.src0 = 144 * part;
+    p.ldim0 = 144 * part;
+  } else {
+    p.n_code = part ? 4 : 12;
+    p.n_rope = part ? 8 : 0;
+    p.src0 = 256 + 192 * part;
+    p.ldim0 = 192 * part;
   }
+  return p;
+}
+
+constexpr int kSlotBytes = 128 * 16;  // one 16-byte slot of all 128 converters
+
+// Cache row of entry `idx` of the compacted list.
+template <bool kFused>
+__device__ __forceinline__ const uint8_t* row_ptr(const DecodeArgs& a, const Ctl* ctl,
+                                                  const int* list, const uint8_t* shard,
+                                                  int idx) {
+  const uint8_t* pool = kFused ? ctl->pool[shard[idx]] : a.kv;
+  return pool + int64_t(list[idx]) * SMLA_ROW_BYTES;
+}
+
+// Stage this thread's chunks of `row` (nullptr: nothing, past the row's
+// valid count) into its slots of a raw tile: slot k of thread d lives at
+// k * kSlotBytes + 16 d, so a warp's copies and reads of one slot are 512
+// contiguous bytes.  Slot 12 holds the scales.
+__device__ __forceinline__ void stage_row(const uint8_t* row, uint32_t slot0, const ChunkPlan& p) {
+  if (row == nullptr) return;
+  const int n = p.n_code + p.n_rope;
+#pragma unroll 1
+  for (int k = 0; k < n; ++k)
+    cp_async_16(slot0 + k * kSlotBytes,
+                row + (k < p.n_code ? p.src0 + 16 * k : 528 + 16 * (k - p.n_code)));
+  cp_async_16(slot0 + 12 * kSlotBytes, row + 512);
 }
 
 __device__ __forceinline__ void split_scale(float s, __half2& hi, __half2& lo) {
@@ -290,45 +291,96 @@ __device__ __forceinline__ void split_scale(float s, __half2& hi, __half2& lo) {
   lo = __half2half2(__float2half_rn(x - __half2float(h)));
 }
 
-// Convert this thread's chunks of one key into the swizzled fp16 tile (zeros
-// for a key past the row's valid count).
-__device__ __forceinline__ void store_row_regs(const RowRegs& r, uint8_t* op, int key, bool live,
-                                               int c, int part) {
-  __half2 hi[4], lo[4];
-  const __half2 z = __half2half2(__float2half_rn(0.f));
-#pragma unroll
-  for (int g = 0; g < 4; ++g) hi[g] = lo[g] = z;
-  if (live) {
-    split_scale(r.scales.x, hi[0], lo[0]);
-    split_scale(r.scales.y, hi[1], lo[1]);
-    split_scale(r.scales.z, hi[2], lo[2]);
-    split_scale(r.scales.w, hi[3], lo[3]);
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};"
+               :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+__device__ __forceinline__ uint32_t op_addr(uint32_t op, int key, int ldim) {
+  return op + (ldim >> 6) * kKBlockBytes + sw128_offset(key, (ldim & 63) >> 3);
+}
+
+// Convert this thread's staged chunks of its key into the swizzled fp16
+// operand tile at `op` (zeros for a key past the row's valid count).  One
+// rolled loop serves every CTA rank and part (the code stays small enough
+// for the instruction cache); the next chunk's shared load is issued before
+// the current chunk is converted.  A thread's code chunks span at most two
+// scale groups, picked once per key.
+__device__ __forceinline__ void convert_row(uint32_t slot0, uint32_t op, int key, bool live,
+                                            int c, const ChunkPlan& p) {
+  const uint4 s4 = live ? lds128(slot0 + 12 * kSlotBytes) : make_uint4(0, 0, 0, 0);
+  const int abs0 = (c ? 256 : 0) + p.ldim0;  // latent dim of the first code chunk
+  const int ga = abs0 >> 7;                  // its scale group; the other one is ga + 1
+  const float sa = ga == 0 ? __uint_as_float(s4.x) : ga == 1 ? __uint_as_float(s4.y)
+                 : ga == 2 ? __uint_as_float(s4.z) : __uint_as_float(s4.w);
+  const float sb = ga == 0 ? __uint_as_float(s4.y) : ga == 1 ? __uint_as_float(s4.z)
+                                                            : __uint_as_float(s4.w);
+  __half2 ha, la, hb, lb;
+  split_scale(sa, ha, la);
+  split_scale(sb, hb, lb);
+  uint4 nxt = live ? lds128(slot0) : make_uint4(0, 0, 0, 0);
+#pragma unroll 1
+  for (int k = 0; k < p.n_code; ++k) {
+    const uint4 cur = nxt;
+    if (live && k + 1 < p.n_code + p.n_rope) nxt = lds128(slot0 + (k + 1) * kSlotBytes);
+    const int ldim = p.ldim0 + 16 * k;
+    const bool in_b = ((abs0 + 16 * k) >> 7) != ga;
+    const __half2 hh = in_b ? hb : ha, ll = in_b ? lb : la;
+    sts128(op_addr(op, key, ldim), e4m3x8_scaled(make_uint2(cur.x, cur.y), hh, ll));
+    sts128(op_addr(op, key, ldim + 8), e4m3x8_scaled(make_uint2(cur.z, cur.w), hh, ll));
   }
-  const int nch = chunks_of(c);
-#pragma unroll
-  for (int k = 0; k < kChunksPerThread; ++k) {
-    if (k < nch) {
-      int src, ldim, group;
-      bool code;
-      chunk_at(c, part, k, src, ldim, code, group);
-      uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-      if (live) {
-        if (code) {
-          const __half2 hh = group == 0 ? hi[0] : group == 1 ? hi[1] : group == 2 ? hi[2] : hi[3];
-          const __half2 ll = group == 0 ? lo[0] : group == 1 ? lo[1] : group == 2 ? lo[2] : lo[3];
-          v0 = e4m3x8_scaled(make_uint2(r.chunk[k].x, r.chunk[k].y), hh, ll);
-          v1 = e4m3x8_scaled(make_uint2(r.chunk[k].z, r.chunk[k].w), hh, ll);
-        } else {
-          v0 = bf16x8_to_f16x8(r.chunk[k]);
-        }
-      }
-      *reinterpret_cast<uint4*>(op + (ldim >> 6) * kKBlockBytes +
-                                sw128_offset(key, (ldim & 63) >> 3)) = v0;
-      if (code)
-        *reinterpret_cast<uint4*>(op + ((ldim + 8) >> 6) * kKBlockBytes +
-                                  sw128_offset(key, ((ldim + 8) & 63) >> 3)) = v1;
-    }
+#pragma unroll 1
+  for (int r = 0; r < p.n_rope; ++r) {
+    const uint4 cur = nxt;
+    if (live && r + 1 < p.n_rope) nxt = lds128(slot0 + (p.n_code + r + 1) * kSlotBytes);
+    sts128(op_addr(op, key, 256 + 8 * r), bf16x8_to_f16x8(cur));
   }
+}
+
+// One converter thread's tile loop: three tiles of raw rows in flight per
+// thread as cp.async groups, each converted into the fp16 operand stage once
+// the MMAs of the tile two back have released it.  Every thread copies
+// exactly the bytes it later converts, so its own wait_group is the only wait
+// on the raw ring.
+template <bool kFused>
+__device__ void gather_loop(const DecodeArgs& a, Ctl* ctl, uint8_t* sm, int n, int ntiles, int d,
+                            int key, int c, int part, volatile int* abort) {
+  const int* list = reinterpret_cast<const int*>(sm + kOffList);
+  const uint8_t* list_shard = sm + kOffListShard;
+  const uint32_t raw0 = smem_u32(sm + kOffRaw) + d * 16;
+  const uint32_t op0 = smem_u32(sm + kOffOp);
+  const ChunkPlan plan = chunk_plan(c, part);
+  auto row_of = [&](int tile) -> const uint8_t* {
+    const int idx = tile * kTileN + key;
+    return (tile < ntiles && idx < n) ? row_ptr<kFused>(a, ctl, list, list_shard, idx) : nullptr;
+  };
+#pragma unroll 1
+  for (int t = 0; t < kRawStages; ++t) {
+    stage_row(row_of(t), raw0 + t * kRawTileBytes, plan);
+    cp_async_commit();
+  }
+#pragma unroll 1
+  for (int i = 0; i < ntiles; ++i) {
+    cp_async_wait<kRawStages - 1>();  // this thread's copies of tile i have landed
+    if (i >= kStages &&
+        !wait_bar(&ctl->freed[i % kStages], ((i - kStages) / kStages) & 1, abort, kWsFreed))
+      break;
+    const uint32_t slot0 = raw0 + (i % kRawStages) * kRawTileBytes;
+    convert_row(slot0, op0 + (i % kStages) * kOpTileBytes, key, key < n - i * kTileN, c, plan);
+    fence_async_shared();
+    mbar_arrive(&ctl->full[i % kStages]);
+    // the stage is read (by this thread only): refill it with tile i + 3
+    stage_row(row_of(i + kRawStages), slot0, plan);
+    cp_async_commit();
+  }
+  cp_async_wait<0>();  // nothing in flight when the CTA exits
 }
 
 // Split-K epilogue: write this split's unnormalised O half, its log2-domain
@@ -428,15 +480,6 @@ __device__ __forceinline__ const uint4* q_src(const DecodeArgs& a, int64_t t, in
   return reinterpret_cast<const uint4*>(a.q + (t * a.H + (live ? h : 0)) * SMLA_QK_DIM + q_dim0);
 }
 
-// First 16 loads of the q row, issued before the CTA's set-up barrier.
-__device__ __forceinline__ void q_prefetch(const DecodeArgs& a, int64_t t, int h, int q_dim0,
-                                           uint4* pre) {
-  const uint4* src = q_src(a, t, h, q_dim0);
-  const bool live = h < a.H;
-#pragma unroll
-  for (int k = 0; k < 16; ++k) pre[k] = live ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
-}
-
 // Store 8 q loads (64 dims) as fp16 pairs into 32 (or 16) TMEM columns.
 __device__ __forceinline__ void q_store_group(const uint4* raw, uint32_t addr, bool full) {
   uint32_t qr[32];
@@ -455,26 +498,33 @@ __device__ __forceinline__ void q_store_group(const uint4* raw, uint32_t addr, b
 }
 
 // Load this CTA's 288 q dims of q[t, h, :] into tensor memory as fp16 pairs
-// (the A operand of QK^T), one head row per thread; `pre` holds the first 16
-// loads.
+// (the A operand of QK^T), one head row per thread.  The row's 36 16-byte
+// pieces are staged in shared memory with cp.async first (all in flight at
+// once, no registers held), then converted eight at a time.  `stage` is this
+// thread's first slot of the raw ring, idle until the tile loop starts.
 __device__ void load_q_to_tmem(const DecodeArgs& a, int64_t t, uint32_t tb, int warp, int h,
-                               int q_dim0, const uint4* pre) {
-  constexpr int kVec = kQkDims / 8;  // 36 loads per head row
+                               int q_dim0, uint32_t stage) {
+  constexpr int kVec = kQkDims / 8;  // 36 pieces per head row
+  static_assert(kVec * kSlotBytes <= kRawStages * kRawTileBytes, "q staging fits the raw ring");
   const uint4* src = q_src(a, t, h, q_dim0);
   const bool live = h < a.H;
-  uint4 rest[kVec - 16];
-#pragma unroll
-  for (int k = 0; k < kVec - 16; ++k)
-    rest[k] = live ? __ldg(src + 16 + k) : make_uint4(0, 0, 0, 0);
+  if (live) {
+#pragma unroll 1
+    for (int k = 0; k < kVec; ++k) cp_async_16(stage + k * kSlotBytes, src + k);
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
   const uint32_t base = tmem_addr(tb, 32 * warp, kQCol);
-  q_store_group(pre, base, true);
-  q_store_group(pre + 8, base + 32, true);
-  q_store_group(rest, base + 64, true);
-  q_store_group(rest + 8, base + 96, true);
-  uint4 tail[8];
+#pragma unroll 1
+  for (int grp = 0; grp < 5; ++grp) {
+    uint4 g[8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) tail[k] = (k < kVec - 32) ? rest[16 + k] : make_uint4(0, 0, 0, 0);
-  q_store_group(tail, base + 128, false);
+    for (int k = 0; k < 8; ++k) {
+      const int v = 8 * grp + k;
+      g[k] = (live && v < kVec) ? lds128(stage + v * kSlotBytes) : make_uint4(0, 0, 0, 0);
+    }
+    q_store_group(g, base + 32 * grp, grp < 4);
+  }
   tmem_st_wait();
 }
 
@@ -486,8 +536,6 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
   const int warp = tid >> 5;
   const int lane = tid & 31;
   volatile int* abort = &ctl->abort;
-  const int* list = reinterpret_cast<const int*>(sm + kOffList);
-  const uint8_t* list_shard = sm + kOffListShard;
   const int n = ctl->n_list;
   const int ntiles = (n + kTileN - 1) / kTileN;
   const uint32_t tb = ctl->tbase;
@@ -499,14 +547,10 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
     float m_ref = -INFINITY;  // log2-domain reference maximum
     float l = 0.f;
     uint8_t* xbase = sm + kOffX;
-    const uint32_t peer_x0 = map_to_cta(smem_u32(xbase), peer);
-    const uint32_t peer_bar0 = map_to_cta(smem_u32(&ctl->x[0]), peer);
-    const uint32_t peer_bar1 = map_to_cta(smem_u32(&ctl->x[1]), peer);
-    // this CTA expects the peer's partial score tiles of tiles 0 and 1
-    if (h == 0) {
-      if (ntiles > 0) mbar_arrive_expect_tx(&ctl->x[0], kXBytes);
-      if (ntiles > 1) mbar_arrive_expect_tx(&ctl->x[1], kXBytes);
-    }
+    const uint32_t peer_x = map_to_cta(smem_u32(xbase), peer);
+    const uint32_t peer_xbar = map_to_cta(smem_u32(&ctl->x), peer);
+    // this CTA expects the peer's partial score tile of tile 0
+    if (h == 0 && ntiles > 0) mbar_arrive_expect_tx(&ctl->x, kXBytes);
     bool ok = true;
     for (int i = 0; i < ntiles && ok; ++i) {
       ok = __all_sync(0xffffffffu, wait_bar(&ctl->s_full, i & 1, abort, kWsSFull));
@@ -527,17 +571,20 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
       tc_fence_before();
       mbar_arrive(&ctl->s_free);
       // exchange partial scores with the peer CTA: asynchronous remote stores
-      // counted on the peer's barrier; then wait for the peer's tile on ours
-      const int b = i & 1;
-      const uint32_t px = peer_x0 + b * kXBytes;
-      const uint32_t pbar = b ? peer_bar1 : peer_bar0;
+      // counted on the peer's barrier, once the peer has read the previous
+      // tile out of its buffer; then wait for the peer's tile on ours
+      if (i > 0) {
+        ok = __all_sync(0xffffffffu,
+                        wait_bar_cluster(&ctl->x_free, (i - 1) & 1, abort, kWsXFree));
+        if (!ok) break;
+      }
 #pragma unroll
       for (int j4 = 0; j4 < 16; ++j4)
-        st_async_v4(px + (j4 * 128 + h) * 16, s[4 * j4], s[4 * j4 + 1], s[4 * j4 + 2],
-                    s[4 * j4 + 3], pbar);
-      ok = __all_sync(0xffffffffu, wait_bar_cluster(&ctl->x[b], (i >> 1) & 1, abort, kWsExchange));
+        st_async_v4(peer_x + (j4 * 128 + h) * 16, s[4 * j4], s[4 * j4 + 1], s[4 * j4 + 2],
+                    s[4 * j4 + 3], peer_xbar);
+      ok = __all_sync(0xffffffffu, wait_bar_cluster(&ctl->x, i & 1, abort, kWsExchange));
       if (!ok) break;
-      const float4* mine = reinterpret_cast<const float4*>(xbase + b * kXBytes);
+      const float4* mine = reinterpret_cast<const float4*>(xbase);
 #pragma unroll
       for (int j4 = 0; j4 < 16; ++j4) {
         const float4 v = mine[j4 * 128 + h];
@@ -546,8 +593,14 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
         s[4 * j4 + 2] += v.z;
         s[4 * j4 + 3] += v.w;
       }
-      // the buffer is read; it receives tile i + 2 next
-      if (h == 0 && i + 2 < ntiles) mbar_arrive_expect_tx(&ctl->x[b], kXBytes);
+      // the buffer is read: it receives tile i + 1 next (each softmax warp
+      // tells the peer; a transaction count that runs ahead of this
+      // expect_tx is allowed by the barrier)
+      if (i + 1 < ntiles) {
+        if (h == 0) mbar_arrive_expect_tx(&ctl->x, kXBytes);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(&ctl->x_free, peer);
+      }
       const int valid = min(kTileN, n - i * kTileN);
       if (valid < kTileN) {
 #pragma unroll
@@ -583,6 +636,10 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
         ok = __all_sync(0xffffffffu, wait_bar(&ctl->pv_done, (i - 1) & 1, abort, kWsPvDone));
         if (!ok) break;
         tc_fence_after();
+      }
+      // P(i) replaces P(i-1), which PV(i-1) has finished reading
+      tmem_st32(tmem_addr(tb, 32 * warp, kPCol), pk);
+      if (i > 0) {
         // tcgen05.ld/st are warp-collective: the warp rescales together when
         // any of its rows needs it, each lane by its own factor (1 if none)
         if (__any_sync(0xffffffffu, rescale)) {
@@ -598,7 +655,6 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
           }
         }
       }
-      tmem_st32(tmem_addr(tb, 32 * warp, kPCol), pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&ctl->p_full);
@@ -649,32 +705,13 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
     }
   } else if (warp < 8) {
     // ------------------------------------------------ gather + dequantise
-    // Thread d owns key d/2 of every tile and its half `part` of the key's
-    // chunks; it loads tile i+1's bytes into registers while it converts
-    // tile i, so no staging buffer sits between HBM and the operand tiles.
+    // Converter d owns key d % 64 of every tile and half d / 64 of its
+    // chunks, so each warp stores 32 consecutive rows of one chunk column
+    // (conflict-free under the 128-byte swizzle).
     const int d = tid - 128;
-    const int key = d >> 1;
-    const int part = d & 1;
-    uint8_t* op = sm + kOffOp;
-    RowRegs ra, rb;
-    auto convert = [&](const RowRegs& r, int i) -> bool {
-      if (i >= kStages &&
-          !wait_bar(&ctl->freed[i % kStages], ((i - kStages) / kStages) & 1, abort, kWsFreed))
-        return false;
-      store_row_regs(r, op + (i % kStages) * kOpTileBytes, key, key < n - i * kTileN, C, part);
-      fence_async_shared();
-      mbar_arrive(&ctl->full[i % kStages]);
-      return true;
-    };
-    if (ntiles > 0) load_row_regs<kFused>(a, ctl, list, list_shard, n, 0, key, C, part, ra);
-    for (int i = 0; i < ntiles; i += 2) {
-      if (i + 1 < ntiles)
-        load_row_regs<kFused>(a, ctl, list, list_shard, n, i + 1, key, C, part, rb);
-      if (!convert(ra, i) || i + 1 >= ntiles) break;
-      if (i + 2 < ntiles)
-        load_row_regs<kFused>(a, ctl, list, list_shard, n, i + 2, key, C, part, ra);
-      if (!convert(rb, i + 1)) break;
-    }
+    const int key = d & (kTileN - 1);
+    const int part = d >> 6;
+    gather_loop<kFused>(a, ctl, sm, n, ntiles, d, key, C, part, abort);
   } else if (lane == 0) {
     // ------------------------------------------------ MMA issue (one thread)
     constexpr uint32_t idesc_qk = idesc_f16_f32(128, kTileN, false, false);
@@ -744,9 +781,9 @@ __device__ __forceinline__ bool resolve_entry(const DecodeArgs& a, const Ctl* ct
   }
   const int32_t tk = a.topk[row * a.K + j];
   if (tk < 0 || !req_ok) return false;
-  const int d = tk % a.D;
-  const int32_t lp = tk / a.D;
-  const int32_t col = lp / a.block_size;
+  const int32_t lp = int32_t(fastdiv(uint32_t(tk), a.div_D));
+  const int d = tk - lp * a.D;
+  const int32_t col = int32_t(fastdiv(uint32_t(lp), a.div_bs));
   if (col >= ctl->bt_width[d]) {
     err |= SMLA_DEVERR_BLOCK_TABLE;
     return false;
@@ -786,8 +823,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int e_end = min(a.K, e_begin + per_split);
 
   const HalfRt hr = half_of(c);
-  uint4 qpre[16];
-  if (warp < 4) q_prefetch(a, t, tid, hr.q_dim0, qpre);  // in flight during set-up
   if (warp == kMmaWarp) {
     tmem_alloc(&ctl->tbase, kTmemCols);
     tmem_relinquish();
@@ -802,8 +837,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&ctl->s_free, 128);
     mbar_init(&ctl->p_full, 128);
     mbar_init(&ctl->pv_done, 1);
-    mbar_init(&ctl->x[0], 1);  // one expect_tx arrival per phase
-    mbar_init(&ctl->x[1], 1);
+    mbar_init(&ctl->x, 1);       // one expect_tx arrival per phase
+    mbar_init(&ctl->x_free, 4);  // one remote arrival per peer softmax warp
     mbar_init(&ctl->end, 1);
     ctl->abort = 0;
     fence_mbar_init_cluster();
@@ -823,7 +858,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     // Q half -> TMEM, overlapping the compaction below
-    load_q_to_tmem(a, t, ctl->tbase, warp, tid, hr.q_dim0, qpre);
+    load_q_to_tmem(a, t, ctl->tbase, warp, tid, hr.q_dim0, smem_u32(sm + kOffRaw) + tid * 16);
     tc_fence_before();
     mbar_arrive(&ctl->q_ready);
   } else if (warp < 8) {
@@ -962,7 +997,10 @@ cudaError_t launch_impl(const DecodeArgs& args, cudaStream_t s) {
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) { return launch_impl<false>(a, s); }
 
-cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s) {
+cudaError_t launch_decode_fused(const DecodeArgs& args, cudaStream_t s) {
+  DecodeArgs a = args;
+  a.div_D = make_fastdiv(uint32_t(a.D));
+  a.div_bs = make_fastdiv(uint32_t(a.block_size));
   return launch_impl<true>(a, s);
 }
 

@@ -22,6 +22,31 @@ struct IndexArgs {
 
 constexpr int kMaxMerge = 16;
 
+// Division of a non-negative 32-bit int (< 2^31) by a divisor fixed for the
+// whole launch, as a multiply-high, an add and a shift (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994):
+// with s = ceil(log2 d) and m = floor(2^32 (2^s - d) / d) + 1,
+// n / d = (umulhi(n, m) + n) >> s.
+struct FastDiv {
+  uint32_t d, mul, shift;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f;
+  f.d = d;
+  uint32_t s = 0;
+  while ((uint64_t(1) << s) < d) ++s;
+  f.shift = s;
+  f.mul = uint32_t(((uint64_t(1) << 32) * ((uint64_t(1) << s) - d)) / d + 1);
+  return f;
+}
+
+#ifdef __CUDACC__
+__device__ __forceinline__ uint32_t fastdiv(uint32_t n, const FastDiv& f) {
+  return (__umulhi(n, f.mul) + n) >> f.shift;
+}
+#endif
+
 struct DecodeArgs {
   const uint16_t* q;  // bf16 [T, H, 576]
   const uint8_t* kv;  // [num_slots, 656]
@@ -41,6 +66,7 @@ struct DecodeArgs {
   // Fused DCP step only (D > 0): global top-k ids are converted per shard in
   // the kernel prologue and all shards' keys share one softmax.
   int32_t D, block_size, num_reqs;
+  FastDiv div_D, div_bs;  // set by the fused launcher
   const int32_t* req_id;
   const int32_t* topk;
   const uint8_t* pools[kMaxMerge];
