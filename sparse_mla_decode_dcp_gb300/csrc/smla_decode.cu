@@ -14,13 +14,12 @@
 //     so the 576-wide latent keys are shared by all heads (MQA-style).
 //   * The fp32 accumulator O[128 x 512] alone fills a whole SM's tensor
 //     memory, so CTA c of the pair owns value dims [256c, 256c + 256).  The
-//     QK^T contraction is split by key dimension into equal halves of 288:
-//     CTA 0 does latent dims 0..287, CTA 1 latent dims 288..511 plus the 64
-//     rope dims.  Each CTA gathers the dims it contracts plus its value half
-//     (CTA 0 latent 0..287, CTA 1 latent 256..511 + rope), so only latent
-//     dims 256..287 are fetched twice.  The two fp32 partial score tiles are
-//     exchanged through distributed shared memory each tile, so no FLOP is
-//     recomputed.  Both CTAs then run the identical online softmax.
+//     QK^T contraction is split by key dimension the same way: CTA c
+//     contracts latent dims [256c, 256c + 256) (its value half) and rope dims
+//     [32c, 32c + 32), 288 key dims each, so every cache byte is fetched by
+//     one CTA.  The two fp32 partial score tiles are exchanged through
+//     distributed shared memory each tile, so no FLOP is recomputed.  Both
+//     CTAs then run the identical online softmax.
 //   * Q (this CTA's key-dim half) and P live in tensor memory as the A
 //     operand; K/V tiles are the B operand in shared memory (128-byte
 //     swizzle): one buffer serves as K (K-major) for QK^T and as V
@@ -62,10 +61,12 @@ using namespace sm100;
 __device__ unsigned int g_decode_error;
 
 constexpr int kTileN = 64;        // keys per tile (MMA N of QK^T, K of PV)
-constexpr int kThreads = 288;     // 9 warps
-constexpr int kStages = 2;        // fp16 operand tiles in flight
-constexpr int kRawStages = 3;     // raw cache-row tiles in flight
+constexpr int kThreads = 384;     // 12 warps
+constexpr int kStages = 3;        // fp16 operand tiles in flight
+constexpr int kRawStages = 2;     // raw cache-row tiles in flight
 constexpr int kMmaWarp = 8;
+constexpr int kLoaderWarp0 = 9;   // warps 9..11 stage cache rows
+constexpr int kLoaders = 96;
 constexpr int kMaxList = 2048;    // compacted slots one cluster handles
 
 // tensor-memory columns (512 allocated)
@@ -76,23 +77,24 @@ constexpr uint32_t kQCol = 352;   // Q part: 288 fp16 = 144 columns
 constexpr uint32_t kTmemCols = 512;
 
 // shared-memory layout (offsets from a 1024-byte aligned base)
-constexpr int kKBlockBytes = kTileN * 128;          // 64 keys x 64 fp16
-constexpr int kOpTileBytes = 5 * kKBlockBytes;      // up to 320 key dims
-constexpr int kRawChunks = 13;                      // staged 16-byte chunks per converter
-constexpr int kRawTileBytes = kRawChunks * 128 * 16;  // one tile, all 128 converters
+constexpr int kKBlockBytes = kTileN * 128;          // 64 keys x 64 fp16, 128-byte swizzle
+constexpr int kRopeBlock = 4 * kKBlockBytes;        // 64 keys x 32 fp16, 64-byte swizzle
+constexpr int kOpTileBytes = kRopeBlock + kTileN * 64;  // 256 latent + 32 rope dims
+constexpr int kRawStride = 336;                     // staged bytes of one cache row
+constexpr int kRawTileBytes = kTileN * kRawStride;  // one tile of staged rows
 constexpr int kXBytes = 128 * kTileN * 4;           // fp32 partial S tile
 constexpr int kOffOp = 0;
 constexpr int kOffRaw = kOffOp + kStages * kOpTileBytes;
 constexpr int kOffX = kOffRaw + kRawStages * kRawTileBytes;
-constexpr int kOffList = kOffX + kXBytes;
+constexpr int kOffList = kOffX + 2 * kXBytes;  // two exchange buffers
 constexpr int kOffListShard = kOffList + kMaxList * 4;  // fused step: shard of each key
 constexpr int kOffCtl = kOffListShard + kMaxList;
 constexpr int kCtlBytes = 1024;
 constexpr int kSmemBytes = kOffCtl + kCtlBytes + 1024;  // + control block + alignment slack
 
 struct Ctl {
-  uint64_t q_ready, full[kStages], freed[kStages], s_full, s_free, p_full, pv_done, x, x_free,
-      end;
+  uint64_t q_ready, full[kStages], freed[kStages], raw_full[kRawStages], raw_empty[kRawStages],
+      s_full, s_free, p_full, pv_done, x[2], end;
   uint32_t tbase;
   int n_list;
   int abort;
@@ -120,7 +122,7 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // gives up (diagnostic).
 enum WaitSite : uint32_t {
   kWsSFull = 0, kWsExchange, kWsPvDone, kWsPvLast, kWsFreed, kWsQReady, kWsFull, kWsSFree,
-  kWsPFull, kWsDrain, kWsXFree
+  kWsPFull, kWsDrain, kWsRaw, kWsRawEmpty
 };
 
 // Every wait is bounded in time (kWaitNs of the global timer); a wait that
@@ -208,58 +210,44 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// The two CTAs of a pair split the work by key dimension.  CTA 0 gathers
-// latent dims [0, 288) and contracts all of them; CTA 1 gathers latent dims
-// [256, 512) plus the 64 rope dims and contracts key dims [288, 576).  Each
-// contracts 288 key dims (balanced) and holds the 256 value dims of its O
-// half inside its tile.  All of it is runtime data of the CTA's rank, so the
-// two CTAs share one instruction stream (half the code, for the i-cache).
+// The two CTAs of a pair split the work by key dimension, symmetrically:
+// CTA c gathers and contracts latent dims [256c, 256c + 256) (the value dims
+// of its O half) and rope dims [32c, 32c + 32), 288 key dims each, laid out
+// in its operand tile as dims 0..255 (latent) and 256..287 (rope).  Every
+// cache byte is fetched by one CTA (the 16 bytes of scales by both).  All of
+// it is runtime data of the CTA's rank, so the two CTAs share one
+// instruction stream (half the code, for the instruction cache).
 constexpr int kQkDims = 288;
 constexpr int kKSteps = kQkDims / 16;  // MMA K = 16
 
 struct HalfRt {
-  int c;           // CTA rank in the pair
-  int qk_local0;   // first contracted tile dim (0 or 32)
-  int q_dim0;      // first q dim (0 or 288)
+  int c;  // CTA rank in the pair
 };
 
 __device__ __forceinline__ HalfRt half_of(uint32_t c) {
   HalfRt r;
   r.c = int(c);
-  r.qk_local0 = c ? 32 : 0;
-  r.q_dim0 = c ? 288 : 0;
   return r;
 }
 
-// Converter thread (key, part) of CTA c stages and converts up to 12 chunks
-// of 16 bytes of its key's cache row, plus the row's 16 bytes of scales:
-// first `n_code` chunks of 16 e4m3 codes, consecutive in the row from byte
-// `src0` and in the operand tile from dim `ldim0`, then `n_rope` chunks of 8
-// bf16 rope values (row bytes 528 + 16r, tile dims 256 + 8r).
-//   CTA 0: codes [0, 288) = 18 chunks, 9 per part
-//   CTA 1: codes [256, 512) = 16 chunks + 8 rope chunks; part 0 takes code
-//          chunks 0..11, part 1 code chunks 12..15 and the rope chunks
-struct ChunkPlan {
-  int n_code, n_rope, src0, ldim0;
-};
-
-__device__ __forceinline__ ChunkPlan chunk_plan(int c, int part) {
-  ChunkPlan p;
-  if (c == 0) {
-    p.n_code = 9;
-    p.n_rope = 0;
-    p.src0 = 144 * part;
-    p.ldim0 = 144 * part;
-  } else {
-    p.n_code = part ? 4 : 12;
-    p.n_rope = part ? 8 : 0;
-    p.src0 = 256 + 192 * part;
-    p.ldim0 = 192 * part;
-  }
-  return p;
+// The bytes of a cache row CTA c stages, at kRawStride per row, in 21
+// pieces of 16 bytes:
+//   pieces 0..15:  codes [256c, 256c + 256)      -> raw [0, 256)
+//   piece  16:     the four fp32 scales [512, 528) -> raw [256, 272)
+//   pieces 17..20: rope bf16 [528 + 64c, 592 + 64c) -> raw [272, 336)
+constexpr int kPiecesPerRow = 21;
+__device__ __forceinline__ int piece_src(int c, int j) {
+  return j < 16 ? 256 * c + 16 * j : j == 16 ? 512 : 528 + 64 * c + 16 * (j - 17);
 }
+constexpr int kRawScales = 256;
+constexpr int kRawRope = 272;
 
-constexpr int kSlotBytes = 128 * 16;  // one 16-byte slot of all 128 converters
+// Converter thread (key, part) of CTA c converts its key's code pieces
+// [8 part, 8 part + 8) (tile dims 128 part .. 128 part + 127, all in scale
+// group 2c + part) and rope pieces 2 part, 2 part + 1 (tile dims 256 + 16 part
+// .. 256 + 16 part + 15).
+constexpr int kCodePerPart = 8;
+constexpr int kRopePerPart = 2;
 
 // Cache row of entry `idx` of the compacted list.
 template <bool kFused>
@@ -268,20 +256,6 @@ __device__ __forceinline__ const uint8_t* row_ptr(const DecodeArgs& a, const Ctl
                                                   int idx) {
   const uint8_t* pool = kFused ? ctl->pool[shard[idx]] : a.kv;
   return pool + int64_t(list[idx]) * SMLA_ROW_BYTES;
-}
-
-// Stage this thread's chunks of `row` (nullptr: nothing, past the row's
-// valid count) into its slots of a raw tile: slot k of thread d lives at
-// k * kSlotBytes + 16 d, so a warp's copies and reads of one slot are 512
-// contiguous bytes.  Slot 12 holds the scales.
-__device__ __forceinline__ void stage_row(const uint8_t* row, uint32_t slot0, const ChunkPlan& p) {
-  if (row == nullptr) return;
-  const int n = p.n_code + p.n_rope;
-#pragma unroll 1
-  for (int k = 0; k < n; ++k)
-    cp_async_16(slot0 + k * kSlotBytes,
-                row + (k < p.n_code ? p.src0 + 16 * k : 528 + 16 * (k - p.n_code)));
-  cp_async_16(slot0 + 12 * kSlotBytes, row + 512);
 }
 
 __device__ __forceinline__ void split_scale(float s, __half2& hi, __half2& lo) {
@@ -303,84 +277,116 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
                :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
+// Operand tile address of 8 consecutive dims from tile dim `ldim` of `key`:
+// dims 0..255 in four 128-byte-swizzled K-blocks, dims 256..287 (rope) in
+// one 64-byte-swizzled block.
 __device__ __forceinline__ uint32_t op_addr(uint32_t op, int key, int ldim) {
-  return op + (ldim >> 6) * kKBlockBytes + sw128_offset(key, (ldim & 63) >> 3);
+  return ldim < 256 ? op + (ldim >> 6) * kKBlockBytes + sw128_offset(key, (ldim & 63) >> 3)
+                    : op + kRopeBlock + sw64_offset(key, (ldim - 256) >> 3);
 }
 
-// Convert this thread's staged chunks of its key into the swizzled fp16
-// operand tile at `op` (zeros for a key past the row's valid count).  One
-// rolled loop serves every CTA rank and part (the code stays small enough
-// for the instruction cache); the next chunk's shared load is issued before
-// the current chunk is converted.  A thread's code chunks span at most two
-// scale groups, picked once per key.
-__device__ __forceinline__ void convert_row(uint32_t slot0, uint32_t op, int key, bool live,
-                                            int c, const ChunkPlan& p) {
-  const uint4 s4 = live ? lds128(slot0 + 12 * kSlotBytes) : make_uint4(0, 0, 0, 0);
-  const int abs0 = (c ? 256 : 0) + p.ldim0;  // latent dim of the first code chunk
-  const int ga = abs0 >> 7;                  // its scale group; the other one is ga + 1
-  const float sa = ga == 0 ? __uint_as_float(s4.x) : ga == 1 ? __uint_as_float(s4.y)
-                 : ga == 2 ? __uint_as_float(s4.z) : __uint_as_float(s4.w);
-  const float sb = ga == 0 ? __uint_as_float(s4.y) : ga == 1 ? __uint_as_float(s4.z)
-                                                            : __uint_as_float(s4.w);
-  __half2 ha, la, hb, lb;
-  split_scale(sa, ha, la);
-  split_scale(sb, hb, lb);
-  uint4 nxt = live ? lds128(slot0) : make_uint4(0, 0, 0, 0);
+// Convert this thread's staged pieces of its key (`row` = the key's staged
+// row) into the swizzled fp16 operand tile at `op` (zeros for a key past the
+// row's valid count).  One rolled loop serves both CTA ranks and parts (the
+// code stays small enough for the instruction cache); the next piece's
+// shared load is issued before the current piece is converted.  Lanes read
+// rows kRawStride apart: 16-byte accesses of 8 consecutive keys hit 8
+// different bank groups.
+__device__ __forceinline__ void convert_row(uint32_t row, uint32_t op, int key, bool live, int c,
+                                            int part) {
+  __half2 hi = __half2half2(__float2half_rn(0.f)), lo = hi;
+  if (live) {
+    const uint4 s4 = lds128(row + kRawScales);
+    const int g = 2 * c + part;  // the one scale group of this thread's codes
+    split_scale(__uint_as_float(g == 0 ? s4.x : g == 1 ? s4.y : g == 2 ? s4.z : s4.w), hi, lo);
+  }
+  const uint32_t code0 = row + 16 * kCodePerPart * part;
+  uint4 nxt = live ? lds128(code0) : make_uint4(0, 0, 0, 0);
 #pragma unroll 1
-  for (int k = 0; k < p.n_code; ++k) {
+  for (int k = 0; k < kCodePerPart; ++k) {
     const uint4 cur = nxt;
-    if (live && k + 1 < p.n_code + p.n_rope) nxt = lds128(slot0 + (k + 1) * kSlotBytes);
-    const int ldim = p.ldim0 + 16 * k;
-    const bool in_b = ((abs0 + 16 * k) >> 7) != ga;
-    const __half2 hh = in_b ? hb : ha, ll = in_b ? lb : la;
-    sts128(op_addr(op, key, ldim), e4m3x8_scaled(make_uint2(cur.x, cur.y), hh, ll));
-    sts128(op_addr(op, key, ldim + 8), e4m3x8_scaled(make_uint2(cur.z, cur.w), hh, ll));
+    if (live) nxt = lds128(k + 1 < kCodePerPart ? code0 + 16 * (k + 1)
+                                                 : row + kRawRope + 32 * part);
+    const int ldim = 128 * part + 16 * k;
+    sts128(op_addr(op, key, ldim), e4m3x8_scaled(make_uint2(cur.x, cur.y), hi, lo));
+    sts128(op_addr(op, key, ldim + 8), e4m3x8_scaled(make_uint2(cur.z, cur.w), hi, lo));
   }
 #pragma unroll 1
-  for (int r = 0; r < p.n_rope; ++r) {
+  for (int r = 0; r < kRopePerPart; ++r) {
     const uint4 cur = nxt;
-    if (live && r + 1 < p.n_rope) nxt = lds128(slot0 + (p.n_code + r + 1) * kSlotBytes);
-    sts128(op_addr(op, key, 256 + 8 * r), bf16x8_to_f16x8(cur));
+    if (live && r + 1 < kRopePerPart) nxt = lds128(row + kRawRope + 32 * part + 16 * (r + 1));
+    sts128(op_addr(op, key, 256 + 16 * part + 8 * r), bf16x8_to_f16x8(cur));
   }
 }
 
-// One converter thread's tile loop: three tiles of raw rows in flight per
-// thread as cp.async groups, each converted into the fp16 operand stage once
-// the MMAs of the tile two back have released it.  Every thread copies
-// exactly the bytes it later converts, so its own wait_group is the only wait
-// on the raw ring.
+// Stage tile `tile`'s rows into raw stage `stage` with cp.async, the pieces
+// spread over the loader threads so that consecutive lanes copy consecutive
+// 16 bytes of a row (whole sectors, few transactions); each loader then
+// arrives on the stage's barrier when its copies have landed.
 template <bool kFused>
-__device__ void gather_loop(const DecodeArgs& a, Ctl* ctl, uint8_t* sm, int n, int ntiles, int d,
-                            int key, int c, int part, volatile int* abort) {
+__device__ __forceinline__ void stage_tile(const DecodeArgs& a, const Ctl* ctl, const int* list,
+                                           const uint8_t* shard, int n, int tile, uint32_t stage,
+                                           int c, int ld, uint64_t* bar) {
+  const int base = tile * kTileN;
+  const int cnt = min(kTileN, n - base);
+  const int pieces = cnt * kPiecesPerRow;
+#pragma unroll 1
+  for (int p = ld; p < pieces; p += kLoaders) {
+    const int r = int((uint32_t(p) * 3121u) >> 16);  // p / 21, exact for p < 64 * 21
+    const int j = p - r * kPiecesPerRow;
+    const uint8_t* row = row_ptr<kFused>(a, ctl, list, shard, base + r);
+    cp_async_16(stage + r * kRawStride + 16 * j, row + piece_src(c, j));
+  }
+  cp_async_arrive(bar);
+}
+
+// The loader warps' loop: keep kRawStages tiles of raw rows in flight, each
+// stage refilled once the four converter warps have read it.  Copy-issue
+// stalls (the memory system's request slots) fall on these warps, not on the
+// converters.
+template <bool kFused>
+__device__ void loader_loop(const DecodeArgs& a, Ctl* ctl, uint8_t* sm, int n, int ntiles, int c,
+                            int ld, volatile int* abort) {
   const int* list = reinterpret_cast<const int*>(sm + kOffList);
   const uint8_t* list_shard = sm + kOffListShard;
-  const uint32_t raw0 = smem_u32(sm + kOffRaw) + d * 16;
-  const uint32_t op0 = smem_u32(sm + kOffOp);
-  const ChunkPlan plan = chunk_plan(c, part);
-  auto row_of = [&](int tile) -> const uint8_t* {
-    const int idx = tile * kTileN + key;
-    return (tile < ntiles && idx < n) ? row_ptr<kFused>(a, ctl, list, list_shard, idx) : nullptr;
-  };
+  const uint32_t raw0 = smem_u32(sm + kOffRaw);
 #pragma unroll 1
-  for (int t = 0; t < kRawStages; ++t) {
-    stage_row(row_of(t), raw0 + t * kRawTileBytes, plan);
-    cp_async_commit();
+  for (int t = 0; t < ntiles; ++t) {
+    const int st = t % kRawStages;
+    if (t >= kRawStages &&
+        !wait_bar(&ctl->raw_empty[st], ((t - kRawStages) / kRawStages) & 1, abort, kWsRawEmpty))
+      break;
+    stage_tile<kFused>(a, ctl, list, list_shard, n, t, raw0 + st * kRawTileBytes, c, ld,
+                       &ctl->raw_full[st]);
   }
+  // nothing in flight when the CTA exits (the copies above belong to no
+  // commit group until this one)
+  cp_async_commit();
+  cp_async_wait<0>();
+}
+
+// The converter threads' tile loop: each staged tile is converted into the
+// fp16 operand stage once the MMAs of the tile two back have released it,
+// then handed back to the loaders (one arrival per warp).
+__device__ void convert_loop(Ctl* ctl, uint8_t* sm, int n, int ntiles, int key, int c, int part,
+                             int lane, volatile int* abort) {
+  const uint32_t raw0 = smem_u32(sm + kOffRaw);
+  const uint32_t op0 = smem_u32(sm + kOffOp);
 #pragma unroll 1
   for (int i = 0; i < ntiles; ++i) {
-    cp_async_wait<kRawStages - 1>();  // this thread's copies of tile i have landed
+    const int st = i % kRawStages;
+    if (!wait_bar(&ctl->raw_full[st], (i / kRawStages) & 1, abort, kWsRaw)) break;
     if (i >= kStages &&
         !wait_bar(&ctl->freed[i % kStages], ((i - kStages) / kStages) & 1, abort, kWsFreed))
       break;
-    const uint32_t slot0 = raw0 + (i % kRawStages) * kRawTileBytes;
-    convert_row(slot0, op0 + (i % kStages) * kOpTileBytes, key, key < n - i * kTileN, c, plan);
+    convert_row(raw0 + st * kRawTileBytes + key * kRawStride, op0 + (i % kStages) * kOpTileBytes,
+                key, key < n - i * kTileN, c, part);
     fence_async_shared();
     mbar_arrive(&ctl->full[i % kStages]);
-    // the stage is read (by this thread only): refill it with tile i + 3
-    stage_row(row_of(i + kRawStages), slot0, plan);
-    cp_async_commit();
+    // the warp's reads of the raw stage are complete (their values are used)
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->raw_empty[st]);
   }
-  cp_async_wait<0>();  // nothing in flight when the CTA exits
 }
 
 // Split-K epilogue: write this split's unnormalised O half, its log2-domain
@@ -474,10 +480,14 @@ __device__ void split_epilogue(const DecodeArgs& a, Ctl* ctl, int C, int64_t t, 
   if (h == 0) a.ws_tick[t * 2 + C] = 0;
 }
 
-// This CTA's 288 q dims of head row h (bf16), as 16-byte loads.
-__device__ __forceinline__ const uint4* q_src(const DecodeArgs& a, int64_t t, int h, int q_dim0) {
+// Load v (16 bytes, 8 dims) of this CTA's 288 q dims of head row h, in
+// operand-tile order: loads 0..31 are latent dims [256c, 256c + 256), loads
+// 32..35 rope dims [32c, 32c + 32) (q dims 512 + 32c ..).
+__device__ __forceinline__ const uint4* q_src(const DecodeArgs& a, int64_t t, int h, int c,
+                                              int v) {
   const bool live = h < a.H;
-  return reinterpret_cast<const uint4*>(a.q + (t * a.H + (live ? h : 0)) * SMLA_QK_DIM + q_dim0);
+  const uint16_t* row = a.q + (t * a.H + (live ? h : 0)) * SMLA_QK_DIM;
+  return reinterpret_cast<const uint4*>(row + (v < 32 ? 256 * c + 8 * v : 512 + 32 * c + 8 * (v - 32)));
 }
 
 // Store 8 q loads (64 dims) as fp16 pairs into 32 (or 16) TMEM columns.
@@ -497,20 +507,25 @@ __device__ __forceinline__ void q_store_group(const uint4* raw, uint32_t addr, b
     tmem_st16(addr, qr);  // trailing 32 dims
 }
 
+constexpr int kSlotBytes = 128 * 16;  // one 16-byte slot for each of 128 threads
+
 // Load this CTA's 288 q dims of q[t, h, :] into tensor memory as fp16 pairs
 // (the A operand of QK^T), one head row per thread.  The row's 36 16-byte
 // pieces are staged in shared memory with cp.async first (all in flight at
 // once, no registers held), then converted eight at a time.  `stage` is this
-// thread's first slot of the raw ring, idle until the tile loop starts.
+// thread's first slot of the raw ring (ring and exchange buffers are idle
+// until the tile loop starts).
 __device__ void load_q_to_tmem(const DecodeArgs& a, int64_t t, uint32_t tb, int warp, int h,
-                               int q_dim0, uint32_t stage) {
+                               int c, uint32_t stage) {
   constexpr int kVec = kQkDims / 8;  // 36 pieces per head row
-  static_assert(kVec * kSlotBytes <= kRawStages * kRawTileBytes, "q staging fits the raw ring");
-  const uint4* src = q_src(a, t, h, q_dim0);
+  // the staging spans the raw ring and the exchange buffers that follow it:
+  // both are idle until the tile loop, which starts after the cluster barrier
+  static_assert(kOffX == kOffRaw + kRawStages * kRawTileBytes, "ring and buffers are contiguous");
+  static_assert(kVec * kSlotBytes <= kRawStages * kRawTileBytes + 2 * kXBytes, "q staging fits");
   const bool live = h < a.H;
   if (live) {
 #pragma unroll 1
-    for (int k = 0; k < kVec; ++k) cp_async_16(stage + k * kSlotBytes, src + k);
+    for (int k = 0; k < kVec; ++k) cp_async_16(stage + k * kSlotBytes, q_src(a, t, h, c, k));
   }
   cp_async_commit();
   cp_async_wait<0>();
@@ -546,11 +561,18 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
     const float scale_log2 = a.sm_scale * kLog2e;
     float m_ref = -INFINITY;  // log2-domain reference maximum
     float l = 0.f;
+    // The peer's partial score tiles arrive in two buffers used in turn.
+    // The peer writes tile i into buffer i % 2 only after it has received
+    // this CTA's tile i - 1, which this CTA sent after it had read tile i - 2
+    // out of that buffer: no "buffer free" signal is needed.
     uint8_t* xbase = sm + kOffX;
-    const uint32_t peer_x = map_to_cta(smem_u32(xbase), peer);
-    const uint32_t peer_xbar = map_to_cta(smem_u32(&ctl->x), peer);
-    // this CTA expects the peer's partial score tile of tile 0
-    if (h == 0 && ntiles > 0) mbar_arrive_expect_tx(&ctl->x, kXBytes);
+    const uint32_t peer_x0 = map_to_cta(smem_u32(xbase), peer);
+    const uint32_t peer_bar0 = map_to_cta(smem_u32(&ctl->x[0]), peer);
+    const uint32_t peer_bar1 = map_to_cta(smem_u32(&ctl->x[1]), peer);
+    if (h == 0) {
+      if (ntiles > 0) mbar_arrive_expect_tx(&ctl->x[0], kXBytes);
+      if (ntiles > 1) mbar_arrive_expect_tx(&ctl->x[1], kXBytes);
+    }
     bool ok = true;
     for (int i = 0; i < ntiles && ok; ++i) {
       ok = __all_sync(0xffffffffu, wait_bar(&ctl->s_full, i & 1, abort, kWsSFull));
@@ -571,20 +593,17 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
       tc_fence_before();
       mbar_arrive(&ctl->s_free);
       // exchange partial scores with the peer CTA: asynchronous remote stores
-      // counted on the peer's barrier, once the peer has read the previous
-      // tile out of its buffer; then wait for the peer's tile on ours
-      if (i > 0) {
-        ok = __all_sync(0xffffffffu,
-                        wait_bar_cluster(&ctl->x_free, (i - 1) & 1, abort, kWsXFree));
-        if (!ok) break;
-      }
+      // counted on the peer's barrier; then wait for the peer's tile on ours
+      const int b = i & 1;
+      const uint32_t px = peer_x0 + b * kXBytes;
+      const uint32_t pbar = b ? peer_bar1 : peer_bar0;
 #pragma unroll
       for (int j4 = 0; j4 < 16; ++j4)
-        st_async_v4(peer_x + (j4 * 128 + h) * 16, s[4 * j4], s[4 * j4 + 1], s[4 * j4 + 2],
-                    s[4 * j4 + 3], peer_xbar);
-      ok = __all_sync(0xffffffffu, wait_bar_cluster(&ctl->x, i & 1, abort, kWsExchange));
+        st_async_v4(px + (j4 * 128 + h) * 16, s[4 * j4], s[4 * j4 + 1], s[4 * j4 + 2],
+                    s[4 * j4 + 3], pbar);
+      ok = __all_sync(0xffffffffu, wait_bar_cluster(&ctl->x[b], (i >> 1) & 1, abort, kWsExchange));
       if (!ok) break;
-      const float4* mine = reinterpret_cast<const float4*>(xbase);
+      const float4* mine = reinterpret_cast<const float4*>(xbase + b * kXBytes);
 #pragma unroll
       for (int j4 = 0; j4 < 16; ++j4) {
         const float4 v = mine[j4 * 128 + h];
@@ -593,14 +612,8 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
         s[4 * j4 + 2] += v.z;
         s[4 * j4 + 3] += v.w;
       }
-      // the buffer is read: it receives tile i + 1 next (each softmax warp
-      // tells the peer; a transaction count that runs ahead of this
-      // expect_tx is allowed by the barrier)
-      if (i + 1 < ntiles) {
-        if (h == 0) mbar_arrive_expect_tx(&ctl->x, kXBytes);
-        __syncwarp();
-        if (lane == 0) mbar_arrive_remote(&ctl->x_free, peer);
-      }
+      // the buffer is read; it receives tile i + 2 next
+      if (h == 0 && i + 2 < ntiles) mbar_arrive_expect_tx(&ctl->x[b], kXBytes);
       const int valid = min(kTileN, n - i * kTileN);
       if (valid < kTileN) {
 #pragma unroll
@@ -704,14 +717,15 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
       split_epilogue(a, ctl, C, t, split, ntiles, m_ref, l, tb, warp, h);
     }
   } else if (warp < 8) {
-    // ------------------------------------------------ gather + dequantise
+    // ------------------------------------------------ dequantise
     // Converter d owns key d % 64 of every tile and half d / 64 of its
-    // chunks, so each warp stores 32 consecutive rows of one chunk column
+    // pieces, so each warp stores 32 consecutive rows of one chunk column
     // (conflict-free under the 128-byte swizzle).
     const int d = tid - 128;
-    const int key = d & (kTileN - 1);
-    const int part = d >> 6;
-    gather_loop<kFused>(a, ctl, sm, n, ntiles, d, key, C, part, abort);
+    convert_loop(ctl, sm, n, ntiles, d & (kTileN - 1), C, d >> 6, lane, abort);
+  } else if (warp >= kLoaderWarp0) {
+    // ------------------------------------------------ stage cache rows
+    loader_loop<kFused>(a, ctl, sm, n, ntiles, C, tid - 32 * kLoaderWarp0, abort);
   } else if (lane == 0) {
     // ------------------------------------------------ MMA issue (one thread)
     constexpr uint32_t idesc_qk = idesc_f16_f32(128, kTileN, false, false);
@@ -719,34 +733,52 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
     const uint32_t op0 = smem_u32(sm + kOffOp);
     bool ok = wait_bar(&ctl->q_ready, 0, abort, kWsQReady);
     tc_fence_after();
-    for (int i = 0; ok && i <= ntiles; ++i) {
-      if (i < ntiles) {
-        if (!wait_bar(&ctl->full[i % kStages], (i / kStages) & 1, abort, kWsFull)) break;
-        if (i > 0 && !wait_bar(&ctl->s_free, (i - 1) & 1, abort, kWsSFree)) break;
+    // QK^T of tile iq and PV of tile ip are issued in whatever order they
+    // become ready (QK first when both are): PV of a tile is not held behind
+    // the conversion of the next one.  QK(iq) needs its operand stage
+    // converted and S(iq - 1) read by the softmax; PV(ip) needs P(ip).
+    int iq = 0, ip = 0;
+    uint64_t t_progress = globaltimer_ns();
+    uint32_t idle = 0;
+    while (ok && ip < ntiles) {
+      if (iq < ntiles && mbar_test(&ctl->full[iq % kStages], (iq / kStages) & 1) &&
+          (iq == 0 || mbar_test(&ctl->s_free, (iq - 1) & 1))) {
         tc_fence_after();
-        const uint32_t base = op0 + (i % kStages) * kOpTileBytes;
+        const uint32_t base = op0 + (iq % kStages) * kOpTileBytes;
 #pragma unroll
         for (int k = 0; k < kKSteps; ++k) {
-          const int ldim = hr.qk_local0 + 16 * k;  // first tile dim of this K step
+          const int ldim = 16 * k;  // first tile dim of this K step
           const uint64_t bd =
-              sdesc_sw128(base + (ldim >> 6) * kKBlockBytes + (ldim & 63) * 2, 16, 1024);
+              ldim < 256 ? sdesc_sw128(base + (ldim >> 6) * kKBlockBytes + (ldim & 63) * 2, 16, 1024)
+                         : sdesc_sw64(base + kRopeBlock + (ldim - 256) * 2, 16, 512);
           mma_ts(tb + kSCol, tb + kQCol + 8 * k, bd, idesc_qk, k > 0);
         }
         mma_commit(&ctl->s_full);
-      }
-      if (i > 0) {
-        const int j = i - 1;
-        if (!wait_bar(&ctl->p_full, j & 1, abort, kWsPFull)) break;
+        ++iq;
+      } else if (ip < iq && mbar_test(&ctl->p_full, ip & 1)) {
         tc_fence_after();
-        const uint32_t base = op0 + (j % kStages) * kOpTileBytes;
+        const uint32_t base = op0 + (ip % kStages) * kOpTileBytes;
 #pragma unroll
         for (int k = 0; k < kTileN / 16; ++k) {
           const uint64_t bd = sdesc_sw128(base + k * 2048, kKBlockBytes, 1024);
-          mma_ts(tb + kOCol, tb + kPCol + 8 * k, bd, idesc_pv, (j > 0 || k > 0));
+          mma_ts(tb + kOCol, tb + kPCol + 8 * k, bd, idesc_pv, (ip > 0 || k > 0));
         }
         mma_commit(&ctl->pv_done);
-        mma_commit(&ctl->freed[j % kStages]);
+        mma_commit(&ctl->freed[ip % kStages]);
+        ++ip;
+      } else {
+        // nothing ready: yield the issue slots briefly; give up (bounded)
+        __nanosleep(32);
+        if (*abort) break;
+        if ((++idle & 63u) == 0 && globaltimer_ns() - t_progress > kWaitNs) {
+          atomicOr(&g_decode_error,
+                   SMLA_DEVERR_TIMEOUT | (1u << (8 + (iq < ntiles ? kWsFull : kWsPFull))));
+          *abort = 1;
+          break;
+        }
+        continue;
       }
+      t_progress = globaltimer_ns();
     }
     // drain: every MMA issued above has completed before TMEM is released
     // (waited on even after an abort, with its own bound).  A CTA whose row
@@ -837,8 +869,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&ctl->s_free, 128);
     mbar_init(&ctl->p_full, 128);
     mbar_init(&ctl->pv_done, 1);
-    mbar_init(&ctl->x, 1);       // one expect_tx arrival per phase
-    mbar_init(&ctl->x_free, 4);  // one remote arrival per peer softmax warp
+    for (int st = 0; st < kRawStages; ++st) {
+      mbar_init(&ctl->raw_full[st], kLoaders);  // one cp.async arrival per loader
+      mbar_init(&ctl->raw_empty[st], 4);        // one arrival per converter warp
+    }
+    mbar_init(&ctl->x[0], 1);  // one expect_tx arrival per phase
+    mbar_init(&ctl->x[1], 1);
     mbar_init(&ctl->end, 1);
     ctl->abort = 0;
     fence_mbar_init_cluster();
@@ -858,7 +894,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     // Q half -> TMEM, overlapping the compaction below
-    load_q_to_tmem(a, t, ctl->tbase, warp, tid, hr.q_dim0, smem_u32(sm + kOffRaw) + tid * 16);
+    load_q_to_tmem(a, t, ctl->tbase, warp, tid, hr.c, smem_u32(sm + kOffRaw) + tid * 16);
     tc_fence_before();
     mbar_arrive(&ctl->q_ready);
   } else if (warp < 8) {
