@@ -319,50 +319,60 @@ __device__ __forceinline__ void convert_row(uint32_t row, uint32_t op, int key, 
   }
 }
 
-// Stage tile `tile`'s rows into raw stage `stage` with cp.async, the pieces
-// spread over the loader threads so that consecutive lanes copy consecutive
-// 16 bytes of a row (whole sectors, few transactions); each loader then
-// arrives on the stage's barrier when its copies have landed.
-template <bool kFused>
-__device__ __forceinline__ void stage_tile(const DecodeArgs& a, const Ctl* ctl, const int* list,
-                                           const uint8_t* shard, int n, int tile, uint32_t stage,
-                                           int c, int ld, uint64_t* bar) {
-  const int base = tile * kTileN;
-  const int cnt = min(kTileN, n - base);
-  const int pieces = cnt * kPiecesPerRow;
-#pragma unroll 1
-  for (int p = ld; p < pieces; p += kLoaders) {
-    const int r = int((uint32_t(p) * 3121u) >> 16);  // p / 21, exact for p < 64 * 21
-    const int j = p - r * kPiecesPerRow;
-    const uint8_t* row = row_ptr<kFused>(a, ctl, list, shard, base + r);
-    cp_async_16(stage + r * kRawStride + 16 * j, row + piece_src(c, j));
-  }
-  cp_async_arrive(bar);
-}
+// The loader warps' loop.  Loader ld owns pieces ld + 96k (k < 14) of every
+// tile (a tile has 64 rows x 21 pieces = 14 x 96), so consecutive lanes read
+// consecutive 16 bytes of a row (whole sectors, few transactions).  A tile's
+// pieces are loaded into registers while the two raw stages hold the two
+// tiles before it, and stored into a stage once the four converter warps have
+// read that stage's previous tile: three tiles are in flight with two stages
+// of shared memory.  Load-issue stalls (the memory system's request slots)
+// fall on these warps, not on the converters.
+constexpr int kPiecesPerLoader = kTileN * kPiecesPerRow / kLoaders;
+static_assert(kPiecesPerLoader * kLoaders == kTileN * kPiecesPerRow, "loaders share a tile evenly");
 
-// The loader warps' loop: keep kRawStages tiles of raw rows in flight, each
-// stage refilled once the four converter warps have read it.  Copy-issue
-// stalls (the memory system's request slots) fall on these warps, not on the
-// converters.
 template <bool kFused>
 __device__ void loader_loop(const DecodeArgs& a, Ctl* ctl, uint8_t* sm, int n, int ntiles, int c,
                             int ld, volatile int* abort) {
   const int* list = reinterpret_cast<const int*>(sm + kOffList);
   const uint8_t* list_shard = sm + kOffListShard;
   const uint32_t raw0 = smem_u32(sm + kOffRaw);
+  uint4 buf[kPiecesPerLoader];
+  auto load = [&](int tile) {
+    const int base = tile * kTileN;
+    const int pieces = min(kTileN, n - base) * kPiecesPerRow;
+#pragma unroll
+    for (int k = 0; k < kPiecesPerLoader; ++k) {
+      const int p = ld + kLoaders * k;
+      if (p < pieces) {
+        const int r = int((uint32_t(p) * 3121u) >> 16);  // p / 21, exact for p < 64 * 21
+        const int j = p - r * kPiecesPerRow;
+        const uint8_t* row = row_ptr<kFused>(a, ctl, list, list_shard, base + r);
+        buf[k] = __ldg(reinterpret_cast<const uint4*>(row + piece_src(c, j)));
+      }
+    }
+  };
+  auto store = [&](int tile, uint32_t stage) {
+    const int pieces = min(kTileN, n - tile * kTileN) * kPiecesPerRow;
+#pragma unroll
+    for (int k = 0; k < kPiecesPerLoader; ++k) {
+      const int p = ld + kLoaders * k;
+      if (p < pieces) {
+        const int r = int((uint32_t(p) * 3121u) >> 16);
+        sts128(stage + r * kRawStride + 16 * (p - r * kPiecesPerRow), buf[k]);
+      }
+    }
+  };
+  if (ntiles > 0) load(0);
 #pragma unroll 1
   for (int t = 0; t < ntiles; ++t) {
     const int st = t % kRawStages;
     if (t >= kRawStages &&
         !wait_bar(&ctl->raw_empty[st], ((t - kRawStages) / kRawStages) & 1, abort, kWsRawEmpty))
       break;
-    stage_tile<kFused>(a, ctl, list, list_shard, n, t, raw0 + st * kRawTileBytes, c, ld,
-                       &ctl->raw_full[st]);
+    store(t, raw0 + st * kRawTileBytes);
+    mbar_arrive(&ctl->raw_full[st]);
+    if (t + 1 < ntiles) load(t + 1);
   }
-  // nothing in flight when the CTA exits (the copies above belong to no
-  // commit group until this one)
-  cp_async_commit();
-  cp_async_wait<0>();
 }
 
 // The converter threads' tile loop: each staged tile is converted into the
@@ -870,7 +880,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&ctl->p_full, 128);
     mbar_init(&ctl->pv_done, 1);
     for (int st = 0; st < kRawStages; ++st) {
-      mbar_init(&ctl->raw_full[st], kLoaders);  // one cp.async arrival per loader
+      mbar_init(&ctl->raw_full[st], kLoaders);  // one arrival per loader
       mbar_init(&ctl->raw_empty[st], 4);        // one arrival per converter warp
     }
     mbar_init(&ctl->x[0], 1);  // one expect_tx arrival per phase
