@@ -82,19 +82,26 @@ constexpr int kRopeBlock = 4 * kKBlockBytes;        // 64 keys x 32 fp16, 64-byt
 constexpr int kOpTileBytes = kRopeBlock + kTileN * 64;  // 256 latent + 32 rope dims
 constexpr int kRawStride = 336;                     // staged bytes of one cache row
 constexpr int kRawTileBytes = kTileN * kRawStride;  // one tile of staged rows
-constexpr int kXBytes = 128 * kTileN * 4;           // fp32 partial S tile
+// Per tile and direction the pair exchanges the fp32 partial scores of half
+// the tile's keys (XA) and then the fp16 P of the other half plus each row's
+// reference maximum and partial sum (XB).
+constexpr int kXABytes = 128 * (kTileN / 2) * 4;
+constexpr int kXBPBytes = 128 * (kTileN / 2) * 2;
+constexpr int kXBBytes = kXBPBytes + 128 * 8;
+constexpr int kXBytes = kXABytes + kXBBytes;         // one buffer set
 constexpr int kOffOp = 0;
 constexpr int kOffRaw = kOffOp + kStages * kOpTileBytes;
 constexpr int kOffX = kOffRaw + kRawStages * kRawTileBytes;
-constexpr int kOffList = kOffX + 2 * kXBytes;  // two exchange buffers
+constexpr int kOffList = kOffX + 2 * kXBytes;  // two buffer sets
+constexpr int kBtStageMax = 2 * kXBytes / 4;    // staged block-table entries (fused prologue)
 constexpr int kOffListShard = kOffList + kMaxList * 4;  // fused step: shard of each key
 constexpr int kOffCtl = kOffListShard + kMaxList;
 constexpr int kCtlBytes = 1024;
 constexpr int kSmemBytes = kOffCtl + kCtlBytes + 1024;  // + control block + alignment slack
 
 struct Ctl {
-  uint64_t q_ready, full[kStages], freed[kStages], raw_full[kRawStages], raw_empty[kRawStages],
-      s_full, s_free, p_full, pv_done, x[2], end;
+  uint64_t q_tma, q_ready, full[kStages], freed[kStages], raw_full[kRawStages], raw_empty[kRawStages],
+      s_full, s_free, p_full, pv_done, xa[2], xb[2], end;
   uint32_t tbase;
   int n_list;
   int abort;
@@ -105,6 +112,8 @@ struct Ctl {
   const int32_t* bt_row[kMaxMerge];
   int64_t pool_slots[kMaxMerge];
   int32_t bt_width[kMaxMerge];
+  int32_t bt_off[kMaxMerge];  // each shard's staged block-table row in the prologue
+  int bt_staged;              // the rows fit the staging area
 };
 static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -122,7 +131,7 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // gives up (diagnostic).
 enum WaitSite : uint32_t {
   kWsSFull = 0, kWsExchange, kWsPvDone, kWsPvLast, kWsFreed, kWsQReady, kWsFull, kWsSFree,
-  kWsPFull, kWsDrain, kWsRaw, kWsRawEmpty
+  kWsPFull, kWsDrain, kWsRaw, kWsRawEmpty, kWsExchangeP
 };
 
 // Every wait is bounded in time (kWaitNs of the global timer); a wait that
@@ -490,16 +499,6 @@ __device__ void split_epilogue(const DecodeArgs& a, Ctl* ctl, int C, int64_t t, 
   if (h == 0) a.ws_tick[t * 2 + C] = 0;
 }
 
-// Load v (16 bytes, 8 dims) of this CTA's 288 q dims of head row h, in
-// operand-tile order: loads 0..31 are latent dims [256c, 256c + 256), loads
-// 32..35 rope dims [32c, 32c + 32) (q dims 512 + 32c ..).
-__device__ __forceinline__ const uint4* q_src(const DecodeArgs& a, int64_t t, int h, int c,
-                                              int v) {
-  const bool live = h < a.H;
-  const uint16_t* row = a.q + (t * a.H + (live ? h : 0)) * SMLA_QK_DIM;
-  return reinterpret_cast<const uint4*>(row + (v < 32 ? 256 * c + 8 * v : 512 + 32 * c + 8 * (v - 32)));
-}
-
 // Store 8 q loads (64 dims) as fp16 pairs into 32 (or 16) TMEM columns.
 __device__ __forceinline__ void q_store_group(const uint4* raw, uint32_t addr, bool full) {
   uint32_t qr[32];
@@ -517,36 +516,41 @@ __device__ __forceinline__ void q_store_group(const uint4* raw, uint32_t addr, b
     tmem_st16(addr, qr);  // trailing 32 dims
 }
 
-constexpr int kSlotBytes = 128 * 16;  // one 16-byte slot for each of 128 threads
+// q staging in the prologue, in the operand stages (idle until the tile
+// loop): four 16 KB boxes of 64 latent dims x 128 head rows (128-byte
+// swizzle) and one 8 KB box of 32 rope dims x 128 head rows (64-byte
+// swizzle).
+constexpr int kQLatBox = 128 * 128;
+constexpr int kQBytes = 4 * kQLatBox + 128 * 64;
+static_assert(kQBytes <= kStages * kOpTileBytes, "q staging fits the operand stages");
 
-// Load this CTA's 288 q dims of q[t, h, :] into tensor memory as fp16 pairs
-// (the A operand of QK^T), one head row per thread.  The row's 36 16-byte
-// pieces are staged in shared memory with cp.async first (all in flight at
-// once, no registers held), then converted eight at a time.  `stage` is this
-// thread's first slot of the raw ring (ring and exchange buffers are idle
-// until the tile loop starts).
-__device__ void load_q_to_tmem(const DecodeArgs& a, int64_t t, uint32_t tb, int warp, int h,
-                               int c, uint32_t stage) {
-  constexpr int kVec = kQkDims / 8;  // 36 pieces per head row
-  // the staging spans the raw ring and the exchange buffers that follow it:
-  // both are idle until the tile loop, which starts after the cluster barrier
-  static_assert(kOffX == kOffRaw + kRawStages * kRawTileBytes, "ring and buffers are contiguous");
-  static_assert(kVec * kSlotBytes <= kRawStages * kRawTileBytes + 2 * kXBytes, "q staging fits");
-  const bool live = h < a.H;
-  if (live) {
-#pragma unroll 1
-    for (int k = 0; k < kVec; ++k) cp_async_16(stage + k * kSlotBytes, q_src(a, t, h, c, k));
-  }
-  cp_async_commit();
-  cp_async_wait<0>();
+// Issue the TMA loads of this CTA's 288 q dims of token t (latent dims
+// [256c, 256c + 256), rope dims [32c, 32c + 32)) for 128 head rows.
+__device__ __forceinline__ void issue_q_tma(const DecodeArgs& a, int64_t t, int c, uint32_t dst,
+                                            uint64_t* bar) {
+  mbar_arrive_expect_tx(bar, kQBytes);
+  const int32_t y = int32_t(t * a.H);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) tma_load_2d(dst + k * kQLatBox, &a.q_lat, 256 * c + 64 * k, y, bar);
+  tma_load_2d(dst + 4 * kQLatBox, &a.q_rope, 512 + 32 * c, y, bar);
+}
+
+// Convert head row h of the staged q into tensor memory as fp16 pairs (the
+// A operand of QK^T), 64 dims per group of 32 columns; reads follow the
+// boxes' swizzles, so 8 consecutive rows hit 8 different bank groups.
+__device__ void q_to_tmem(uint32_t tb, int warp, int h, bool live, uint32_t src) {
   const uint32_t base = tmem_addr(tb, 32 * warp, kQCol);
 #pragma unroll 1
   for (int grp = 0; grp < 5; ++grp) {
     uint4 g[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int v = 8 * grp + k;
-      g[k] = (live && v < kVec) ? lds128(stage + v * kSlotBytes) : make_uint4(0, 0, 0, 0);
+    for (int v = 0; v < 8; ++v) {
+      uint32_t addr;
+      if (grp < 4)
+        addr = src + grp * kQLatBox + sw128_offset(h, v);
+      else
+        addr = src + 4 * kQLatBox + sw64_offset(h, v & 3);
+      g[v] = (live && (grp < 4 || v < 4)) ? lds128(addr) : make_uint4(0, 0, 0, 0);
     }
     q_store_group(g, base + 32 * grp, grp < 4);
   }
@@ -571,22 +575,37 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
     const float scale_log2 = a.sm_scale * kLog2e;
     float m_ref = -INFINITY;  // log2-domain reference maximum
     float l = 0.f;
-    // The peer's partial score tiles arrive in two buffers used in turn.
-    // The peer writes tile i into buffer i % 2 only after it has received
-    // this CTA's tile i - 1, which this CTA sent after it had read tile i - 2
-    // out of that buffer: no "buffer free" signal is needed.
+    // Key-column split of the softmax: CTA c finishes the scores of keys
+    // [32c, 32c + 32) of each tile (its own partial plus the peer's, XA),
+    // computes their P against a reference maximum, and sends that P, the
+    // reference and the partial sum to the peer (XB); P of all 64 keys then
+    // sits in both CTAs.  Both sides move the shared reference R to the same
+    // max(own reference, peer reference), so O, l and P stay consistent.
+    // Buffers alternate by tile parity: the peer writes tile i into buffer
+    // set i % 2 only after it has received this CTA's tile-i partial scores,
+    // which this CTA sent after it had read tile i - 2 out of that set.
+    const int oc0 = 32 * C;  // this CTA's key columns (the peer's: 32 (1 - C) ..)
     uint8_t* xbase = sm + kOffX;
-    const uint32_t peer_x0 = map_to_cta(smem_u32(xbase), peer);
-    const uint32_t peer_bar0 = map_to_cta(smem_u32(&ctl->x[0]), peer);
-    const uint32_t peer_bar1 = map_to_cta(smem_u32(&ctl->x[1]), peer);
+    const uint32_t peer_x = map_to_cta(smem_u32(xbase), peer);
+    const uint32_t peer_xa0 = map_to_cta(smem_u32(&ctl->xa[0]), peer);
+    const uint32_t peer_xa1 = map_to_cta(smem_u32(&ctl->xa[1]), peer);
+    const uint32_t peer_xb0 = map_to_cta(smem_u32(&ctl->xb[0]), peer);
+    const uint32_t peer_xb1 = map_to_cta(smem_u32(&ctl->xb[1]), peer);
     if (h == 0) {
-      if (ntiles > 0) mbar_arrive_expect_tx(&ctl->x[0], kXBytes);
-      if (ntiles > 1) mbar_arrive_expect_tx(&ctl->x[1], kXBytes);
+      for (int b = 0; b < 2 && b < ntiles; ++b) {
+        mbar_arrive_expect_tx(&ctl->xa[b], kXABytes);
+        mbar_arrive_expect_tx(&ctl->xb[b], kXBBytes);
+      }
     }
-    bool ok = true;
-    for (int i = 0; i < ntiles && ok; ++i) {
-      ok = __all_sync(0xffffffffu, wait_bar(&ctl->s_full, i & 1, abort, kWsSFull));
-      if (!ok) break;
+    // The loop is software-pipelined across tiles: while the P of tile i is
+    // in flight between the CTAs, the scores of tile i + 1 are read and the
+    // peer's half of them sent, so the two exchanges of consecutive tiles
+    // overlap.
+    float sown[32];  // this CTA's partial scores of its own columns, next tile
+    // Read tile t's partial scores (QK^T of tile t done), release S for the
+    // next QK^T, send the peer's columns, keep this CTA's.
+    auto start_tile = [&](int t) -> bool {
+      if (!__all_sync(0xffffffffu, wait_bar(&ctl->s_full, t & 1, abort, kWsSFull))) return false;
       tc_fence_after();
       float s[64];
       {
@@ -602,66 +621,140 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
       }
       tc_fence_before();
       mbar_arrive(&ctl->s_free);
-      // exchange partial scores with the peer CTA: asynchronous remote stores
-      // counted on the peer's barrier; then wait for the peer's tile on ours
+      const int b = t & 1;
+      const uint32_t xa_p = peer_x + b * kXBytes;
+#pragma unroll
+      for (int j4 = 0; j4 < 8; ++j4) {
+        // columns 32 (1 - C) + 4 j4 ..: a select between two static indices
+        const int lo = 4 * j4, hi = 32 + 4 * j4;
+        st_async_v4(xa_p + (j4 * 128 + h) * 16, C ? s[lo] : s[hi], C ? s[lo + 1] : s[hi + 1],
+                    C ? s[lo + 2] : s[hi + 2], C ? s[lo + 3] : s[hi + 3], b ? peer_xa1 : peer_xa0);
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) sown[j] = C ? s[32 + j] : s[j];
+      return true;
+    };
+    bool ok = ntiles == 0 || start_tile(0);
+    for (int i = 0; i < ntiles && ok; ++i) {
       const int b = i & 1;
-      const uint32_t px = peer_x0 + b * kXBytes;
-      const uint32_t pbar = b ? peer_bar1 : peer_bar0;
-#pragma unroll
-      for (int j4 = 0; j4 < 16; ++j4)
-        st_async_v4(px + (j4 * 128 + h) * 16, s[4 * j4], s[4 * j4 + 1], s[4 * j4 + 2],
-                    s[4 * j4 + 3], pbar);
-      ok = __all_sync(0xffffffffu, wait_bar_cluster(&ctl->x[b], (i >> 1) & 1, abort, kWsExchange));
+      const uint32_t xa_l = smem_u32(xbase) + b * kXBytes;  // this CTA's buffer set b
+      const uint32_t xa_p = peer_x + b * kXBytes;           // the peer's
+      // 1) full scores of this CTA's columns of tile i
+      ok = __all_sync(0xffffffffu, wait_bar_cluster(&ctl->xa[b], (i >> 1) & 1, abort, kWsExchange));
       if (!ok) break;
-      const float4* mine = reinterpret_cast<const float4*>(xbase + b * kXBytes);
+      float f[32];
 #pragma unroll
-      for (int j4 = 0; j4 < 16; ++j4) {
-        const float4 v = mine[j4 * 128 + h];
-        s[4 * j4] += v.x;
-        s[4 * j4 + 1] += v.y;
-        s[4 * j4 + 2] += v.z;
-        s[4 * j4 + 3] += v.w;
+      for (int j4 = 0; j4 < 8; ++j4) {
+        const float4 v = ld_shared_f4(xa_l + (j4 * 128 + h) * 16);
+        f[4 * j4] = sown[4 * j4] + v.x;
+        f[4 * j4 + 1] = sown[4 * j4 + 1] + v.y;
+        f[4 * j4 + 2] = sown[4 * j4 + 2] + v.z;
+        f[4 * j4 + 3] = sown[4 * j4 + 3] + v.w;
       }
-      // the buffer is read; it receives tile i + 2 next
-      if (h == 0 && i + 2 < ntiles) mbar_arrive_expect_tx(&ctl->x[b], kXBytes);
-      const int valid = min(kTileN, n - i * kTileN);
-      if (valid < kTileN) {
+      if (h == 0 && i + 2 < ntiles) mbar_arrive_expect_tx(&ctl->xa[b], kXABytes);
+      const int valid = min(kTileN, n - i * kTileN) - oc0;  // valid columns of this CTA's 32
+      if (valid < 32) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) s[j] = (j < valid) ? s[j] : -INFINITY;
+        for (int j = 0; j < 32; ++j) f[j] = (j < valid) ? f[j] : -INFINITY;
       }
-      float mq[8];  // tree-shaped maximum: 8 independent chains, then 3 levels
+      float mq[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mq[k] = s[k];
+      for (int k = 0; k < 8; ++k) mq[k] = f[k];
 #pragma unroll
-      for (int j = 8; j < 64; ++j) mq[j & 7] = fmaxf(mq[j & 7], s[j]);
-      float mx = fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])),
-                       fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7])));
-      mx *= scale_log2;
-      float alpha = 1.f;  // this row's rescale factor for O and l
+      for (int j = 8; j < 32; ++j) mq[j & 7] = fmaxf(mq[j & 7], f[j]);
+      const float mx = scale_log2 * fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])),
+                                          fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7])));
+      // 2) P of this CTA's columns against its reference (R, or its own
+      //    maximum when that exceeds R by more than 2^8)
+      const float my_ref = (mx > m_ref + 8.f) ? mx : m_ref;
+      uint32_t pk[16];
+      float l_part = 0.f;
+      // P against reference `ref` (fp16 pairs, one rounding) and its sum;
+      // nothing valid yet: zeros
+      auto own_p = [&](float ref) {
+        l_part = 0.f;
+        if (ref == -INFINITY) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pk[j] = 0u;
+          return;
+        }
+        float sums[4] = {0.f, 0.f, 0.f, 0.f};
+        const float neg_m = -ref;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float p0 = ex2(fmaf(f[2 * j], scale_log2, neg_m));
+          const float p1 = ex2(fmaf(f[2 * j + 1], scale_log2, neg_m));
+          sums[j & 3] += p0 + p1;
+          pk[j] = h2_bits(__floats2half2_rn(p0, p1));
+        }
+        l_part = (sums[0] + sums[1]) + (sums[2] + sums[3]);
+      };
+      own_p(my_ref);
+      // 3) P, reference and partial sum go to the peer
+      const uint32_t xb_p = xa_p + kXABytes;
+      const uint32_t xbb = b ? peer_xb1 : peer_xb0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        st_async_v4(xb_p + (q * 128 + h) * 16, __uint_as_float(pk[4 * q]),
+                    __uint_as_float(pk[4 * q + 1]), __uint_as_float(pk[4 * q + 2]),
+                    __uint_as_float(pk[4 * q + 3]), xbb);
+      st_async_v2(xb_p + kXBPBytes + h * 8, my_ref, l_part, xbb);
+      // 4) while that is in flight: tile i + 1's scores (its QK^T could start
+      //    once S(i) was read)
+      if (i + 1 < ntiles && !start_tile(i + 1)) {
+        ok = false;
+        break;
+      }
+      // 5) the peer's P of tile i
+      ok = __all_sync(0xffffffffu, wait_bar_cluster(&ctl->xb[b], (i >> 1) & 1, abort, kWsExchangeP));
+      if (!ok) break;
+      const uint32_t xb_l = xa_l + kXABytes;
+      uint32_t pp[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = lds128(xb_l + (q * 128 + h) * 16);
+        pp[4 * q] = v.x;
+        pp[4 * q + 1] = v.y;
+        pp[4 * q + 2] = v.z;
+        pp[4 * q + 3] = v.w;
+      }
+      const float2 peer_rl = ld_shared_f2(xb_l + kXBPBytes + h * 8);
+      if (h == 0 && i + 2 < ntiles) mbar_arrive_expect_tx(&ctl->xb[b], kXBBytes);
+      // 6) the shared reference moves to the larger of the two (identically
+      //    on both CTAs); what was computed against a smaller one is redone
+      const float r_new = fmaxf(my_ref, peer_rl.x);
+      float alpha = 1.f;  // O and l
       bool rescale = false;
-      if (mx > m_ref + 8.f) {
-        alpha = ex2(m_ref - mx);  // 0 on the first tile
-        m_ref = mx;
+      if (r_new != m_ref) {
+        alpha = ex2(m_ref - r_new);  // 0 while nothing was valid yet
         rescale = (i > 0);
       }
-      const float neg_m = -m_ref;
-      float sums[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[32];
+      // own P against a smaller reference: recomputed from the fp32 scores
+      // (one rounding); the peer's: scaled in fp32 and rounded once more
+      if (my_ref != r_new) own_p(r_new);
+      float l_peer = peer_rl.y;
+      if (peer_rl.x != r_new) {
+        const float fp = (peer_rl.x == -INFINITY) ? 0.f : ex2(peer_rl.x - r_new);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float p0 = ex2(fmaf(s[2 * j], scale_log2, neg_m));
-        const float p1 = ex2(fmaf(s[2 * j + 1], scale_log2, neg_m));
-        sums[j & 3] += p0 + p1;
-        pk[j] = h2_bits(__floats2half2_rn(p0, p1));
+        for (int j = 0; j < 16; ++j) {
+          const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&pp[j]));
+          pp[j] = h2_bits(__floats2half2_rn(v.x * fp, v.y * fp));
+        }
+        l_peer *= fp;
       }
-      l = l * alpha + ((sums[0] + sums[1]) + (sums[2] + sums[3]));
+      const float l_own = l_part;
+      m_ref = r_new;
+      // the same sum on both CTAs: keys 0..31 first, then 32..63
+      l = l * alpha + (C ? l_peer + l_own : l_own + l_peer);
       if (i > 0) {
         ok = __all_sync(0xffffffffu, wait_bar(&ctl->pv_done, (i - 1) & 1, abort, kWsPvDone));
         if (!ok) break;
         tc_fence_after();
       }
-      // P(i) replaces P(i-1), which PV(i-1) has finished reading
-      tmem_st32(tmem_addr(tb, 32 * warp, kPCol), pk);
+      // P(i) replaces P(i-1), which PV(i-1) has finished reading: keys
+      // 0..31 in columns 0..15, keys 32..63 in columns 16..31
+      tmem_st16(tmem_addr(tb, 32 * warp, kPCol + 16 * C), pk);
+      tmem_st16(tmem_addr(tb, 32 * warp, kPCol + 16 * (1 - C)), pp);
       if (i > 0) {
         // tcgen05.ld/st are warp-collective: the warp rescales together when
         // any of its rows needs it, each lane by its own factor (1 if none)
@@ -801,18 +894,18 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
   }
 }
 
-// Resolve entry j of row `row` to (slot, shard).  Per-shard launch: the
-// entry already is a local slot.  Fused DCP step: the entry is a global
-// position t, owned by shard t mod D at local position t div D (interleave
-// 1), then mapped through that shard's block-table row for this request
-// (cached in the control block).  Returns false for -1 / foreign / invalid
-// entries, recording input errors in `err`.
+// Resolve raw entry v to (slot, shard).  Per-shard launch: the entry
+// already is a local slot.  Fused DCP step: the entry is a global position
+// v, owned by shard v mod D at local position v div D (interleave 1), then
+// mapped through that shard's block-table row for this request (staged in
+// shared memory at `bt` when it fits, else read from global memory).
+// Returns false for -1 / foreign / invalid entries, recording input errors
+// in `err`.
 template <bool kFused>
-__device__ __forceinline__ bool resolve_entry(const DecodeArgs& a, const Ctl* ctl, int64_t row,
-                                              bool req_ok, int j, int32_t& slot, int& shard,
+__device__ __forceinline__ bool resolve_entry(const DecodeArgs& a, const Ctl* ctl, const int32_t* bt,
+                                              bool req_ok, int32_t v, int32_t& slot, int& shard,
                                               unsigned& err) {
   if (!kFused) {
-    const int32_t v = a.slots[row * a.K + j];
     if (v >= a.num_slots) {
       err |= SMLA_DEVERR_SLOT_RANGE;
       return false;
@@ -821,16 +914,15 @@ __device__ __forceinline__ bool resolve_entry(const DecodeArgs& a, const Ctl* ct
     shard = 0;
     return v >= 0;
   }
-  const int32_t tk = a.topk[row * a.K + j];
-  if (tk < 0 || !req_ok) return false;
-  const int32_t lp = int32_t(fastdiv(uint32_t(tk), a.div_D));
-  const int d = tk - lp * a.D;
+  if (v < 0 || !req_ok) return false;
+  const int32_t lp = int32_t(fastdiv(uint32_t(v), a.div_D));
+  const int d = v - lp * a.D;
   const int32_t col = int32_t(fastdiv(uint32_t(lp), a.div_bs));
   if (col >= ctl->bt_width[d]) {
     err |= SMLA_DEVERR_BLOCK_TABLE;
     return false;
   }
-  const int32_t blk = __ldg(ctl->bt_row[d] + col);
+  const int32_t blk = ctl->bt_staged ? bt[ctl->bt_off[d] + col] : __ldg(ctl->bt_row[d] + col);
   if (blk < 0) {
     err |= SMLA_DEVERR_BLOCK_TABLE;
     return false;
@@ -870,6 +962,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (tid == 0) {
+    mbar_init(&ctl->q_tma, 1);
     mbar_init(&ctl->q_ready, 128);
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&ctl->full[st], 128);
@@ -883,11 +976,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->raw_full[st], kLoaders);  // one arrival per loader
       mbar_init(&ctl->raw_empty[st], 4);        // one arrival per converter warp
     }
-    mbar_init(&ctl->x[0], 1);  // one expect_tx arrival per phase
-    mbar_init(&ctl->x[1], 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&ctl->xa[b], 1);  // one expect_tx arrival per phase
+      mbar_init(&ctl->xb[b], 1);
+    }
     mbar_init(&ctl->end, 1);
     ctl->abort = 0;
     fence_mbar_init_cluster();
+    // q lands in the (still idle) operand stages while the CTA sets up
+    issue_q_tma(a, t, hr.c, smem_u32(sm + kOffOp), &ctl->q_tma);
   }
   if (kFused && tid < a.D) {
     // per-shard pointers of this row's request, read once
@@ -898,13 +995,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ctl->pool_slots[tid] = a.pool_slots[tid];
     ctl->bt_width[tid] = a.bt_width[tid];
   }
+  if (kFused && tid == 0) {
+    // the request's block-table rows of all shards, staged in the exchange
+    // buffers (idle until the tile loop) when they fit
+    int off = 0;
+    for (int d = 0; d < a.D; ++d) {
+      ctl->bt_off[d] = off;
+      off += a.bt_width[d];
+    }
+    ctl->bt_staged = off <= kBtStageMax;
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
 
   if (warp < 4) {
     // Q half -> TMEM, overlapping the compaction below
-    load_q_to_tmem(a, t, ctl->tbase, warp, tid, hr.c, smem_u32(sm + kOffRaw) + tid * 16);
+    // the whole q tile landed (issued by thread 0 before the set-up barrier)
+    bool qok = wait_bar(&ctl->q_tma, 0, &ctl->abort, kWsQReady);
+    q_to_tmem(ctl->tbase, warp, tid, qok && tid < a.H, smem_u32(sm + kOffOp));
     tc_fence_before();
     mbar_arrive(&ctl->q_ready);
   } else if (warp < 8) {
@@ -924,15 +1033,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       req_ok = r >= 0 && r < a.num_reqs;
       if (!req_ok && d == 0) err |= SMLA_DEVERR_REQ_ID;
     }
+    // 1) this thread's 16 raw entries, all loads in flight at once (four
+    //    16-byte loads when the row allows), and, for the fused step, the
+    //    request's block-table rows copied into shared memory by all 128
+    //    threads; one memory round trip for both
     const int j0 = e_begin + d * kPer;
+    const int32_t* src = (kFused ? a.topk : a.slots) + t * a.K;
     int32_t vs[kPer];
+    if (j0 + kPer <= e_end && (reinterpret_cast<uintptr_t>(src + j0) & 15u) == 0) {
+#pragma unroll
+      for (int q4 = 0; q4 < kPer / 4; ++q4) {
+        const int4 w = __ldg(reinterpret_cast<const int4*>(src + j0) + q4);
+        vs[4 * q4] = w.x;
+        vs[4 * q4 + 1] = w.y;
+        vs[4 * q4 + 2] = w.z;
+        vs[4 * q4 + 3] = w.w;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) vs[k] = (j0 + k < e_end) ? __ldg(src + j0 + k) : -1;
+    }
+    int32_t* bt = reinterpret_cast<int32_t*>(sm + kOffX);
+    if (kFused && ctl->bt_staged) {
+      const uint32_t bt0 = smem_u32(bt);
+#pragma unroll 1
+      for (int sd = 0; sd < a.D; ++sd) {
+#pragma unroll 1
+        for (int col = d; col < ctl->bt_width[sd]; col += 128)
+          cp_async_4(bt0 + 4u * uint32_t(ctl->bt_off[sd] + col), ctl->bt_row[sd] + col);
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+      named_bar_sync(3, 128);  // every thread's copies are visible
+    }
+    // 2) resolve the 16 entries from registers and shared memory
     int shards[kPer];
     unsigned keep = 0;
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
+      const int32_t v = vs[k];
       vs[k] = -1;
       shards[k] = 0;
-      if (j0 + k < e_end && resolve_entry<kFused>(a, ctl, t, req_ok, j0 + k, vs[k], shards[k], err))
+      if (j0 + k < e_end && resolve_entry<kFused>(a, ctl, bt, req_ok, v, vs[k], shards[k], err))
         keep |= 1u << k;
     }
     const int cnt = __popc(keep);
@@ -1015,9 +1157,57 @@ size_t decode_workspace_bytes(int32_t T, int32_t H, int32_t K) {
 
 namespace {
 
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link-time
+// dependency on the driver library).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+cudaError_t encode_tiled_fn(EncodeTiledFn* fn) {
+  static std::mutex m;
+  static EncodeTiledFn cached = nullptr;
+  std::lock_guard<std::mutex> lock(m);
+  if (cached == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    const cudaError_t e = cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || p == nullptr) return cudaErrorNotSupported;
+    cached = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  *fn = cached;
+  return cudaSuccess;
+}
+
+// Tensor maps over q viewed as [T*H rows, 576] bf16: boxes of 64 dims x 128
+// rows with 128-byte swizzle, and 32 dims x 128 rows with 64-byte swizzle.
+// Rows past T*H read as zeros.
+cudaError_t encode_q_maps(DecodeArgs& a) {
+  EncodeTiledFn enc = nullptr;
+  cudaError_t e = encode_tiled_fn(&enc);
+  if (e != cudaSuccess) return e;
+  const cuuint64_t dims[2] = {SMLA_QK_DIM, cuuint64_t(a.T) * cuuint64_t(a.H)};
+  const cuuint64_t strides[1] = {SMLA_QK_DIM * sizeof(uint16_t)};
+  const cuuint32_t box_lat[2] = {64, 128}, box_rope[2] = {32, 128}, ones[2] = {1, 1};
+  void* q = const_cast<uint16_t*>(a.q);
+  if (enc(&a.q_lat, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, dims, strides, box_lat, ones,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+      enc(&a.q_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, dims, strides, box_rope, ones,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  return cudaSuccess;
+}
+
 template <bool kFused>
 cudaError_t launch_impl(const DecodeArgs& args, cudaStream_t s) {
   DecodeArgs a = args;
+  {
+    const cudaError_t e = encode_q_maps(a);
+    if (e != cudaSuccess) return e;
+  }
   a.splits = decode_splits(a.T, a.K);
   const WsLayout w = ws_layout(a.T, a.H, a.K);
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);

@@ -2,6 +2,7 @@
 // translation units.  Not installed; the public surface is include/smla.h.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -67,6 +68,9 @@ struct DecodeArgs {
   // the kernel prologue and all shards' keys share one softmax.
   int32_t D, block_size, num_reqs;
   FastDiv div_D, div_bs;  // set by the fused launcher
+  // q [T*H, 576] bf16 for TMA, set by the launcher: boxes of 64 dims x 128
+  // head rows (128-byte swizzle) and 32 dims x 128 head rows (64-byte swizzle)
+  CUtensorMap q_lat, q_rope;
   const int32_t* req_id;
   const int32_t* topk;
   const uint8_t* pools[kMaxMerge];
