@@ -62,8 +62,8 @@ __device__ unsigned int g_decode_error;
 
 constexpr int kTileN = 64;        // keys per tile (MMA N of QK^T, K of PV)
 constexpr int kThreads = 384;     // 12 warps
-constexpr int kStages = 3;        // fp16 operand tiles in flight
-constexpr int kRawStages = 2;     // raw cache-row tiles in flight
+constexpr int kStages = 4;        // fp16 operand tiles in flight
+constexpr int kRawStages = 1;     // raw cache-row tiles in shared memory (one more in registers)
 constexpr int kMmaWarp = 8;
 constexpr int kLoaderWarp0 = 9;   // warps 9..11 stage cache rows
 constexpr int kLoaders = 96;
