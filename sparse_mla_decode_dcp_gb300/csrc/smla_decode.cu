@@ -294,48 +294,52 @@ __device__ __forceinline__ uint32_t op_addr(uint32_t op, int key, int ldim) {
                     : op + kRopeBlock + sw64_offset(key, (ldim - 256) >> 3);
 }
 
-// Convert this thread's staged pieces of its key (`row` = the key's staged
-// row) into the swizzled fp16 operand tile at `op` (zeros for a key past the
-// row's valid count).  One rolled loop serves both CTA ranks and parts (the
-// code stays small enough for the instruction cache); the next piece's
-// shared load is issued before the current piece is converted.  Lanes read
-// rows kRawStride apart: 16-byte accesses of 8 consecutive keys hit 8
-// different bank groups.
-__device__ __forceinline__ void convert_row(uint32_t row, uint32_t op, int key, bool live, int c,
-                                            int part) {
-  __half2 hi = __half2half2(__float2half_rn(0.f)), lo = hi;
-  if (live) {
-    const uint4 s4 = lds128(row + kRawScales);
-    const int g = 2 * c + part;  // the one scale group of this thread's codes
-    split_scale(__uint_as_float(g == 0 ? s4.x : g == 1 ? s4.y : g == 2 ? s4.z : s4.w), hi, lo);
-  }
+// One converter thread's staged pieces of its key: 8 code pieces, 2 rope
+// pieces and the scale of its code pieces' group.
+struct ConvRegs {
+  uint4 cur[kCodePerPart + kRopePerPart];
+  float scale;
+};
+
+// Read this thread's staged pieces of its key (`row` = the key's staged row;
+// zeros for a key past the row's valid count).  Lanes read rows kRawStride
+// apart: 16-byte accesses of 8 consecutive keys hit 8 different bank groups.
+__device__ __forceinline__ void read_row(uint32_t row, bool live, int c, int part, ConvRegs& r) {
   const uint32_t code0 = row + 16 * kCodePerPart * part;
-  uint4 nxt = live ? lds128(code0) : make_uint4(0, 0, 0, 0);
-#pragma unroll 1
+  const uint32_t rope0 = row + kRawRope + 32 * part;
+#pragma unroll
+  for (int k = 0; k < kCodePerPart; ++k)
+    r.cur[k] = live ? lds128(code0 + 16 * k) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+  for (int q = 0; q < kRopePerPart; ++q)
+    r.cur[kCodePerPart + q] = live ? lds128(rope0 + 16 * q) : make_uint4(0, 0, 0, 0);
+  // the one scale group of this thread's codes
+  r.scale = live ? ld_shared_f32(row + kRawScales + 4 * (2 * c + part)) : 0.f;
+}
+
+// Convert the read pieces into the swizzled fp16 operand tile at `op` (the
+// same code path for both CTA ranks and parts).
+__device__ __forceinline__ void convert_row(const ConvRegs& r, uint32_t op, int key, int part) {
+  __half2 hi, lo;
+  split_scale(r.scale, hi, lo);
+#pragma unroll
   for (int k = 0; k < kCodePerPart; ++k) {
-    const uint4 cur = nxt;
-    if (live) nxt = lds128(k + 1 < kCodePerPart ? code0 + 16 * (k + 1)
-                                                 : row + kRawRope + 32 * part);
     const int ldim = 128 * part + 16 * k;
-    sts128(op_addr(op, key, ldim), e4m3x8_scaled(make_uint2(cur.x, cur.y), hi, lo));
-    sts128(op_addr(op, key, ldim + 8), e4m3x8_scaled(make_uint2(cur.z, cur.w), hi, lo));
+    sts128(op_addr(op, key, ldim), e4m3x8_scaled(make_uint2(r.cur[k].x, r.cur[k].y), hi, lo));
+    sts128(op_addr(op, key, ldim + 8), e4m3x8_scaled(make_uint2(r.cur[k].z, r.cur[k].w), hi, lo));
   }
-#pragma unroll 1
-  for (int r = 0; r < kRopePerPart; ++r) {
-    const uint4 cur = nxt;
-    if (live && r + 1 < kRopePerPart) nxt = lds128(row + kRawRope + 32 * part + 16 * (r + 1));
-    sts128(op_addr(op, key, 256 + 16 * part + 8 * r), bf16x8_to_f16x8(cur));
-  }
+#pragma unroll
+  for (int q = 0; q < kRopePerPart; ++q)
+    sts128(op_addr(op, key, 256 + 16 * part + 8 * q), bf16x8_to_f16x8(r.cur[kCodePerPart + q]));
 }
 
 // The loader warps' loop.  Loader ld owns pieces ld + 96k (k < 14) of every
 // tile (a tile has 64 rows x 21 pieces = 14 x 96), so consecutive lanes read
 // consecutive 16 bytes of a row (whole sectors, few transactions).  A tile's
-// pieces are loaded into registers while the two raw stages hold the two
-// tiles before it, and stored into a stage once the four converter warps have
-// read that stage's previous tile: three tiles are in flight with two stages
-// of shared memory.  Load-issue stalls (the memory system's request slots)
-// fall on these warps, not on the converters.
+// pieces are loaded into registers while the raw stage holds the tile before
+// it, and stored once the converter warps have read that tile out of the
+// stage.  Load-issue stalls (the memory system's request slots) fall on these
+// warps, not on the converters.
 constexpr int kPiecesPerLoader = kTileN * kPiecesPerRow / kLoaders;
 static_assert(kPiecesPerLoader * kLoaders == kTileN * kPiecesPerRow, "loaders share a tile evenly");
 
@@ -395,16 +399,19 @@ __device__ void convert_loop(Ctl* ctl, uint8_t* sm, int n, int ntiles, int key, 
   for (int i = 0; i < ntiles; ++i) {
     const int st = i % kRawStages;
     if (!wait_bar(&ctl->raw_full[st], (i / kRawStages) & 1, abort, kWsRaw)) break;
+    ConvRegs r;
+    read_row(raw0 + st * kRawTileBytes + key * kRawStride, key < n - i * kTileN, c, part, r);
+    // the raw stage goes back to the loaders as soon as the warp has read it
+    // (the warp barrier orders the lanes' reads before lane 0's release), so
+    // they refill it while this tile is converted
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->raw_empty[st]);
     if (i >= kStages &&
         !wait_bar(&ctl->freed[i % kStages], ((i - kStages) / kStages) & 1, abort, kWsFreed))
       break;
-    convert_row(raw0 + st * kRawTileBytes + key * kRawStride, op0 + (i % kStages) * kOpTileBytes,
-                key, key < n - i * kTileN, c, part);
+    convert_row(r, op0 + (i % kStages) * kOpTileBytes, key, part);
     fence_async_shared();
     mbar_arrive(&ctl->full[i % kStages]);
-    // the warp's reads of the raw stage are complete (their values are used)
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&ctl->raw_empty[st]);
   }
 }
 
