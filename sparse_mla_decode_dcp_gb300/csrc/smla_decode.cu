@@ -360,7 +360,7 @@ __device__ void loader_loop(const DecodeArgs& a, Ctl* ctl, uint8_t* sm, int n, i
         const int r = int((uint32_t(p) * 3121u) >> 16);  // p / 21, exact for p < 64 * 21
         const int j = p - r * kPiecesPerRow;
         const uint8_t* row = row_ptr<kFused>(a, ctl, list, list_shard, base + r);
-        buf[k] = __ldg(reinterpret_cast<const uint4*>(row + piece_src(c, j)));
+        buf[k] = ldg_stream(row + piece_src(c, j));
       }
     }
   };
