@@ -342,6 +342,8 @@ __device__ __forceinline__ void convert_row(const ConvRegs& r, uint32_t op, int 
 // warps, not on the converters.
 constexpr int kPiecesPerLoader = kTileN * kPiecesPerRow / kLoaders;
 static_assert(kPiecesPerLoader * kLoaders == kTileN * kPiecesPerRow, "loaders share a tile evenly");
+static_assert(kTileN * kRawStride <= (1 << 15) && SMLA_ROW_BYTES <= (1 << 10) && kTileN <= (1 << 7),
+              "packed piece offsets fit their fields");
 
 template <bool kFused>
 __device__ void loader_loop(const DecodeArgs& a, Ctl* ctl, uint8_t* sm, int n, int ntiles, int c,
@@ -350,30 +352,35 @@ __device__ void loader_loop(const DecodeArgs& a, Ctl* ctl, uint8_t* sm, int n, i
   const uint8_t* list_shard = sm + kOffListShard;
   const uint32_t raw0 = smem_u32(sm + kOffRaw);
   uint4 buf[kPiecesPerLoader];
+  // Each piece's place is the same in every tile: its row r in the tile, its
+  // source offset in the cache row and its destination offset in the raw
+  // stage, packed once as r << 25 | src << 15 | dst (dst < 2^15, src < 2^10).
+  uint32_t pk[kPiecesPerLoader];
+#pragma unroll
+  for (int k = 0; k < kPiecesPerLoader; ++k) {
+    const int p = ld + kLoaders * k;                   // < 64 * 21
+    const int r = int((uint32_t(p) * 3121u) >> 16);  // p / 21, exact for p < 64 * 21
+    const int j = p - r * kPiecesPerRow;
+    pk[k] = uint32_t(r) << 25 | uint32_t(piece_src(c, j)) << 15 |
+            uint32_t(r * kRawStride + 16 * j);
+  }
   auto load = [&](int tile) {
     const int base = tile * kTileN;
-    const int pieces = min(kTileN, n - base) * kPiecesPerRow;
+    const uint32_t rows = uint32_t(min(kTileN, n - base));
 #pragma unroll
     for (int k = 0; k < kPiecesPerLoader; ++k) {
-      const int p = ld + kLoaders * k;
-      if (p < pieces) {
-        const int r = int((uint32_t(p) * 3121u) >> 16);  // p / 21, exact for p < 64 * 21
-        const int j = p - r * kPiecesPerRow;
-        const uint8_t* row = row_ptr<kFused>(a, ctl, list, list_shard, base + r);
-        buf[k] = ldg_stream(row + piece_src(c, j));
+      const uint32_t r = pk[k] >> 25;
+      if (r < rows) {
+        const uint8_t* row = row_ptr<kFused>(a, ctl, list, list_shard, base + int(r));
+        buf[k] = ldg_stream(row + ((pk[k] >> 15) & 1023u));
       }
     }
   };
   auto store = [&](int tile, uint32_t stage) {
-    const int pieces = min(kTileN, n - tile * kTileN) * kPiecesPerRow;
+    const uint32_t rows = uint32_t(min(kTileN, n - tile * kTileN));
 #pragma unroll
-    for (int k = 0; k < kPiecesPerLoader; ++k) {
-      const int p = ld + kLoaders * k;
-      if (p < pieces) {
-        const int r = int((uint32_t(p) * 3121u) >> 16);
-        sts128(stage + r * kRawStride + 16 * (p - r * kPiecesPerRow), buf[k]);
-      }
-    }
+    for (int k = 0; k < kPiecesPerLoader; ++k)
+      if ((pk[k] >> 25) < rows) sts128(stage + (pk[k] & 0x7fffu), buf[k]);
   };
   if (ntiles > 0) load(0);
 #pragma unroll 1
