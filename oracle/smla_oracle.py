@@ -18,8 +18,11 @@ Pins (tests/test_oracle.py), all independent of this file's arithmetic:
   bf16_bits_to_f64 ... every bit pattern class against torch.bfloat16
   parse_rows ......... rows packed by struct/torch encoders round-trip
   dcp_filter_convert_index ... a KV-append simulation (per-shard running
-                       counters and block allocation), partition/inverse
-                       invariants, D=1 plain paged mapping
+                       counters and block allocation) for interleave sizes
+                       1..4, partition/inverse invariants, D=1 plain paged
+                       mapping for any interleave size
+  dcp_local_seq_len .. closed forms (whole rounds of I*D positions plus the
+                       partial round) for interleave sizes 1..4
   sparse_mla_decode .. torch float64 scaled_dot_product_attention + logsumexp
                        on dense cases, q=0 closed form, single-slot closed
                        form, order invariance, the pages' empty-row case
@@ -96,24 +99,31 @@ def parse_rows(rows: np.ndarray):
 # DCP filter + convert [P3 implementation breakdown step 2 and the
 # _forward_fp8_kv_mixed_batch snippet; P1 Summary "convert global sparse
 # top-k token ids to this DCP rank's local physical KV slots"].
-# Interleave 1: global position t lives on rank t mod D at rank-local
-# position t div D; the rank-local position then goes through that rank's
-# paged block table.  Entries that are negative or owned by another rank
-# become -1 *in place* (compact_valid_to_front=False).  With D=1 this is the
-# plain request-index -> global-slot conversion of the non-DCP branch.
+# Interleave size I (the snippet passes cp_kv_cache_interleave_size; the
+# pages validate only I = 1 [P3 implementation breakdown step 4]): groups of
+# I consecutive positions go to the ranks in turn, so position t lives on
+# rank (t div I) mod D at rank-local position (t div (I*D))*I + t mod I --
+# for I = 1, rank t mod D at position t div D.  The rank-local position then
+# goes through that rank's paged block table.  Entries that are negative or
+# owned by another rank become -1 *in place* (compact_valid_to_front=False).
+# With D=1 this is the plain request-index -> global-slot conversion of the
+# non-DCP branch, whatever I is.
 # --------------------------------------------------------------------------
-def dcp_filter_convert_index(req_id, block_table, topk, D, rank, block_size):
+def dcp_filter_convert_index(req_id, block_table, topk, D, rank, block_size, interleave=1):
     """Returns (local_slots int32 [T, K], valid_count int32 [T])."""
     topk = np.asarray(topk, dtype=np.int64)
     req_id = np.asarray(req_id, dtype=np.int64)
     bt = np.asarray(block_table, dtype=np.int64)
+    I = int(interleave)
+    assert I >= 1
     T, K = topk.shape
     out = np.full((T, K), -1, dtype=np.int64)
     for i in range(T):
         r = req_id[i]
         t = topk[i]
-        mine = (t >= 0) & (t % D == rank)
-        lp = t[mine] // D  # rank-local position
+        mine = (t >= 0) & ((t // I) % D == rank)
+        tm = t[mine]
+        lp = (tm // (I * D)) * I + tm % I  # rank-local position
         col = lp // block_size
         assert np.all(col < bt.shape[1]), "top-k id beyond the block table"
         phys = bt[r, col]
@@ -123,10 +133,12 @@ def dcp_filter_convert_index(req_id, block_table, topk, D, rank, block_size):
     return out.astype(np.int32), valid_count.astype(np.int32)
 
 
-def dcp_local_seq_len(ctx: int, D: int, rank: int) -> int:
-    """Number of a request's ctx positions that rank holds under interleave 1
-    [P2 "DCP decode rank scalar", get_dcp_local_seq_lens]."""
-    return sum(1 for t in range(int(ctx)) if t % D == rank)
+def dcp_local_seq_len(ctx: int, D: int, rank: int, interleave: int = 1) -> int:
+    """Number of a request's ctx positions that rank holds [P2 "DCP decode
+    rank scalar", get_dcp_local_seq_lens], groups of `interleave` positions
+    going to the ranks in turn."""
+    I = int(interleave)
+    return sum(1 for t in range(int(ctx)) if (t // I) % D == rank)
 
 
 # --------------------------------------------------------------------------

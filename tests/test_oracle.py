@@ -113,19 +113,23 @@ def test_index_worked_examples():
         assert count.tolist() == case["valid_count"], case["note"]
 
 
-def _simulate_paged_cache(ctx, D, bs, rng):
+def _simulate_paged_cache(ctx, D, bs, rng, interleave=1):
     """Fill a D-rank paged KV cache one token at a time, the way a cache
-    manager appends: each rank keeps a running row counter per request and
-    takes a fresh random free block when the current one is full.  Returns
-    per-rank block tables and where[(r, t)] = (rank, slot)."""
+    manager appends: runs of `interleave` consecutive tokens go to the ranks
+    in turn, each rank keeps a running row counter per request and takes a
+    fresh random free block when the current one is full.  Returns per-rank
+    block tables and where[(r, t)] = (rank, slot)."""
     R = len(ctx)
     tables = [[[] for _ in range(R)] for _ in range(D)]
     free = [list(rng.permutation(4 * sum(ctx) // bs + 8 * R + 8)) for _ in range(D)]
     counters = np.zeros((D, R), dtype=np.int64)
     where = {}
     for r in range(R):
+        d, run = 0, 0  # the rank taking tokens now, and how many it has taken in a row
         for t in range(ctx[r]):
-            d = t % D  # interleave 1: position t is owned by rank t mod D
+            if run == interleave:
+                d, run = (d + 1) % D, 0
+            run += 1
             c = counters[d, r]
             if c % bs == 0:
                 tables[d][r].append(int(free[d].pop()))
@@ -141,12 +145,14 @@ def _simulate_paged_cache(ctx, D, bs, rng):
     return bts, where, counters
 
 
-@pytest.mark.parametrize("D,bs,ctx", [
-    (1, 4, [13, 5]), (2, 4, [13, 1, 9]), (3, 2, [7, 2, 11]),
-    (4, 16, [200, 3, 1, 64]), (8, 4, [50, 7])])
-def test_index_matches_append_simulation(D, bs, ctx):
-    rng = np.random.default_rng(D * 100 + bs)
-    bts, where, counters = _simulate_paged_cache(ctx, D, bs, rng)
+@pytest.mark.parametrize("D,bs,ctx,interleave", [
+    (1, 4, [13, 5], 1), (2, 4, [13, 1, 9], 1), (3, 2, [7, 2, 11], 1),
+    (4, 16, [200, 3, 1, 64], 1), (8, 4, [50, 7], 1),
+    (1, 4, [13, 5], 3), (2, 4, [13, 1, 9], 2), (3, 2, [7, 2, 11], 4),
+    (4, 16, [200, 3, 1, 64], 2), (4, 4, [77, 30], 3), (8, 4, [50, 7], 4)])
+def test_index_matches_append_simulation(D, bs, ctx, interleave):
+    rng = np.random.default_rng(D * 100 + bs + 7 * interleave)
+    bts, where, counters = _simulate_paged_cache(ctx, D, bs, rng, interleave)
     R = len(ctx)
     rows, req = [], []
     for r in range(R):
@@ -159,7 +165,8 @@ def test_index_matches_append_simulation(D, bs, ctx):
     req_id = np.array(req, dtype=np.int32)
     owned = np.zeros(topk.shape, dtype=np.int64)
     for d in range(D):
-        slots, count = oracle.dcp_filter_convert_index(req_id, bts[d], topk, D, d, bs)
+        slots, count = oracle.dcp_filter_convert_index(req_id, bts[d], topk, D, d, bs,
+                                                       interleave=interleave)
         for i in range(topk.shape[0]):
             for j in range(topk.shape[1]):
                 t = int(topk[i, j])
@@ -174,7 +181,7 @@ def test_index_matches_append_simulation(D, bs, ctx):
     # per-rank counts of a request equal the local sequence length helper
     for d in range(D):
         for r in range(R):
-            assert counters[d, r] == oracle.dcp_local_seq_len(ctx[r], D, d)
+            assert counters[d, r] == oracle.dcp_local_seq_len(ctx[r], D, d, interleave)
 
 
 def test_index_all_positions_counts_equal_local_seq_lens():
@@ -198,6 +205,52 @@ def test_local_seq_len_closed_form():
             for rank in range(D):
                 want = max(0, -(-(ctx - rank) // D))
                 assert oracle.dcp_local_seq_len(ctx, D, rank) == want
+
+
+def test_local_seq_len_closed_form_interleaved():
+    # whole rounds of I*D positions give each rank I; in the partial round the
+    # rank's run starts at I*rank
+    for ctx in range(0, 60):
+        for D in (1, 2, 3, 4):
+            for I in (1, 2, 3, 4):
+                for rank in range(D):
+                    rounds, rem = divmod(ctx, I * D)
+                    want = rounds * I + min(max(rem - I * rank, 0), I)
+                    assert oracle.dcp_local_seq_len(ctx, D, rank, I) == want
+
+
+def test_index_interleave_is_a_bijection_onto_rank_local_positions():
+    # per request, (rank, rank-local position) of the positions 0..ctx-1 are
+    # distinct and each rank's local positions are exactly 0..count-1, so a
+    # rank's identity block table (block b -> b) maps them to slots 0..count-1
+    bs = 4
+    for D in (1, 2, 3, 4):
+        for I in (1, 2, 3, 5):
+            ctx = 3 * I * D + 2
+            t = np.arange(ctx, dtype=np.int32)[None]
+            seen = set()
+            for d in range(D):
+                W = ctx // bs + 2
+                ident = np.arange(W, dtype=np.int32)[None]
+                slots, count = oracle.dcp_filter_convert_index(
+                    np.zeros(1, np.int32), ident, t, D, d, bs, interleave=I)
+                local = sorted(int(x) for x in slots[0] if x >= 0)
+                assert local == list(range(int(count[0])))
+                seen.update((d, x) for x in local)
+            assert len(seen) == ctx
+
+
+def test_index_single_rank_is_plain_paging_for_any_interleave():
+    rng = np.random.default_rng(11)
+    bt = rng.permutation(40).astype(np.int32).reshape(2, 20)
+    topk = rng.integers(-1, 79, size=(2, 16)).astype(np.int32)
+    for I in (1, 2, 7):
+        slots, _ = oracle.dcp_filter_convert_index(np.array([0, 1], np.int32), bt, topk, 1, 0, 4,
+                                                   interleave=I)
+        for i in range(2):
+            for j in range(16):
+                t = int(topk[i, j])
+                assert slots[i, j] == (-1 if t < 0 else bt[i, t // 4] * 4 + t % 4)
 
 
 # ----------------------------------------------------------------- attention

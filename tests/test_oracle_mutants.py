@@ -16,8 +16,10 @@ PIN_CALLS = [
     pins.test_bf16_widen_matches_torch,
     pins.test_parse_rows_roundtrip_known_values,
     pins.test_index_worked_examples,
-    lambda: pins.test_index_matches_append_simulation(2, 4, [13, 1, 9]),
-    lambda: pins.test_index_matches_append_simulation(3, 2, [7, 2, 11]),
+    lambda: pins.test_index_matches_append_simulation(2, 4, [13, 1, 9], 1),
+    lambda: pins.test_index_matches_append_simulation(3, 2, [7, 2, 11], 1),
+    lambda: pins.test_index_matches_append_simulation(4, 4, [77, 30], 3),
+    pins.test_index_interleave_is_a_bijection_onto_rank_local_positions,
     lambda: pins.test_attention_dense_matches_torch_sdpa(7, 16),
     pins.test_attention_q_zero_closed_form,
     pins.test_attention_single_slot_closed_form,
@@ -61,14 +63,24 @@ def _parse_swapped_parts(rows):
 
 
 def _convert(variant):
-    def f(req_id, block_table, topk, D, rank, block_size):
+    def f(req_id, block_table, topk, D, rank, block_size, interleave=1):
         topk = np.asarray(topk, dtype=np.int64)
         bt = np.asarray(block_table, dtype=np.int64)
         out = np.full(topk.shape, -1, dtype=np.int64)
+        I = interleave
         for i in range(topk.shape[0]):
             t = topk[i]
-            mine = (t >= 0) & (t % D == rank)
-            lp = t[mine] // D if variant != "no_div" else t[mine]
+            if variant == "interleave_owner_by_position":
+                mine = (t >= 0) & (t % D == rank)
+            else:
+                mine = (t >= 0) & ((t // I) % D == rank)
+            tm = t[mine]
+            if variant == "no_div":
+                lp = tm
+            elif variant == "interleave_local_as_plain":
+                lp = tm // D
+            else:
+                lp = (tm // (I * D)) * I + tm % I
             lp = np.minimum(lp, bt.shape[1] * block_size - 1)
             phys = bt[int(req_id[i]), lp // block_size]
             if variant == "no_mod":
@@ -135,6 +147,10 @@ MUTANTS = {
     "convert_no_mod": ("dcp_filter_convert_index", _convert("no_mod")),
     "convert_block_major": ("dcp_filter_convert_index", _convert("block_major")),
     "convert_keep_foreign": ("dcp_filter_convert_index", _convert("keep_foreign")),
+    "convert_interleave_local_as_plain": ("dcp_filter_convert_index",
+                                          _convert("interleave_local_as_plain")),
+    "convert_interleave_owner_by_position": ("dcp_filter_convert_index",
+                                             _convert("interleave_owner_by_position")),
     "attn_no_scale": ("sparse_mla_decode_rows", _rows_variant("no_scale")),
     "attn_rope_negated": ("sparse_mla_decode_rows", _rows_variant("rope_negated")),
     "attn_log2": ("sparse_mla_decode_rows", _rows_variant("log2")),
