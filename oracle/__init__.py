@@ -10,9 +10,11 @@ from .smla_oracle import (  # noqa: F401
     bf16_bits_to_f64,
     dcp_filter_convert_index,
     dcp_local_seq_len,
+    dcp_topk_merge,
     e4m3_to_f64,
     lse_merge,
     parse_rows,
     sparse_mla_decode,
     sparse_mla_decode_rows,
+    topk_select,
 )

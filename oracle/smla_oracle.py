@@ -23,6 +23,10 @@ Pins (tests/test_oracle.py), all independent of this file's arithmetic:
                        mapping for any interleave size
   dcp_local_seq_len .. closed forms (whole rounds of I*D positions plus the
                        partial round) for interleave sizes 1..4
+  topk_select ........ torch.topk on distinct scores, numpy argmax at K=1,
+                       the all-equal closed form, short rows
+  dcp_topk_merge ..... per-rank local top-k then merge equals the unsharded
+                       selection, with and without ties
   sparse_mla_decode .. torch float64 scaled_dot_product_attention + logsumexp
                        on dense cases, q=0 closed form, single-slot closed
                        form, order invariance, the pages' empty-row case
@@ -139,6 +143,52 @@ def dcp_local_seq_len(ctx: int, D: int, rank: int, interleave: int = 1) -> int:
     going to the ranks in turn."""
     I = int(interleave)
     return sum(1 for t in range(int(ctx)) if (t // I) % D == rank)
+
+
+# --------------------------------------------------------------------------
+# Global top-k of indexer scores, the step that produces this path's input
+# [P1 Summary "global sparse top-k token ids"; P3 related PRs, the DCP
+# sparse-indexer mechanism "global top-k merge, DCP index filtering"].  The
+# pages do not spell the selection out.  Reading taken: a row keeps the K
+# largest scores among its candidate positions 0..n-1 (n = the request's
+# context, or the query's own position + 1 in spec decode), ranked by score
+# descending and, among equal scores, by position ascending; with fewer than
+# K candidates it keeps all of them and pads with -1.  The output lists the
+# kept positions in that rank order, padding last.
+# --------------------------------------------------------------------------
+def topk_select(scores, n_cand, K):
+    """scores float [T, L]; n_cand int [T] (positions >= n_cand[i] are not
+    candidates); returns int32 [T, K] positions, -1 padded."""
+    scores = np.asarray(scores, dtype=np.float64)
+    T = scores.shape[0]
+    out = np.full((T, K), -1, dtype=np.int64)
+    for i in range(T):
+        n = int(n_cand[i])
+        pos = np.arange(n)
+        # lexsort: the last key is the primary one
+        order = np.lexsort((pos, -scores[i, :n]))
+        keep = order[:K]
+        out[i, :len(keep)] = pos[keep]
+    return out.astype(np.int32)
+
+
+# Under DCP each rank scores only the positions it holds and keeps its own
+# top-k of them, as global ids; the global top-k is then the top-k of the
+# union of the ranks' candidates, by the same rank order.
+def dcp_topk_merge(cand_ids, cand_scores, K):
+    """cand_ids: sequence over ranks of int [T, K_d] global positions (-1 =
+    no candidate); cand_scores: the matching scores.  Returns int32 [T, K]."""
+    ids = np.concatenate([np.asarray(c, dtype=np.int64) for c in cand_ids], axis=1)
+    sc = np.concatenate([np.asarray(c, dtype=np.float64) for c in cand_scores], axis=1)
+    T = ids.shape[0]
+    out = np.full((T, K), -1, dtype=np.int64)
+    for i in range(T):
+        live = ids[i] >= 0
+        pos, val = ids[i, live], sc[i, live]
+        order = np.lexsort((pos, -val))
+        keep = order[:K]
+        out[i, :len(keep)] = pos[keep]
+    return out.astype(np.int32)
 
 
 # --------------------------------------------------------------------------

@@ -480,3 +480,67 @@ def test_generator_structure_tiny():
         assert s.live_rows == sum(oracle.dcp_local_seq_len(c, 2, d) for c in wl.ctx)
         poison = (s.pool.numpy() == 0xFF).all(axis=1)
         assert (~poison).sum() == s.live_rows
+
+
+# ------------------------------------------------------------- top-k select
+def test_topk_select_matches_torch_topk_on_distinct_scores():
+    rng = np.random.default_rng(21)
+    for K in (1, 5, 64):
+        T, L = 6, 150
+        scores = rng.standard_normal((T, L))
+        assert len(np.unique(scores)) == scores.size  # distinct: one right answer
+        n_cand = rng.integers(0, L + 1, size=T)
+        n_cand[0], n_cand[1] = L, 3
+        got = oracle.topk_select(scores, n_cand, K)
+        for i in range(T):
+            n = int(n_cand[i])
+            m = min(K, n)
+            want = torch.topk(torch.from_numpy(scores[i, :n]), m, sorted=True).indices.numpy()
+            assert got[i, :m].tolist() == want.tolist()
+            assert np.all(got[i, m:] == -1)
+
+
+def test_topk_select_k1_is_numpy_argmax_with_ties():
+    rng = np.random.default_rng(22)
+    scores = rng.integers(0, 4, size=(40, 30)).astype(np.float64)  # many ties
+    got = oracle.topk_select(scores, np.full(40, 30), 1)
+    assert got[:, 0].tolist() == np.argmax(scores, axis=1).tolist()  # first of equal maxima
+
+
+def test_topk_select_all_equal_scores_keep_the_first_positions():
+    for n in (0, 1, 7, 20):
+        for K in (1, 7, 12):
+            got = oracle.topk_select(np.zeros((1, 25)), [n], K)[0]
+            m = min(K, n)
+            assert got.tolist() == list(range(m)) + [-1] * (K - m)
+
+
+def test_topk_select_short_rows_keep_every_candidate():
+    rng = np.random.default_rng(23)
+    scores = rng.standard_normal((3, 10))
+    got = oracle.topk_select(scores, [0, 4, 10], 16)
+    assert got[0].tolist() == [-1] * 16
+    assert sorted(got[1, :4].tolist()) == [0, 1, 2, 3] and np.all(got[1, 4:] == -1)
+    assert sorted(got[2, :10].tolist()) == list(range(10)) and np.all(got[2, 10:] == -1)
+
+
+@pytest.mark.parametrize("D,K,decimals", [(1, 8, 6), (2, 16, 6), (4, 16, 1), (3, 40, 0)])
+def test_dcp_topk_merge_of_rank_local_topk_equals_unsharded(D, K, decimals):
+    # every global top-k entry is in its owner's local top-k under the same
+    # order, so shard-then-merge selects exactly what one unsharded pass does
+    rng = np.random.default_rng(D * 10 + K)
+    T, L = 5, 97
+    scores = np.round(rng.standard_normal((T, L)), decimals)  # decimals=0/1: heavy ties
+    n_cand = rng.integers(1, L + 1, size=T)
+    want = oracle.topk_select(scores, n_cand, K)
+    cand_ids, cand_scores = [], []
+    for d in range(D):
+        local = scores[:, d::D]  # rank d holds positions d, d + D, ... (interleave 1)
+        n_local = np.array([oracle.dcp_local_seq_len(int(n), D, d) for n in n_cand])
+        lp = oracle.topk_select(local, n_local, K).astype(np.int64)
+        ids = np.where(lp >= 0, lp * D + d, -1)
+        cand_ids.append(ids)
+        cand_scores.append(np.where(ids >= 0, np.take_along_axis(scores, np.maximum(ids, 0), 1),
+                                    0.0))
+    got = oracle.dcp_topk_merge(cand_ids, cand_scores, K)
+    assert np.array_equal(got, want)

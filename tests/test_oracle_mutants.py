@@ -27,6 +27,11 @@ PIN_CALLS = [
     pins.test_merge_identity_changes_nothing_and_no_nan,
     pins.test_merge_all_empty_is_identity,
     pins.test_merge_of_shards_equals_unsharded_with_empty_shards,
+    pins.test_topk_select_matches_torch_topk_on_distinct_scores,
+    pins.test_topk_select_k1_is_numpy_argmax_with_ties,
+    pins.test_topk_select_all_equal_scores_keep_the_first_positions,
+    pins.test_topk_select_short_rows_keep_every_candidate,
+    lambda: pins.test_dcp_topk_merge_of_rank_local_topk_equals_unsharded(4, 16, 1),
 ]
 
 
@@ -95,6 +100,32 @@ def _convert(variant):
     return f
 
 
+def _topk_variant(variant):
+    def f(scores, n_cand, K):
+        scores = np.asarray(scores, dtype=np.float64)
+        out = np.full((scores.shape[0], K), -1, dtype=np.int64)
+        for i in range(scores.shape[0]):
+            n = scores.shape[1] if variant == "no_bound" else int(n_cand[i])
+            pos = np.arange(n)
+            if variant == "ascending":
+                order = np.lexsort((pos, scores[i, :n]))
+            elif variant == "ties_last_first":
+                order = np.lexsort((-pos, -scores[i, :n]))
+            else:
+                order = np.lexsort((pos, -scores[i, :n]))
+            keep = order[:K]
+            out[i, :len(keep)] = pos[keep]
+        return out.astype(np.int32)
+    return f
+
+
+_MERGE = so.dcp_topk_merge  # the real merge, bound before any patching
+
+
+def _topk_merge_first_rank(cand_ids, cand_scores, K):
+    return _MERGE(cand_ids[:1], cand_scores[:1], K)
+
+
 def _rows_variant(variant):
     def f(q_row, rows, sm_scale):
         H = q_row.shape[0]
@@ -151,6 +182,10 @@ MUTANTS = {
                                           _convert("interleave_local_as_plain")),
     "convert_interleave_owner_by_position": ("dcp_filter_convert_index",
                                              _convert("interleave_owner_by_position")),
+    "topk_ascending": ("topk_select", _topk_variant("ascending")),
+    "topk_ties_last_first": ("topk_select", _topk_variant("ties_last_first")),
+    "topk_no_candidate_bound": ("topk_select", _topk_variant("no_bound")),
+    "topk_merge_first_rank_only": ("dcp_topk_merge", _topk_merge_first_rank),
     "attn_no_scale": ("sparse_mla_decode_rows", _rows_variant("no_scale")),
     "attn_rope_negated": ("sparse_mla_decode_rows", _rows_variant("rope_negated")),
     "attn_log2": ("sparse_mla_decode_rows", _rows_variant("log2")),
