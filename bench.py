@@ -467,6 +467,8 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": args.workload, "T": wl.T, "H": wl.H, "K": wl.K, "D": wl.D,
+                   "block_size": wl.spec.block_size, "requests": wl.spec.num_reqs,
+                   "cached_tokens": int(sum(int(c) for c in wl.ctx)),
                    "sample_rows_per_step": n},
         "cpu_baseline": b,
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
