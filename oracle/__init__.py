@@ -11,7 +11,9 @@ from .smla_oracle import (  # noqa: F401
     dcp_filter_convert_index,
     dcp_local_seq_len,
     dcp_topk_merge,
+    dense_mla_decode,
     e4m3_to_f64,
+    flatten_lse_bhs,
     lse_merge,
     parse_rows,
     sparse_mla_decode,

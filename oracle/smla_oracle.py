@@ -27,6 +27,10 @@ Pins (tests/test_oracle.py), all independent of this file's arithmetic:
                        the all-equal closed form, short rows
   dcp_topk_merge ..... per-rank local top-k then merge equals the unsharded
                        selection, with and without ties
+  dense_mla_decode ... paged, sharded over D ranks and merged, against torch
+                       float64 SDPA with a causal mask over the logical token
+                       sequence; spec-decode tokens equal single-token requests
+  flatten_lse_bhs .... torch permute + reshape
   sparse_mla_decode .. torch float64 scaled_dot_product_attention + logsumexp
                        on dense cases, q=0 closed form, single-slot closed
                        form, order invariance, the pages' empty-row case
@@ -232,6 +236,51 @@ def sparse_mla_decode(q_bits: np.ndarray, pool: np.ndarray,
         assert np.all(valid < pool.shape[0]), "slot beyond the pool"
         out[i], lse[i] = sparse_mla_decode_rows(q[i], pool[valid], sm_scale)
     return out, lse
+
+
+# --------------------------------------------------------------------------
+# Dense MLA decode with LSE return [P3 key snippets, the dense FlashMLA
+# decode path (vllm/v1/attention/backends/mla/flashmla.py): under DCP it
+# returns the LSE, flattened from [batch, heads, seq_len] to
+# [tokens, heads]].  Request b has S query tokens at positions
+# ctx_b - S .. ctx_b - 1; token s attends every position up to and including
+# its own.  Under DCP, rank d attends only the positions it holds, so its
+# (out, lse) per token is a partial that the LSE merge combines.  Rows come
+# out in token order b*S + s.
+# --------------------------------------------------------------------------
+def dense_mla_decode(q_bits, pool, block_table, ctx, S, D, rank, block_size, sm_scale,
+                     interleave=1):
+    """q_bits uint16 [B*S, H, 576] (row b*S + s); pool uint8 [num_slots, 656]
+    and block_table int32 [B, W] of rank `rank`; ctx int [B].  Returns
+    (out float64 [B*S, H, 512], lse float64 [B*S, H])."""
+    ctx = np.asarray(ctx, dtype=np.int64)
+    B = ctx.shape[0]
+    T = B * S
+    H = q_bits.shape[1]
+    out = np.zeros((T, H, NOPE_DIM))
+    lse = np.full((T, H), -np.inf)
+    for b in range(B):
+        for s_ in range(S):
+            i = b * S + s_
+            p = int(ctx[b]) - S + s_  # this token's position
+            positions = np.arange(p + 1, dtype=np.int32)[None]
+            slots, _ = dcp_filter_convert_index(np.array([b]), block_table, positions, D, rank,
+                                                block_size, interleave)
+            mine = slots[0][slots[0] >= 0]
+            q = bf16_bits_to_f64(q_bits[i])
+            out[i], lse[i] = sparse_mla_decode_rows(q, np.asarray(pool)[mine], sm_scale)
+    return out, lse
+
+
+def flatten_lse_bhs(lse_bhs):
+    """[batch, heads, seq_len] -> [batch * seq_len, heads], row b*S + s."""
+    lse_bhs = np.asarray(lse_bhs)
+    B, H, S = lse_bhs.shape
+    flat = np.empty((B * S, H), dtype=lse_bhs.dtype)
+    for b in range(B):
+        for s_ in range(S):
+            flat[b * S + s_] = lse_bhs[b, :, s_]
+    return flat
 
 
 # --------------------------------------------------------------------------

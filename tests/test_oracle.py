@@ -544,3 +544,60 @@ def test_dcp_topk_merge_of_rank_local_topk_equals_unsharded(D, K, decimals):
                                     0.0))
     got = oracle.dcp_topk_merge(cand_ids, cand_scores, K)
     assert np.array_equal(got, want)
+
+
+# ------------------------------------------------------------- dense decode
+def _paged_dense_case(ctx, D, bs, S, H, seed, interleave=1):
+    """Logical token rows per request, the D ranks' paged pools holding them
+    (every row no token owns is NaN bytes), the ranks' block tables and q."""
+    rng = np.random.default_rng(seed)
+    gen = torch.Generator().manual_seed(seed)
+    bts, where, _ = _simulate_paged_cache(ctx, D, bs, rng, interleave)
+    tokens = [inputs.random_rows(c, gen, "cpu").numpy() for c in ctx]
+    n_slots = max(s for (_, s) in where.values()) + bs
+    pools = [np.full((n_slots, 656), 0xFF, dtype=np.uint8) for _ in range(D)]
+    for (r, t), (d, slot) in where.items():
+        pools[d][slot] = tokens[r][t]
+    q = torch.randn((len(ctx) * S, H, 576), generator=gen).to(torch.bfloat16)
+    return tokens, pools, bts, q
+
+
+@pytest.mark.parametrize("D,S,interleave", [(1, 1, 1), (1, 2, 1), (2, 2, 1), (4, 1, 1), (3, 2, 2)])
+def test_dense_decode_sharded_and_merged_matches_torch_causal_sdpa(D, S, interleave):
+    ctx, bs, H = [37, 9, 64], 8, 4
+    tokens, pools, bts, q = _paged_dense_case(ctx, D, bs, S, H, seed=D * 10 + S, interleave=interleave)
+    parts = [oracle.dense_mla_decode(_q_bits(q), pools[d], bts[d], ctx, S, D, d, bs, SM_SCALE,
+                                     interleave) for d in range(D)]
+    out, lse = oracle.lse_merge([p[0] for p in parts], [p[1] for p in parts])
+    for b, c in enumerate(ctx):
+        for s in range(S):
+            i, p = b * S + s, c - S + s
+            k, v = _torch_dequant(torch.from_numpy(tokens[b][: p + 1]))
+            qd = q[i].to(torch.float64)
+            n = p + 1
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                qd.unsqueeze(1), k.unsqueeze(0).expand(H, n, 576),
+                v.unsqueeze(0).expand(H, n, 512), scale=SM_SCALE).squeeze(1)
+            ref_lse = torch.logsumexp(SM_SCALE * (qd @ k.T), dim=1)
+            assert np.allclose(out[i], ref.numpy(), rtol=1e-12, atol=1e-12)
+            assert np.allclose(lse[i], ref_lse.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_dense_decode_spec_tokens_equal_single_token_requests():
+    # a request's 2 query tokens at positions c-2, c-1 are the 1-token requests
+    # with contexts c-1 and c over the same cache
+    ctx, bs, H = [21, 40], 4, 3
+    tokens, pools, bts, q = _paged_dense_case(ctx, 2, bs, 2, H, seed=9)
+    single_ctx = [c - 1 + s for c in ctx for s in range(2)]
+    single_bts = [np.repeat(bt[: len(ctx)], 2, axis=0) for bt in bts]
+    for d in range(2):
+        o2, l2 = oracle.dense_mla_decode(_q_bits(q), pools[d], bts[d], ctx, 2, 2, d, bs, SM_SCALE)
+        o1, l1 = oracle.dense_mla_decode(_q_bits(q), pools[d], single_bts[d], single_ctx, 1, 2, d,
+                                         bs, SM_SCALE)
+        assert np.array_equal(o2, o1) and np.array_equal(l2, l1)
+
+
+def test_flatten_lse_matches_torch_permute_reshape():
+    x = torch.arange(2 * 3 * 4, dtype=torch.float64).reshape(2, 3, 4)  # [batch, heads, seq_len]
+    want = x.permute(0, 2, 1).reshape(2 * 4, 3)
+    assert np.array_equal(oracle.flatten_lse_bhs(x.numpy()), want.numpy())

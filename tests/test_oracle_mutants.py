@@ -32,6 +32,9 @@ PIN_CALLS = [
     pins.test_topk_select_all_equal_scores_keep_the_first_positions,
     pins.test_topk_select_short_rows_keep_every_candidate,
     lambda: pins.test_dcp_topk_merge_of_rank_local_topk_equals_unsharded(4, 16, 1),
+    lambda: pins.test_dense_decode_sharded_and_merged_matches_torch_causal_sdpa(2, 2, 1),
+    pins.test_dense_decode_spec_tokens_equal_single_token_requests,
+    pins.test_flatten_lse_matches_torch_permute_reshape,
 ]
 
 
@@ -126,6 +129,38 @@ def _topk_merge_first_rank(cand_ids, cand_scores, K):
     return _MERGE(cand_ids[:1], cand_scores[:1], K)
 
 
+def _dense_variant(variant):
+    def f(q_bits, pool, block_table, ctx, S, D, rank, block_size, sm_scale, interleave=1):
+        ctx = np.asarray(ctx, dtype=np.int64)
+        T, H = ctx.shape[0] * S, q_bits.shape[1]
+        out, lse = np.zeros((T, H, 512)), np.full((T, H), -np.inf)
+        for b in range(ctx.shape[0]):
+            for s_ in range(S):
+                i = b * S + s_
+                if variant == "excludes_own":
+                    p = int(ctx[b]) - S + s_ - 1
+                else:  # "no_causal": every token sees the whole context
+                    p = int(ctx[b]) - 1
+                pos = np.arange(p + 1, dtype=np.int32)[None]
+                slots, _ = so.dcp_filter_convert_index(np.array([b]), block_table, pos, D, rank,
+                                                       block_size, interleave)
+                mine = slots[0][slots[0] >= 0]
+                out[i], lse[i] = so.sparse_mla_decode_rows(so.bf16_bits_to_f64(q_bits[i]),
+                                                           np.asarray(pool)[mine], sm_scale)
+        return out, lse
+    return f
+
+
+def _flatten_transposed(lse_bhs):
+    lse_bhs = np.asarray(lse_bhs)
+    B, H, S = lse_bhs.shape
+    flat = np.empty((B * S, H), dtype=lse_bhs.dtype)
+    for b in range(B):
+        for s_ in range(S):
+            flat[s_ * B + b] = lse_bhs[b, :, s_]
+    return flat
+
+
 def _rows_variant(variant):
     def f(q_row, rows, sm_scale):
         H = q_row.shape[0]
@@ -186,6 +221,9 @@ MUTANTS = {
     "topk_ties_last_first": ("topk_select", _topk_variant("ties_last_first")),
     "topk_no_candidate_bound": ("topk_select", _topk_variant("no_bound")),
     "topk_merge_first_rank_only": ("dcp_topk_merge", _topk_merge_first_rank),
+    "dense_excludes_own_position": ("dense_mla_decode", _dense_variant("excludes_own")),
+    "dense_no_causal_mask": ("dense_mla_decode", _dense_variant("no_causal")),
+    "flatten_transposed": ("flatten_lse_bhs", _flatten_transposed),
     "attn_no_scale": ("sparse_mla_decode_rows", _rows_variant("no_scale")),
     "attn_rope_negated": ("sparse_mla_decode_rows", _rows_variant("rope_negated")),
     "attn_log2": ("sparse_mla_decode_rows", _rows_variant("log2")),
