@@ -9,6 +9,13 @@
  *                                     returning out and the softmax LSE
  *   3. smla_dcp_lse_merge             LSE-weighted merge of D partials
  *
+ * and two more entry points run it differently:
+ *
+ *   smla_dcp_sparse_mla_decode_fused  steps 1-3 for D pools held by one GPU,
+ *                                     in a single launch
+ *   smla_sparse_mla_decode_noalloc    step 2 with library-owned split-K
+ *                                     scratch (no workspace argument)
+ *
  * Sources (page title, then section):
  *   [P1] "[eldritch] attention: support DCP in SM120 FlashInfer sparse MLA"
  *   [P2] "[Bugfix][Attention] Stabilize sparse-MLA DCP for GLM PCP evals"
