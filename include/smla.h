@@ -24,7 +24,10 @@
  * Conventions shared by every call:
  *   - Pointers marked "device" point to memory of the current CUDA device;
  *     the caller allocates and owns all of it.  The library never allocates,
- *     frees or synchronises, and keeps no pointer after a call returns.
+ *     frees or synchronises, and keeps no pointer after a call returns, with
+ *     one exception: smla_sparse_mla_decode_noalloc's split-K scratch is a
+ *     library-owned device array of SMLA_NOALLOC_SCRATCH_BYTES per GPU, whose
+ *     device address the library looks up once per device and keeps.
  *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*,
  *     NULL = legacy default stream) and takes every scalar by value, so no
  *     call issues a host->device copy or a host sync [P2 "DCP decode rank
@@ -155,9 +158,10 @@ size_t smla_decode_workspace_size(int32_t T, int32_t H, int32_t K);
  *               b*S + s) [P3 implementation breakdown steps 1 and 5]
  *   workspace   device scratch of at least
  *               smla_decode_workspace_size(T, H, K) bytes, 256-byte aligned,
- *               zero-filled before its first use (every call leaves it
- *               zero-filled again); may be NULL when that size is 0.
- *               Calls that run concurrently need distinct workspaces.
+ *               zero-filled before its first use (every call, including one
+ *               that sets SMLA_DEVERR_TIMEOUT, leaves its arrival counters
+ *               zero again); may be NULL when that size is 0.  Calls that
+ *               run concurrently need distinct workspaces.
  * Errors: INVALID_ARG for null pointers, T < 0, K < 1, H < 1, num_slots < 0,
  * sm_scale not finite and positive, misaligned q/kv_cache/out; UNSUPPORTED
  * for H > SMLA_MAX_HEADS; WORKSPACE

@@ -39,14 +39,16 @@
 //     O accumulator in TMEM is rescaled only when the row maximum grows by
 //     more than 2^8.
 //
-// Warp roles (288 threads): warps 0-3 softmax/epilogue (TMEM lanes 0-127,
-// one head row per thread), warps 4-7 gather + dequantise, warp 8 allocates
-// TMEM and issues the MMAs (one thread).  Every wait is bounded; a wait that
-// runs out sets SMLA_DEVERR_TIMEOUT and the CTA unwinds.
+// Warp roles (384 threads): warps 0-3 softmax/epilogue (TMEM lanes 0-127,
+// one head row per thread; thread 0 also issues each tile's PV as soon as
+// the four warps have stored P), warps 4-7 dequantise, warp 8 allocates TMEM
+// and issues QK^T (one thread), warps 9-11 gather.  Every wait is bounded; a
+// wait that runs out sets SMLA_DEVERR_TIMEOUT and the CTA unwinds.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/smla.h"
@@ -101,7 +103,7 @@ constexpr int kSmemBytes = kOffCtl + kCtlBytes + 1024;  // + control block + ali
 
 struct Ctl {
   uint64_t q_tma, q_ready, full[kStages], freed[kStages], raw_full[kRawStages], raw_empty[kRawStages],
-      s_full, s_free, p_full, pv_done, xa[2], xb[2], end;
+      s_full, s_free, pv_done, xa[2], xb[2], end, end_pv;
   uint32_t tbase;
   int n_list;
   int abort;
@@ -425,13 +427,17 @@ __device__ void convert_loop(Ctl* ctl, uint8_t* sm, int n, int ntiles, int key, 
 // Split-K epilogue: write this split's unnormalised O half, its log2-domain
 // reference maximum and its sum; the last split of the row to arrive (per
 // value half) combines all of them and resets the row's arrival counter.
+// A split whose CTA gave up on a wait (`ok` false, SMLA_DEVERR_TIMEOUT set)
+// still arrives, contributing nothing, so the counter always returns to zero
+// and the workspace stays valid for the next call.
 __device__ void split_epilogue(const DecodeArgs& a, Ctl* ctl, int C, int64_t t, int split, int ntiles,
-                               float m_ref, float l, uint32_t tb, int warp, int h) {
+                               float m_ref, float l, uint32_t tb, int warp, int h, bool ok) {
   const int S = a.splits;
   const bool live = h < a.H;
   const int64_t row = (t * S + split) * a.H + (live ? h : 0);
   float4* wo = reinterpret_cast<float4*>(a.ws_o + row * SMLA_V_DIM + C * 256);
-  if (ntiles > 0) {
+  const bool has = ok && ntiles > 0;
+  if (has) {
 #pragma unroll 1
     for (int cc = 0; cc < 8; ++cc) {
       uint32_t r[32];
@@ -447,8 +453,8 @@ __device__ void split_epilogue(const DecodeArgs& a, Ctl* ctl, int C, int64_t t, 
   }
   float* ml = a.ws_ml + ((t * S + split) * 2 + C) * 2 * a.H;
   if (live) {
-    ml[h] = (ntiles > 0) ? m_ref : -INFINITY;
-    ml[a.H + h] = (ntiles > 0) ? l : 0.f;
+    ml[h] = has ? m_ref : -INFINITY;
+    ml[a.H + h] = has ? l : 0.f;
   }
   __threadfence();
   named_bar_sync(2, 128);
@@ -571,6 +577,35 @@ __device__ void q_to_tmem(uint32_t tb, int warp, int h, bool live, uint32_t src)
   tmem_st_wait();
 }
 
+// MMA issue, fully unrolled: one thread issues a tcgen05.mma every few tens
+// of cycles at best, and computing each descriptor in the loop about doubles
+// that, which for the N = 64 QK^T steps is slower than the tensor core runs
+// them.  A descriptor's start address field is the byte address / 16, so
+// stepping through a stage adds a constant to the stage's base descriptor
+// (shared-memory addresses stay below 256 KB: no carry leaves the field).
+__device__ __forceinline__ void issue_qk(uint32_t tb, uint32_t op) {
+  constexpr uint32_t idesc = idesc_f16_f32(128, kTileN, false, false);
+  const uint64_t lat = sdesc_sw128(op, 16, 1024);
+  const uint64_t rope = sdesc_sw64(op + kRopeBlock, 16, 512);
+#pragma unroll
+  for (int k = 0; k < kKSteps; ++k) {
+    // 16 dims = 32 bytes of a row; a 128-byte swizzled K-block holds 64 dims
+    const uint64_t bd = k < 16 ? lat + uint64_t((k >> 2) * (kKBlockBytes >> 4) + (k & 3) * 2)
+                               : rope + uint64_t((k - 16) * 2);
+    mma_ts(tb + kSCol, tb + kQCol + 8 * k, bd, idesc, k > 0);
+  }
+}
+
+// PV of one tile: P (TMEM) x V, V = the operand stage read MN-major, 16 keys
+// = 2048 bytes per step.
+__device__ __forceinline__ void issue_pv(uint32_t tb, uint32_t op, bool accumulate) {
+  constexpr uint32_t idesc = idesc_f16_f32(128, 256, false, true);
+  const uint64_t v = sdesc_sw128(op, kKBlockBytes, 1024);
+#pragma unroll
+  for (int k = 0; k < kTileN / 16; ++k)
+    mma_ts(tb + kOCol, tb + kPCol + 8 * k, v + uint64_t(k * (2048 >> 4)), idesc, accumulate || k > 0);
+}
+
 template <bool kFused>
 __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt& hr, int64_t t,
                         int split, uint32_t peer) {
@@ -589,6 +624,7 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
     const float scale_log2 = a.sm_scale * kLog2e;
     float m_ref = -INFINITY;  // log2-domain reference maximum
     float l = 0.f;
+    int pv_issued = 0;        // thread 0: PV MMAs issued so far
     // Key-column split of the softmax: CTA c finishes the scores of keys
     // [32c, 32c + 32) of each tile (its own partial plus the peer's, XA),
     // computes their P against a reference maximum, and sends that P, the
@@ -787,17 +823,37 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&ctl->p_full);
+      // P(i) of all 128 head rows is in TMEM: one softmax thread issues PV(i)
+      // at once (no other thread polls for it), and its completion releases
+      // the operand stage and lets the next P overwrite this one
+      named_bar_sync(5, 128);
+      if (h == 0) {
+        tc_fence_after();
+        issue_pv(tb, smem_u32(sm + kOffOp) + (i % kStages) * kOpTileBytes, i > 0);
+        mma_commit(&ctl->pv_done);
+        mma_commit(&ctl->freed[i % kStages]);
+        pv_issued = i + 1;
+      }
     }
     // epilogue
     if (ok && ntiles > 0) {
       ok = __all_sync(0xffffffffu, wait_bar(&ctl->pv_done, (ntiles - 1) & 1, abort, kWsPvLast));
       tc_fence_after();
     }
+    // thread 0's PV MMAs have all completed before TMEM is read or released
+    // (waited on even after an abort, with its own bound)
+    if (h == 0 && pv_issued > 0) {
+      mma_commit(&ctl->end_pv);
+      int no_abort = 0;
+      wait_bar(&ctl->end_pv, 0, &no_abort, kWsDrain);
+      tc_fence_after();
+    }
     // one decision for all four softmax warps (the split epilogue below uses a
     // 128-thread named barrier)
     ok = !named_bar_or(4, 128, !ok);
-    if (ok && a.splits == 1) {
+    if (a.splits > 1) {
+      split_epilogue(a, ctl, C, t, split, ntiles, m_ref, l, tb, warp, h, ok);
+    } else if (ok) {
       // tcgen05.ld is warp-collective: every lane loads, only live heads store
       const bool live = h < a.H;
       uint4* dst = reinterpret_cast<uint4*>(a.out + (t * a.H + (live ? h : 0)) * SMLA_V_DIM +
@@ -830,8 +886,6 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
       }
       if (C == 0 && live)
         a.lse[t * a.H + h] = (ntiles == 0) ? -INFINITY : (m_ref + log2f(l)) * kLn2;
-    } else if (ok) {
-      split_epilogue(a, ctl, C, t, split, ntiles, m_ref, l, tb, warp, h);
     }
   } else if (warp < 8) {
     // ------------------------------------------------ dequantise
@@ -844,58 +898,20 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
     // ------------------------------------------------ stage cache rows
     loader_loop<kFused>(a, ctl, sm, n, ntiles, C, tid - 32 * kLoaderWarp0, abort);
   } else if (lane == 0) {
-    // ------------------------------------------------ MMA issue (one thread)
-    constexpr uint32_t idesc_qk = idesc_f16_f32(128, kTileN, false, false);
-    constexpr uint32_t idesc_pv = idesc_f16_f32(128, 256, false, true);
+    // ------------------------------------------------ QK^T issue (one thread)
+    // QK(i) needs its operand stage converted and S(i - 1) read by the
+    // softmax; the thread sleeps on each barrier until the hardware wakes it
+    // at the phase change.  (PV is issued by a softmax thread.)
     const uint32_t op0 = smem_u32(sm + kOffOp);
     bool ok = wait_bar(&ctl->q_ready, 0, abort, kWsQReady);
-    tc_fence_after();
-    // QK^T of tile iq and PV of tile ip are issued in whatever order they
-    // become ready (QK first when both are): PV of a tile is not held behind
-    // the conversion of the next one.  QK(iq) needs its operand stage
-    // converted and S(iq - 1) read by the softmax; PV(ip) needs P(ip).
-    int iq = 0, ip = 0;
-    uint64_t t_progress = globaltimer_ns();
-    uint32_t idle = 0;
-    while (ok && ip < ntiles) {
-      if (iq < ntiles && mbar_test(&ctl->full[iq % kStages], (iq / kStages) & 1) &&
-          (iq == 0 || mbar_test(&ctl->s_free, (iq - 1) & 1))) {
-        tc_fence_after();
-        const uint32_t base = op0 + (iq % kStages) * kOpTileBytes;
-#pragma unroll
-        for (int k = 0; k < kKSteps; ++k) {
-          const int ldim = 16 * k;  // first tile dim of this K step
-          const uint64_t bd =
-              ldim < 256 ? sdesc_sw128(base + (ldim >> 6) * kKBlockBytes + (ldim & 63) * 2, 16, 1024)
-                         : sdesc_sw64(base + kRopeBlock + (ldim - 256) * 2, 16, 512);
-          mma_ts(tb + kSCol, tb + kQCol + 8 * k, bd, idesc_qk, k > 0);
-        }
-        mma_commit(&ctl->s_full);
-        ++iq;
-      } else if (ip < iq && mbar_test(&ctl->p_full, ip & 1)) {
-        tc_fence_after();
-        const uint32_t base = op0 + (ip % kStages) * kOpTileBytes;
-#pragma unroll
-        for (int k = 0; k < kTileN / 16; ++k) {
-          const uint64_t bd = sdesc_sw128(base + k * 2048, kKBlockBytes, 1024);
-          mma_ts(tb + kOCol, tb + kPCol + 8 * k, bd, idesc_pv, (ip > 0 || k > 0));
-        }
-        mma_commit(&ctl->pv_done);
-        mma_commit(&ctl->freed[ip % kStages]);
-        ++ip;
-      } else {
-        // nothing ready: yield the issue slots briefly; give up (bounded)
-        __nanosleep(32);
-        if (*abort) break;
-        if ((++idle & 63u) == 0 && globaltimer_ns() - t_progress > kWaitNs) {
-          atomicOr(&g_decode_error,
-                   SMLA_DEVERR_TIMEOUT | (1u << (8 + (iq < ntiles ? kWsFull : kWsPFull))));
-          *abort = 1;
-          break;
-        }
-        continue;
-      }
-      t_progress = globaltimer_ns();
+#pragma unroll 1
+    for (int i = 0; i < ntiles && ok; ++i) {
+      ok = wait_bar(&ctl->full[i % kStages], (i / kStages) & 1, abort, kWsFull) &&
+           (i == 0 || wait_bar(&ctl->s_free, (i - 1) & 1, abort, kWsSFree));
+      if (!ok) break;
+      tc_fence_after();
+      issue_qk(tb, op0 + (i % kStages) * kOpTileBytes);
+      mma_commit(&ctl->s_full);
     }
     // drain: every MMA issued above has completed before TMEM is released
     // (waited on even after an abort, with its own bound).  A CTA whose row
@@ -984,7 +1000,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_init(&ctl->s_full, 1);
     mbar_init(&ctl->s_free, 128);
-    mbar_init(&ctl->p_full, 128);
     mbar_init(&ctl->pv_done, 1);
     for (int st = 0; st < kRawStages; ++st) {
       mbar_init(&ctl->raw_full[st], kLoaders);  // one arrival per loader
@@ -995,6 +1010,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->xb[b], 1);
     }
     mbar_init(&ctl->end, 1);
+    mbar_init(&ctl->end_pv, 1);
     ctl->abort = 0;
     fence_mbar_init_cluster();
     // q lands in the (still idle) operand stages while the CTA sets up
@@ -1215,6 +1231,24 @@ cudaError_t encode_q_maps(DecodeArgs& a) {
   return cudaSuccess;
 }
 
+// The kernels' shared-memory size attribute, set once per device and kernel,
+// safe when several host threads make their first launch at once.
+constexpr int kMaxDevices = 64;
+
+template <bool kFused>
+cudaError_t ensure_smem_attribute(int dev) {
+  static std::atomic<bool> done[kMaxDevices];
+  static std::mutex m;
+  const bool tracked = dev >= 0 && dev < kMaxDevices;
+  if (tracked && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(m);
+  if (tracked && done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(sparse_mla_decode_kernel<kFused>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess && tracked) done[dev].store(true, std::memory_order_release);
+  return e;
+}
+
 template <bool kFused>
 cudaError_t launch_impl(const DecodeArgs& args, cudaStream_t s) {
   DecodeArgs a = args;
@@ -1231,13 +1265,8 @@ cudaError_t launch_impl(const DecodeArgs& args, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  static bool attr_done[64] = {};
-  if (dev < 64 && !attr_done[dev]) {
-    e = cudaFuncSetAttribute(sparse_mla_decode_kernel<kFused>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
+  e = ensure_smem_attribute<kFused>(dev);
+  if (e != cudaSuccess) return e;
   const int64_t ctas = 2 * int64_t(a.T) * a.splits;
   sparse_mla_decode_kernel<kFused><<<dim3(unsigned(ctas)), dim3(kThreads), kSmemBytes, s>>>(a);
   return cudaGetLastError();
@@ -1265,7 +1294,6 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes]
 
 namespace {
 
-constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mutex;
 void* g_noalloc_ptr[kMaxDevices] = {};
 

@@ -1,7 +1,8 @@
 // Thin inline-PTX wrappers for the sm_100-family features the decode kernel
 // uses: mbarriers (local and cluster-remote), tensor memory (TMEM) allocation
-// and loads/stores, tcgen05 MMAs with shared-memory / TMEM operands, cluster
-// shared-memory addressing, and Ampere-style 16-byte async copies.
+// and loads/stores, tcgen05 MMAs with a TMEM A operand, cluster shared-memory
+// addressing, TMA tile loads, per-warpgroup register budgets and Ampere-style
+// 16-byte async copies.
 //
 // The try-wait helpers return after one probe; callers loop with an
 // iteration bound, so no wait here can hang a GPU.  Nothing traps.
@@ -34,11 +35,6 @@ __device__ __forceinline__ uint32_t map_to_cta(uint32_t local_addr, uint32_t cta
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};"
-               :: "r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
 // Asynchronous 16-byte store into another CTA's shared memory (`addr` and
@@ -175,15 +171,9 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
 }
-
-// Bulk asynchronous copy of `bytes` (a multiple of 16, both addresses 16-byte
-// aligned) from global memory into this CTA's shared memory; its completion
-// counts `bytes` transaction bytes on `bar`.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      :: "r"(dst), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+// Wait for every cp.async this thread has issued, committed or not.
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // 2-D tiled TMA load of the box at (x, y) of `map` into this CTA's shared
@@ -216,6 +206,20 @@ __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, boo
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(r) : "r"(uint32_t(pred)), "r"(id), "r"(nthreads) : "memory");
   return r != 0;
+}
+
+// ------------------------------------------------------ register budgets
+// Per-warpgroup register budgets (all four warps of an aligned warpgroup run
+// the same instruction).  An increase waits until other warpgroups of the
+// CTA have released enough registers with a decrease; the budgets the kernel
+// uses add up to no more than the CTA was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(N));
 }
 
 // --------------------------------------------------------------------- TMEM
@@ -323,16 +327,6 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn_maj
                                                       bool b_mn_major) {
   return (1u << 4) | (uint32_t(a_mn_major) << 15) | (uint32_t(b_mn_major) << 16) |
          (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
-}
-
-// D[tmem] (+)= A[smem] * B[smem]^T
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]^T
