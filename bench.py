@@ -237,33 +237,53 @@ def _timed_steps(fn, n, flush, stream):
     return [a.elapsed_time(b) for a, b in zip(starts, ends)]
 
 
-def _pipeline_decode_ms(step, wl, n, flush, stream):
-    """Per-launch times of the per-shard decode kernel inside the 2D+1 launch
-    pipeline (events on the launching stream around each decode launch)."""
+def _pipeline_launch_ms(step, wl, n, flush, stream):
+    """Per-launch times of the three kernels inside the 2D+1 launch pipeline
+    (events on the launching stream around each launch; L2 flushed before
+    each step).  Returns (index [n, D], decode [n, D], merge [n]) in ms."""
     import torch
 
     from sparse_mla_decode_dcp_gb300 import capi
     D = wl.D
-    out = []
+    idx, dec, mrg = [], [], []
     for _ in range(n):
         flush.fill_(1)
-        evs = []
+        ev_i, ev_d = [], []
         for d in range(D):
-            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            ev[0].record(stream)
             capi.dcp_filter_convert_index(
                 step.req_id, step.block_tables[d], step.topk, D, d, wl.spec.block_size,
-                bt_width=step.bt_widths[d], local_slots=step.local_slots[d],
+                interleave=wl.spec.interleave, bt_width=step.bt_widths[d],
+                local_slots=step.local_slots[d],
                 valid_count=step.valid_count[d])
-            ev[0].record(stream)
+            ev[1].record(stream)
             capi.sparse_mla_decode(step.q, step.pools[d], step.local_slots[d], wl.spec.sm_scale,
                                    out=step.part_out[d], lse=step.part_lse[d],
                                    workspace=step.workspace)
-            ev[1].record(stream)
-            evs.append(ev)
+            ev[2].record(stream)
+            ev_i.append((ev[0], ev[1]))
+            ev_d.append((ev[1], ev[2]))
+        em = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        em[0].record(stream)
         capi.dcp_lse_merge(step.part_out, step.part_lse, out=step.out, lse=step.lse)
+        em[1].record(stream)
         torch.cuda.synchronize()
-        out.append([a.elapsed_time(b) for a, b in evs])
-    return np.array(out)  # [n, D]
+        idx.append([a.elapsed_time(b) for a, b in ev_i])
+        dec.append([a.elapsed_time(b) for a, b in ev_d])
+        mrg.append(em[0].elapsed_time(em[1]))
+    return np.array(idx), np.array(dec), np.array(mrg)
+
+
+def _hbm_roofline(kernel, launch_ms, nbytes, peaks, unit_note):
+    """HBM roofline of a memory-bound kernel: algorithmic bytes per launch
+    over its mean launch time, against the measured copy bandwidth."""
+    achieved = nbytes / (launch_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": kernel,
+            "launch_us": launch_ms * 1e3, "algorithmic_bytes_per_launch": nbytes,
+            "bytes": unit_note,
+            "peak_source": f"{peaks['source']} MEASURED_PEAKS.json copy bandwidth"}
 
 
 def _roofline(kernel, launch_ms, keys_per_launch, H, peaks, workload):
@@ -365,7 +385,7 @@ def run_gpu(args):
     # The other form of the same step, and per-launch decode times.
     n_aux = max(10, min(args.steps, 50))
     alt_ms = float(np.mean(_timed_steps(alt_fn, n_aux, flush, stream)))
-    dec_ms = _pipeline_decode_ms(step, wl, n_aux, flush, stream)
+    idx_ms, dec_ms, mrg_ms = _pipeline_launch_ms(step, wl, n_aux, flush, stream)
     if args.path == "fused":
         roof = _roofline("smla_dcp_sparse_mla_decode_fused", ms_per_step, total_keys, H, peaks,
                          args.workload)
@@ -380,6 +400,15 @@ def run_gpu(args):
     fused_ms = ms_per_step if args.path == "fused" else alt_ms
     per_shard_roof = _roofline("smla_sparse_mla_decode", float(dec_ms.mean()), total_keys / D, H,
                                peaks, args.workload)
+    # index: read the top-k ids and write the slots (4 B each per entry),
+    # read the row's request id and write its valid count
+    index_roof = _hbm_roofline("smla_dcp_filter_convert_index", float(idx_ms.mean()),
+                               8 * T * K + 8 * T, peaks,
+                               "8 B per top-k entry (id in, slot out) + 8 B per row")
+    # merge: D partial rows of 512 bf16 + fp32 lse in, one merged row out
+    merge_roof = _hbm_roofline("smla_dcp_lse_merge", float(mrg_ms.mean()),
+                               (D + 1) * T * H * (2 * V_DIM + 4), peaks,
+                               "(D + 1) x (1024 B out row + 4 B lse) per (token, head)")
 
     # End to end through the public API with host buffers: every step copies
     # q and the top-k ids from pinned host memory and reads out + lse back.
@@ -418,7 +447,11 @@ def run_gpu(args):
             "pipeline": {"ms_per_step": pipeline_ms, "value": world * T / (pipeline_ms * 1e-3),
                          "launches_per_step": step.launches_per_step,
                          "decode_launch_us": [float(x) * 1e3 for x in dec_ms.mean(axis=0)],
-                         "decode_roofline": per_shard_roof},
+                         "decode_roofline": per_shard_roof,
+                         "index_launch_us": [float(x) * 1e3 for x in idx_ms.mean(axis=0)],
+                         "index_roofline": index_roof,
+                         "merge_launch_us": float(mrg_ms.mean()) * 1e3,
+                         "merge_roofline": merge_roof},
         },
         "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},

@@ -96,11 +96,14 @@ smla_status smla_get_device_error(uint32_t* flags, int clear);
  * the _forward_fp8_kv_mixed_batch snippet; P1 Summary].
  *
  * For row i (request r = req_id_per_token[i]) and entry j, with t =
- * topk_global[i*K + j]:
- *   t < 0 or t mod D != rank          -> local_slots[i*K + j] = -1
- *   otherwise lp = t div D (interleave 1: rank-local position),
- *             local_slots[i*K + j] = block_table[r*bt_row_stride + lp div
- *                                    block_size] * block_size + lp mod block_size
+ * topk_global[i*K + j] and interleave size I (runs of I consecutive
+ * positions go to the ranks in turn; the pages name the size,
+ * cp_kv_cache_interleave_size, and validate only I = 1 [P3 implementation
+ * breakdown step 4]):
+ *   t < 0 or (t div I) mod D != rank  -> local_slots[i*K + j] = -1
+ *   otherwise lp = (t div (I*D))*I + t mod I (rank-local position; I = 1:
+ *             t div D), local_slots[i*K + j] = block_table[r*bt_row_stride +
+ *             lp div block_size] * block_size + lp mod block_size
  * The -1s stay in place (compact_valid_to_front = False).  With D = 1 and
  * rank = 0 this is the plain paged request-index -> slot conversion.
  * valid_count[i] (optional, may be NULL) receives the number of
@@ -113,17 +116,17 @@ smla_status smla_get_device_error(uint32_t* flags, int clear);
  *   local_slots       device int32 [T, K] output (may not alias inputs)
  *   valid_count       device int32 [T] output or NULL
  * Errors: INVALID_ARG for null pointers (T > 0), T < 0, K < 1, D < 1,
- * rank outside [0, D), block_size < 1, num_reqs < 1, bt_width < 1 or
- * bt_row_stride < bt_width.  On the device an out-of-range request id or a
- * position past the block table (or in a -1 block) yields -1 and sets a
- * device error bit.
+ * rank outside [0, D), block_size < 1, interleave < 1, num_reqs < 1,
+ * bt_width < 1 or bt_row_stride < bt_width.  On the device an out-of-range
+ * request id or a position past the block table (or in a -1 block) yields -1
+ * and sets a device error bit.
  */
 smla_status smla_dcp_filter_convert_index(
     const int32_t* req_id_per_token, const int32_t* block_table,
     int64_t bt_row_stride, int32_t bt_width, int32_t num_reqs,
     const int32_t* topk_global, int32_t T, int32_t K, int32_t D, int32_t rank,
-    int32_t block_size, int32_t* local_slots, int32_t* valid_count,
-    void* stream);
+    int32_t block_size, int32_t interleave, int32_t* local_slots,
+    int32_t* valid_count, void* stream);
 
 /*
  * Bytes of caller-owned workspace smla_sparse_mla_decode needs for (T, H,
@@ -218,7 +221,7 @@ smla_status smla_sparse_mla_decode_noalloc(
  *
  *   q, T, H, K, sm_scale, out, lse   as in smla_sparse_mla_decode (out/lse
  *                                    receive the merged result)
- *   req_id_per_token, topk_global, num_reqs, D, block_size
+ *   req_id_per_token, topk_global, num_reqs, D, block_size, interleave
  *                                    as in smla_dcp_filter_convert_index
  *   kv_caches      host array of D device pointers, pool d = uint8
  *                  [num_slots[d], 656], 16-byte aligned
@@ -227,14 +230,15 @@ smla_status smla_sparse_mla_decode_noalloc(
  *                  [num_reqs, bt_row_strides[d]], columns [0, bt_widths[d])
  *   workspace      >= smla_decode_workspace_size(T, H, K) bytes, same rules
  *                  as for smla_sparse_mla_decode
- * Errors: as the three calls above; UNSUPPORTED for D > SMLA_MAX_DCP.
+ * Errors: as the three calls above (INVALID_ARG for interleave < 1);
+ * UNSUPPORTED for D > SMLA_MAX_DCP.
  * Device-side input errors (ids past a block table, bad request ids, slots
  * past a pool) drop the entry and set the device error word.
  */
 smla_status smla_dcp_sparse_mla_decode_fused(
     const uint16_t* q, int32_t T, int32_t H, int32_t K, float sm_scale,
     const int32_t* req_id_per_token, const int32_t* topk_global, int32_t num_reqs,
-    int32_t D, int32_t block_size, const uint8_t* const* kv_caches,
+    int32_t D, int32_t block_size, int32_t interleave, const uint8_t* const* kv_caches,
     const int64_t* num_slots, const int32_t* const* block_tables,
     const int64_t* bt_row_strides, const int32_t* bt_widths, uint16_t* out,
     float* lse, void* workspace, size_t workspace_bytes, void* stream);

@@ -41,7 +41,7 @@ SIGNATURES = {
     "smla_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
     "smla_dcp_filter_convert_index": (ctypes.c_int, [
         _c_vp, _c_vp, _c_i64, _c_i32, _c_i32, _c_vp, _c_i32, _c_i32, _c_i32, _c_i32,
-        _c_i32, _c_vp, _c_vp, _c_vp]),
+        _c_i32, _c_i32, _c_vp, _c_vp, _c_vp]),
     "smla_decode_workspace_size": (_c_sz, [_c_i32, _c_i32, _c_i32]),
     "smla_sparse_mla_decode": (ctypes.c_int, [
         _c_vp, _c_vp, _c_i64, _c_vp, _c_i32, _c_i32, _c_i32, ctypes.c_float, _c_vp,
@@ -51,7 +51,7 @@ SIGNATURES = {
         _c_vp]),
     "smla_dcp_sparse_mla_decode_fused": (ctypes.c_int, [
         _c_vp, _c_i32, _c_i32, _c_i32, ctypes.c_float, _c_vp, _c_vp, _c_i32, _c_i32, _c_i32,
-        _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]),
+        _c_i32, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]),
     "smla_dcp_lse_merge": (ctypes.c_int, [
         _c_vp, _c_vp, _c_i32, _c_i32, _c_i32, _c_vp, _c_vp, _c_vp]),
 }
@@ -114,7 +114,8 @@ def get_device_error(clear: bool = True) -> int:
 
 def dcp_filter_convert_index(req_id_per_token: torch.Tensor, block_table: torch.Tensor,
                              topk_global: torch.Tensor, D: int, rank: int,
-                             block_size: int, *, bt_width: Optional[int] = None,
+                             block_size: int, *, interleave: int = 1,
+                             bt_width: Optional[int] = None,
                              local_slots: Optional[torch.Tensor] = None,
                              valid_count: Optional[torch.Tensor] = None,
                              with_valid_count: bool = True,
@@ -139,7 +140,7 @@ def dcp_filter_convert_index(req_id_per_token: torch.Tensor, block_table: torch.
     st = load().smla_dcp_filter_convert_index(
         req_id_per_token.data_ptr(), block_table.data_ptr(), block_table.stride(0),
         width, block_table.shape[0], topk_global.data_ptr(), T, K, D, rank,
-        block_size, local_slots.data_ptr(),
+        block_size, int(interleave), local_slots.data_ptr(),
         valid_count.data_ptr() if valid_count is not None else None,
         _stream_ptr(stream, dev))
     _check("smla_dcp_filter_convert_index", st)
@@ -232,7 +233,8 @@ def sparse_mla_decode_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, local_slo
 def dcp_sparse_mla_decode_fused(q: torch.Tensor, req_id_per_token: torch.Tensor,
                                 topk_global: torch.Tensor, kv_caches: Sequence[torch.Tensor],
                                 block_tables: Sequence[torch.Tensor], block_size: int,
-                                sm_scale: float, *, bt_widths: Optional[Sequence[int]] = None,
+                                sm_scale: float, *, interleave: int = 1,
+                                bt_widths: Optional[Sequence[int]] = None,
                                 out: Optional[torch.Tensor] = None,
                                 lse: Optional[torch.Tensor] = None,
                                 workspace: Optional[torch.Tensor] = None,
@@ -277,7 +279,8 @@ def dcp_sparse_mla_decode_fused(q: torch.Tensor, req_id_per_token: torch.Tensor,
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = load().smla_dcp_sparse_mla_decode_fused(
         q.data_ptr(), T, H, K, float(sm_scale), req_id_per_token.data_ptr(),
-        topk_global.data_ptr(), num_reqs, D, block_size, pools, nslots, bts, strides, wids,
+        topk_global.data_ptr(), num_reqs, D, block_size, int(interleave), pools, nslots, bts,
+        strides, wids,
         out.data_ptr(), lse.data_ptr(), ws_ptr, ws_bytes, _stream_ptr(stream, dev))
     _check("smla_dcp_sparse_mla_decode_fused", st)
     return out, lse

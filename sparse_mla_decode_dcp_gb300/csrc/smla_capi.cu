@@ -47,10 +47,10 @@ smla_status smla_dcp_filter_convert_index(
     const int32_t* req_id_per_token, const int32_t* block_table,
     int64_t bt_row_stride, int32_t bt_width, int32_t num_reqs,
     const int32_t* topk_global, int32_t T, int32_t K, int32_t D, int32_t rank,
-    int32_t block_size, int32_t* local_slots, int32_t* valid_count,
+    int32_t block_size, int32_t interleave, int32_t* local_slots, int32_t* valid_count,
     void* stream) {
   if (T < 0 || K < 1 || D < 1 || rank < 0 || rank >= D || block_size < 1 ||
-      num_reqs < 1 || bt_width < 1 || bt_row_stride < bt_width)
+      interleave < 1 || num_reqs < 1 || bt_width < 1 || bt_row_stride < bt_width)
     return SMLA_ERR_INVALID_ARG;
   if (T == 0) return SMLA_OK;
   if (!req_id_per_token || !block_table || !topk_global || !local_slots)
@@ -71,6 +71,7 @@ smla_status smla_dcp_filter_convert_index(
   a.D = D;
   a.rank = rank;
   a.block_size = block_size;
+  a.interleave = interleave;
   a.local_slots = local_slots;
   a.valid_count = valid_count;
   return from_cuda(smla::launch_filter_convert(a, static_cast<cudaStream_t>(stream)));
@@ -147,11 +148,11 @@ smla_status smla_sparse_mla_decode_noalloc(
 smla_status smla_dcp_sparse_mla_decode_fused(
     const uint16_t* q, int32_t T, int32_t H, int32_t K, float sm_scale,
     const int32_t* req_id_per_token, const int32_t* topk_global, int32_t num_reqs,
-    int32_t D, int32_t block_size, const uint8_t* const* kv_caches,
+    int32_t D, int32_t block_size, int32_t interleave, const uint8_t* const* kv_caches,
     const int64_t* num_slots, const int32_t* const* block_tables,
     const int64_t* bt_row_strides, const int32_t* bt_widths, uint16_t* out,
     float* lse, void* workspace, size_t workspace_bytes, void* stream) {
-  if (T < 0 || K < 1 || H < 1 || D < 1 || block_size < 1 || num_reqs < 1 ||
+  if (T < 0 || K < 1 || H < 1 || D < 1 || block_size < 1 || interleave < 1 || num_reqs < 1 ||
       !std::isfinite(sm_scale) || !(sm_scale > 0.f))
     return SMLA_ERR_INVALID_ARG;
   if (H > SMLA_MAX_HEADS || D > SMLA_MAX_DCP) return SMLA_ERR_UNSUPPORTED;
@@ -189,6 +190,7 @@ smla_status smla_dcp_sparse_mla_decode_fused(
   a.workspace_bytes = workspace_bytes;
   a.D = D;
   a.block_size = block_size;
+  a.interleave = interleave;
   a.num_reqs = num_reqs;
   a.req_id = req_id_per_token;
   a.topk = topk_global;

@@ -926,7 +926,9 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
 
 // Resolve raw entry v to (slot, shard).  Per-shard launch: the entry
 // already is a local slot.  Fused DCP step: the entry is a global position
-// v, owned by shard v mod D at local position v div D (interleave 1), then
+// v; with interleave size I, runs of I positions go to the shards in turn,
+// so v is owned by shard (v div I) mod D at local position
+// (v div (I D)) I + v mod I (I = 1: shard v mod D, position v div D), then
 // mapped through that shard's block-table row for this request (staged in
 // shared memory at `bt` when it fits, else read from global memory).
 // Returns false for -1 / foreign / invalid entries, recording input errors
@@ -945,8 +947,10 @@ __device__ __forceinline__ bool resolve_entry(const DecodeArgs& a, const Ctl* ct
     return v >= 0;
   }
   if (v < 0 || !req_ok) return false;
-  const int32_t lp = int32_t(fastdiv(uint32_t(v), a.div_D));
-  const int d = v - lp * a.D;
+  const uint32_t g = fastdiv(uint32_t(v), a.div_I);  // run of I positions
+  const uint32_t round = fastdiv(g, a.div_D);        // round of D runs
+  const int d = int(g - round * uint32_t(a.D));
+  const int32_t lp = int32_t(round) * a.interleave + (v - int32_t(g) * a.interleave);
   const int32_t col = int32_t(fastdiv(uint32_t(lp), a.div_bs));
   if (col >= ctl->bt_width[d]) {
     err |= SMLA_DEVERR_BLOCK_TABLE;
@@ -1278,6 +1282,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) { return launch_i
 
 cudaError_t launch_decode_fused(const DecodeArgs& args, cudaStream_t s) {
   DecodeArgs a = args;
+  a.div_I = make_fastdiv(uint32_t(a.interleave));
   a.div_D = make_fastdiv(uint32_t(a.D));
   a.div_bs = make_fastdiv(uint32_t(a.block_size));
   return launch_impl<true>(a, s);

@@ -17,6 +17,7 @@ struct IndexArgs {
   int32_t num_reqs;
   const int32_t* topk;
   int32_t T, K, D, rank, block_size;
+  int32_t interleave;  // I: runs of I consecutive positions per rank
   int32_t* local_slots;
   int32_t* valid_count;  // may be null
 };
@@ -66,8 +67,8 @@ struct DecodeArgs {
   int32_t* ws_tick;  // [T, 2] arrival counters, left at zero by every call
   // Fused DCP step only (D > 0): global top-k ids are converted per shard in
   // the kernel prologue and all shards' keys share one softmax.
-  int32_t D, block_size, num_reqs;
-  FastDiv div_D, div_bs;  // set by the fused launcher
+  int32_t D, block_size, num_reqs, interleave;
+  FastDiv div_I, div_D, div_bs;  // set by the fused launcher
   // q [T*H, 576] bf16 for TMA, set by the launcher: boxes of 64 dims x 128
   // head rows (128-byte swizzle) and 32 dims x 128 head rows (64-byte swizzle)
   CUtensorMap q_lat, q_rope;

@@ -18,10 +18,11 @@ What it builds, per workload:
   rows and a block table ``[R, W_d]`` (-1 where unused).  A request with
   ``n`` tokens on a shard owns ``ceil(n / block_size)`` physical blocks drawn
   from a random permutation of the shard's blocks, plus ~10% spare blocks that
-  nobody owns.  Which tokens a shard holds comes from the interleave-1 rule
-  (position p is held by shard p mod D); this module uses that rule only to
-  count how many rows each request owns on each shard, the bookkeeping a KV
-  block allocator does.
+  nobody owns.  Which tokens a shard holds comes from the interleave rule
+  (runs of I consecutive positions go to the shards in turn; I = 1: position
+  p is held by shard p mod D); this module uses that rule only to count how
+  many rows each request owns on each shard, the bookkeeping a KV block
+  allocator does.
 * ``q[T, H, 576]`` bf16 ~ N(0, 1).
 
 Row byte layout (the plainest reading of "576 vs 656 layout": the parts in the
@@ -84,6 +85,7 @@ class WorkloadSpec:
     neg_frac: float = 0.0  # fraction of K slots forced to -1 after padding
     spare_frac: float = 0.10
     sm_scale: float = 1.0 / math.sqrt(192.0)
+    interleave: int = 1  # I: runs of I consecutive positions per shard
 
     @property
     def num_tokens(self) -> int:
@@ -187,10 +189,14 @@ def draw_topk_row(rng: np.random.Generator, n_cand: int, K: int,
     return row.astype(np.int32)
 
 
-def rows_on_shard(ctx: int, D: int, d: int) -> int:
-    """How many of a request's ctx cached positions shard d holds under
-    interleave 1 (allocation bookkeeping only)."""
-    return len(range(d, int(ctx), D))
+def rows_on_shard(ctx: int, D: int, d: int, interleave: int = 1) -> int:
+    """How many of a request's ctx cached positions shard d holds when runs
+    of `interleave` consecutive positions go to the shards in turn
+    (allocation bookkeeping only): whole rounds of I*D positions give I each,
+    then the last partial round."""
+    I = int(interleave)
+    full, rem = divmod(int(ctx), I * D)
+    return full * I + min(max(rem - d * I, 0), I)
 
 
 def random_rows(n: int, gen: torch.Generator, device) -> torch.Tensor:
@@ -219,9 +225,10 @@ def random_rows(n: int, gen: torch.Generator, device) -> torch.Tensor:
 
 def build_shard(ctx: np.ndarray, D: int, d: int, block_size: int,
                 spare_frac: float, rng: np.random.Generator,
-                gen: torch.Generator, device, row_stride_pad: int = 0) -> Shard:
+                gen: torch.Generator, device, row_stride_pad: int = 0,
+                interleave: int = 1) -> Shard:
     R = len(ctx)
-    n = np.array([rows_on_shard(c, D, d) for c in ctx], dtype=np.int64)
+    n = np.array([rows_on_shard(c, D, d, interleave) for c in ctx], dtype=np.int64)
     nblk = (n + block_size - 1) // block_size
     used = int(nblk.sum())
     spare = max(1, int(math.ceil(spare_frac * used)))
@@ -276,7 +283,7 @@ def make_workload(spec: WorkloadSpec | str, seed: int = 0, device="cpu",
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     shards = [build_shard(ctx, spec.dcp, d, spec.block_size, spec.spare_frac,
-                          rng, gen, device, row_stride_pad)
+                          rng, gen, device, row_stride_pad, spec.interleave)
               for d in range(spec.dcp)]
     q = torch.randn((T, spec.heads, QK_DIM), generator=gen, device=device,
                     dtype=torch.float32).to(torch.bfloat16)

@@ -49,7 +49,8 @@ class DcpDecodeStep:
         wl = self.wl
         capi.dcp_filter_convert_index(
             self.req_id, self.block_tables[d], self.topk, wl.D, d, wl.spec.block_size,
-            bt_width=self.bt_widths[d], local_slots=self.local_slots[d],
+            interleave=wl.spec.interleave, bt_width=self.bt_widths[d],
+            local_slots=self.local_slots[d],
             valid_count=self.valid_count[d], stream=self.stream)
         capi.sparse_mla_decode(
             self.q, self.pools[d], self.local_slots[d], wl.spec.sm_scale,
@@ -61,7 +62,8 @@ class DcpDecodeStep:
         wl = self.wl
         return capi.dcp_sparse_mla_decode_fused(
             self.q, self.req_id, self.topk, self.pools, self.block_tables,
-            wl.spec.block_size, wl.spec.sm_scale, bt_widths=self.bt_widths,
+            wl.spec.block_size, wl.spec.sm_scale, interleave=wl.spec.interleave,
+            bt_widths=self.bt_widths,
             out=self.out, lse=self.lse, workspace=self.workspace, stream=self.stream)
 
     def run(self):

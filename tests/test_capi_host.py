@@ -57,11 +57,11 @@ FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced
 
 def _convert(lib, **kw):
     a = dict(req=FAKE, bt=FAKE, stride=4, width=4, nreq=2, topk=FAKE, T=3, K=8,
-             D=2, rank=0, bs=16, out=FAKE, cnt=None)
+             D=2, rank=0, bs=16, I=1, out=FAKE, cnt=None)
     a.update(kw)
     return lib.smla_dcp_filter_convert_index(
         a["req"], a["bt"], a["stride"], a["width"], a["nreq"], a["topk"], a["T"],
-        a["K"], a["D"], a["rank"], a["bs"], a["out"], a["cnt"], None)
+        a["K"], a["D"], a["rank"], a["bs"], a["I"], a["out"], a["cnt"], None)
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -71,6 +71,8 @@ def _convert(lib, **kw):
     (dict(rank=2), capi.SMLA_ERR_INVALID_ARG),
     (dict(rank=-1), capi.SMLA_ERR_INVALID_ARG),
     (dict(bs=0), capi.SMLA_ERR_INVALID_ARG),
+    (dict(I=0), capi.SMLA_ERR_INVALID_ARG),
+    (dict(I=-2), capi.SMLA_ERR_INVALID_ARG),
     (dict(nreq=0), capi.SMLA_ERR_INVALID_ARG),
     (dict(width=0), capi.SMLA_ERR_INVALID_ARG),
     (dict(stride=3), capi.SMLA_ERR_INVALID_ARG),
@@ -145,7 +147,7 @@ def test_workspace_size_shape_only(lib):
 
 
 def _fused(lib, D=2, **kw):
-    a = dict(q=FAKE, T=2, H=16, K=64, scale=0.07, req=FAKE, topk=FAKE, nreq=2, bs=16,
+    a = dict(q=FAKE, T=2, H=16, K=64, scale=0.07, req=FAKE, topk=FAKE, nreq=2, bs=16, I=1,
              pools=[FAKE] * D, nslots=[100] * D, bts=[FAKE] * D, strides=[4] * D,
              widths=[4] * D, out=FAKE, lse=FAKE, ws=None, wsb=0)
     a.update(kw)
@@ -153,7 +155,8 @@ def _fused(lib, D=2, **kw):
     arr = lambda typ, xs: (typ * n)(*(list(xs) + [0] * (n - len(xs)))[:n])
     return lib.smla_dcp_sparse_mla_decode_fused(
         a["q"], a["T"], a["H"], a["K"], ctypes.c_float(a["scale"]), a["req"], a["topk"],
-        a["nreq"], D, a["bs"], arr(ctypes.c_void_p, a["pools"]), arr(ctypes.c_int64, a["nslots"]),
+        a["nreq"], D, a["bs"], a["I"], arr(ctypes.c_void_p, a["pools"]),
+        arr(ctypes.c_int64, a["nslots"]),
         arr(ctypes.c_void_p, a["bts"]), arr(ctypes.c_int64, a["strides"]),
         arr(ctypes.c_int32, a["widths"]), a["out"], a["lse"], a["ws"], a["wsb"], None)
 
@@ -165,6 +168,7 @@ def _fused(lib, D=2, **kw):
     (2, dict(T=-1), capi.SMLA_ERR_INVALID_ARG),
     (2, dict(K=0), capi.SMLA_ERR_INVALID_ARG),
     (2, dict(bs=0), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(I=0), capi.SMLA_ERR_INVALID_ARG),
     (2, dict(nreq=0), capi.SMLA_ERR_INVALID_ARG),
     (2, dict(scale=float("nan")), capi.SMLA_ERR_INVALID_ARG),
     (2, dict(scale=-1.0), capi.SMLA_ERR_INVALID_ARG),

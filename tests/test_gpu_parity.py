@@ -324,14 +324,48 @@ def test_fused_small_batches_split_k(cuda_device, K):
     compare_out_lse(out, lse, ref_out, ref_lse, where=f"pipeline K={K}")
 
 
+@pytest.mark.parametrize("interleave", [2, 4, 64])
+def test_interleaved_step_matches_oracle(cuda_device, interleave):
+    """Interleave size I > 1 (runs of I consecutive positions per shard) end
+    to end: per-shard conversion bit-exact, the 2D+1 launch pipeline and the
+    fused step both against the oracle's merge of its per-shard decodes."""
+    dev = cuda_device
+    spec = inputs.WorkloadSpec(
+        name=f"interleave{interleave}", num_reqs=8, tokens_per_req=1, heads=128, topk=2048,
+        dcp=4, block_size=64, ctx_kind="uniform", ctx_lo=2000, ctx_hi=20000,
+        interleave=interleave)
+    wl = inputs.make_workload(spec, seed=interleave, device=dev)
+    step = DcpDecodeStep(wl, device=dev)
+    capi.get_device_error(clear=True)
+    out, lse = step.run()
+    torch.cuda.synchronize()
+    f_out, f_lse = step.run_fused()
+    torch.cuda.synchronize()
+    f_out, f_lse = f_out.clone(), f_lse.clone()
+    assert capi.get_device_error(clear=True) == 0
+    q_bits = _q_bits(wl.q)
+    outs, lses = [], []
+    for d, s in enumerate(wl.shards):
+        sl, cnt = oracle.dcp_filter_convert_index(wl.req_id, s.block_table, wl.topk, wl.D, d,
+                                                  spec.block_size, interleave)
+        assert np.array_equal(step.local_slots[d].cpu().numpy(), sl), f"shard {d}"
+        assert np.array_equal(step.valid_count[d].cpu().numpy(), cnt), f"shard {d}"
+        o, l = oracle.sparse_mla_decode(q_bits, s.pool.cpu().numpy(), sl, spec.sm_scale)
+        outs.append(o)
+        lses.append(l)
+    ref_out, ref_lse = oracle.lse_merge(outs, lses)
+    compare_out_lse(out, lse, ref_out, ref_lse, where=f"pipeline I={interleave}")
+    compare_out_lse(f_out, f_lse, ref_out, ref_lse, where=f"fused I={interleave}")
+
+
 # ---------------------------------------------------------- index edge cases
-def _convert_vs_oracle(req, bt, topk, D, rank, bs, dev, width=None):
+def _convert_vs_oracle(req, bt, topk, D, rank, bs, dev, width=None, interleave=1):
     ls, cnt = capi.dcp_filter_convert_index(
         torch.from_numpy(req).to(dev), torch.from_numpy(bt).to(dev),
-        torch.from_numpy(topk).to(dev), D, rank, bs, bt_width=width)
+        torch.from_numpy(topk).to(dev), D, rank, bs, interleave=interleave, bt_width=width)
     torch.cuda.synchronize()
     ref_ls, ref_cnt = oracle.dcp_filter_convert_index(
-        req, bt if width is None else bt[:, :width], topk, D, rank, bs)
+        req, bt if width is None else bt[:, :width], topk, D, rank, bs, interleave)
     assert np.array_equal(ls.cpu().numpy(), ref_ls)
     assert np.array_equal(cnt.cpu().numpy(), ref_cnt)
 
@@ -351,23 +385,27 @@ def test_index_worked_examples_on_gpu(cuda_device):
         assert cnt.cpu().tolist() == case["valid_count"], case["note"]
 
 
-@pytest.mark.parametrize("K", [1, 5, 37, 64, 2048, 3001])
+@pytest.mark.parametrize("K", [1, 5, 37, 64, 2048, 3001, 8192])
 @pytest.mark.parametrize("D", [1, 2, 3, 4, 8])
-def test_index_random_shapes(cuda_device, K, D):
-    rng = np.random.default_rng(K * 10 + D)
+@pytest.mark.parametrize("interleave", [1, 2, 4, 64])
+def test_index_random_shapes(cuda_device, K, D, interleave):
+    """Random requests, ids and -1s against the oracle, bit-exact, for every
+    rank; K spans one CTA per row and the four-CTA split (with a ragged last
+    chunk at 3001 and several 16-byte groups per thread at 8192)."""
+    rng = np.random.default_rng(K * 10 + D + 1000 * interleave)
     R, bs = 5, 16
     ctx = rng.integers(1, 5000, size=R)
-    W = int(max(-(-(c // D + 1) // bs) for c in ctx)) + 1
+    counts = [[inputs.rows_on_shard(int(c), D, d, interleave) for c in ctx] for d in range(D)]
+    W = int(max(-(-n // bs) for row in counts for n in row)) + 1
     for rank in range(D):
         bt = np.full((R, W + 3), -1, dtype=np.int32)
         for r in range(R):
-            n = len(range(rank, int(ctx[r]), D))
-            nb = -(-n // bs)
+            nb = -(-counts[rank][r] // bs)
             bt[r, :nb] = rng.permutation(10000)[:nb]
         req = rng.integers(0, R, size=7).astype(np.int32)
         topk = np.stack([np.where(rng.random(K) < 0.1, -1,
                                   rng.integers(0, int(ctx[r]), size=K)) for r in req]).astype(np.int32)
-        _convert_vs_oracle(req, bt, topk, D, rank, bs, cuda_device)
+        _convert_vs_oracle(req, bt, topk, D, rank, bs, cuda_device, interleave=interleave)
 
 
 def test_index_bad_inputs_masked_and_flagged(cuda_device):

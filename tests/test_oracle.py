@@ -482,6 +482,29 @@ def test_generator_structure_tiny():
         assert (~poison).sum() == s.live_rows
 
 
+@pytest.mark.parametrize("interleave", [1, 2, 4, 64])
+def test_generator_shard_sizes_follow_the_interleave_rule(interleave):
+    """The generator sizes each shard's block allocation from its own count of
+    the positions a shard holds; that count must equal the oracle's (pinned
+    by the append simulation), and the oracle's conversion of every id must
+    land inside the allocated blocks (it asserts otherwise)."""
+    for ctx in list(range(0, 300)) + [4095, 4096, 65537]:
+        for D in (1, 2, 3, 4, 8):
+            for d in range(D):
+                assert inputs.rows_on_shard(ctx, D, d, interleave) == \
+                    oracle.dcp_local_seq_len(ctx, D, d, interleave), (ctx, D, d)
+    spec = inputs.WorkloadSpec(name="il", num_reqs=3, tokens_per_req=1, heads=4, topk=256,
+                               dcp=4, block_size=16, ctx_kind="uniform", ctx_lo=100,
+                               ctx_hi=3000, interleave=interleave)
+    wl = inputs.make_workload(spec, seed=interleave)
+    for d, s in enumerate(wl.shards):
+        assert s.live_rows == sum(oracle.dcp_local_seq_len(c, 4, d, interleave) for c in wl.ctx)
+        sl, cnt = oracle.dcp_filter_convert_index(wl.req_id, s.block_table, wl.topk, 4, d, 16,
+                                                  interleave)
+        live = ~(s.pool.numpy()[sl[sl >= 0]] == 0xFF).all(axis=1)
+        assert live.all()  # every converted id points at a filled row
+
+
 # ------------------------------------------------------------- top-k select
 def test_topk_select_matches_torch_topk_on_distinct_scores():
     rng = np.random.default_rng(21)
