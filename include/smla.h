@@ -16,6 +16,11 @@
  *   smla_sparse_mla_decode_noalloc    step 2 with library-owned split-K
  *                                     scratch (no workspace argument)
  *
+ * and the dense form of the decode (every cached position of a request's
+ * causal context instead of a top-k list):
+ *
+ *   smla_dcp_dense_mla_decode         per rank or merged over D pools
+ *
  * Sources (page title, then section):
  *   [P1] "[eldritch] attention: support DCP in SM120 FlashInfer sparse MLA"
  *   [P2] "[Bugfix][Attention] Stabilize sparse-MLA DCP for GLM PCP evals"
@@ -67,7 +72,9 @@ enum {
   SMLA_DEVERR_BLOCK_TABLE = 1u, /* id past the block table / unallocated block */
   SMLA_DEVERR_REQ_ID = 2u,      /* req_id_per_token outside [0, num_reqs)      */
   SMLA_DEVERR_SLOT_RANGE = 4u,  /* local slot >= num_slots                     */
-  SMLA_DEVERR_TIMEOUT = 8u      /* a bounded wait inside a kernel gave up      */
+  SMLA_DEVERR_TIMEOUT = 8u,     /* a bounded wait inside a kernel gave up      */
+  SMLA_DEVERR_CONTEXT = 16u     /* dense decode: a context shorter than its
+                                   request's query tokens or past max_ctx     */
 };
 /* With SMLA_DEVERR_TIMEOUT, bits 8..31 of the word tell which of the decode
  * kernel's internal waits gave up (a diagnostic bitmask, one bit per site). */
@@ -239,6 +246,54 @@ smla_status smla_dcp_sparse_mla_decode_fused(
     const uint16_t* q, int32_t T, int32_t H, int32_t K, float sm_scale,
     const int32_t* req_id_per_token, const int32_t* topk_global, int32_t num_reqs,
     int32_t D, int32_t block_size, int32_t interleave, const uint8_t* const* kv_caches,
+    const int64_t* num_slots, const int32_t* const* block_tables,
+    const int64_t* bt_row_strides, const int32_t* bt_widths, uint16_t* out,
+    float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Dense MLA decode with LSE return under DCP [P3 key snippets: the dense
+ * FlashMLA decode path, whose LSE comes back as [batch, heads, seq_len] and
+ * is flattened to [tokens, heads] for the DCP merge; implementation breakdown
+ * step 5].
+ *
+ * Request b has S query tokens (S > 1: an MTP / speculative step); token s
+ * sits at position p = ctx_lens[b] - S + s and attends every cached position
+ * 0..p of its request (causal), with the attention of smla_sparse_mla_decode
+ * over those positions' cache rows.  Position t lives on rank (t div I) mod
+ * D at local position (t div (I*D))*I + t mod I, as in
+ * smla_dcp_filter_convert_index.
+ *   rank = -1       attend all D pools in one launch: out/lse are the merged
+ *                   result (the LSE merge of the ranks' partials)
+ *   rank in [0, D)  attend only rank's positions: out/lse are that rank's
+ *                   partial, to be combined with smla_dcp_lse_merge
+ * Rows come out in token order b*S + s: out [B*S, H, 512], lse [B*S, H] --
+ * the pages' [batch, heads, seq_len] -> [tokens, heads] flattening.
+ *
+ *   q              device bf16 [B*S, H, 576]
+ *   ctx_lens       device int32 [B], each in [S, max_ctx]
+ *   max_ctx        host bound on every ctx_lens[b] (sizes the split-K)
+ *   kv_caches, num_slots, block_tables, bt_row_strides, bt_widths
+ *                  host arrays of D entries as in
+ *                  smla_dcp_sparse_mla_decode_fused (block-table row b
+ *                  belongs to request b); with rank >= 0 only entry [rank]
+ *                  is read and the others may be NULL / 0
+ *   workspace      >= smla_dense_decode_workspace_size(B*S, H, max_ctx, D,
+ *                  interleave, rank) bytes, same rules as for
+ *                  smla_sparse_mla_decode
+ * Errors: INVALID_ARG for null pointers, B < 0, S < 1, H < 1, max_ctx < 1,
+ * D < 1, rank outside [-1, D), block_size < 1, interleave < 1, a bad pool or
+ * table entry that is read, misaligned q/out/lse; UNSUPPORTED for H >
+ * SMLA_MAX_HEADS or D > SMLA_MAX_DCP; WORKSPACE as for smla_sparse_mla_decode.
+ * On the device a request whose context is outside [S, max_ctx] comes out
+ * as (0, -inf) in all its rows and sets SMLA_DEVERR_CONTEXT; a position past
+ * a block table sets SMLA_DEVERR_BLOCK_TABLE.
+ */
+size_t smla_dense_decode_workspace_size(int32_t T, int32_t H, int32_t max_ctx, int32_t D,
+                                        int32_t interleave, int32_t rank);
+smla_status smla_dcp_dense_mla_decode(
+    const uint16_t* q, int32_t B, int32_t S, int32_t H, float sm_scale,
+    const int32_t* ctx_lens, int32_t max_ctx, int32_t D, int32_t rank,
+    int32_t block_size, int32_t interleave, const uint8_t* const* kv_caches,
     const int64_t* num_slots, const int32_t* const* block_tables,
     const int64_t* bt_row_strides, const int32_t* bt_widths, uint16_t* out,
     float* lse, void* workspace, size_t workspace_bytes, void* stream);

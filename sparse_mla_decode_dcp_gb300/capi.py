@@ -26,6 +26,7 @@ DEVERR_BLOCK_TABLE = 1
 DEVERR_REQ_ID = 2
 DEVERR_SLOT_RANGE = 4
 DEVERR_TIMEOUT = 8
+DEVERR_CONTEXT = 16
 
 MAX_HEADS = 128
 MAX_DCP = 16
@@ -51,6 +52,11 @@ SIGNATURES = {
         _c_vp]),
     "smla_dcp_sparse_mla_decode_fused": (ctypes.c_int, [
         _c_vp, _c_i32, _c_i32, _c_i32, ctypes.c_float, _c_vp, _c_vp, _c_i32, _c_i32, _c_i32,
+        _c_i32, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]),
+    "smla_dense_decode_workspace_size": (_c_sz, [_c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
+                                                 _c_i32]),
+    "smla_dcp_dense_mla_decode": (ctypes.c_int, [
+        _c_vp, _c_i32, _c_i32, _c_i32, ctypes.c_float, _c_vp, _c_i32, _c_i32, _c_i32, _c_i32,
         _c_i32, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]),
     "smla_dcp_lse_merge": (ctypes.c_int, [
         _c_vp, _c_vp, _c_i32, _c_i32, _c_i32, _c_vp, _c_vp, _c_vp]),
@@ -283,6 +289,70 @@ def dcp_sparse_mla_decode_fused(q: torch.Tensor, req_id_per_token: torch.Tensor,
         strides, wids,
         out.data_ptr(), lse.data_ptr(), ws_ptr, ws_bytes, _stream_ptr(stream, dev))
     _check("smla_dcp_sparse_mla_decode_fused", st)
+    return out, lse
+
+
+def dense_decode_workspace_size(T: int, H: int, max_ctx: int, D: int, interleave: int = 1,
+                                rank: int = -1) -> int:
+    return int(load().smla_dense_decode_workspace_size(T, H, max_ctx, D, interleave, rank))
+
+
+def dcp_dense_mla_decode(q: torch.Tensor, ctx_lens: torch.Tensor, max_ctx: int, S: int,
+                         kv_caches: Sequence[Optional[torch.Tensor]],
+                         block_tables: Sequence[Optional[torch.Tensor]], block_size: int,
+                         sm_scale: float, *, rank: int = -1, interleave: int = 1,
+                         bt_widths: Optional[Sequence[int]] = None,
+                         out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                         workspace: Optional[torch.Tensor] = None,
+                         stream: Optional[torch.cuda.Stream] = None
+                         ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Dense decode over each request's whole causal context: merged over the
+    D pools (rank = -1) or one rank's partial (rank >= 0; only its pool and
+    table are read).  q is [B*S, H, 576]; rows come out in token order b*S+s."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev)
+    _need(ctx_lens, "ctx_lens", torch.int32, dev)
+    T, H, Dq = q.shape
+    B = ctx_lens.shape[0]
+    if Dq != QK_DIM or T != B * S:
+        raise ValueError("q must be [B*S, H, 576] with B = len(ctx_lens)")
+    D = len(kv_caches)
+    if D != len(block_tables) or D < 1:
+        raise ValueError("need one block table per KV pool (>= 1)")
+    used = [d for d in range(D) if rank < 0 or d == rank]
+    for d in used:
+        kv, bt = kv_caches[d], block_tables[d]
+        _need(kv, "kv_caches[d]", torch.uint8, dev)
+        if kv.dim() != 2 or kv.shape[1] != ROW_BYTES:
+            raise ValueError(f"kv_caches[d] must be [num_slots, {ROW_BYTES}] uint8")
+        if bt.dtype != torch.int32 or bt.device != dev or bt.dim() != 2 or bt.stride(1) != 1:
+            raise ValueError("block_tables[d] must be 2-D int32 with contiguous rows")
+    if out is None:
+        out = torch.empty((T, H, V_DIM), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, dev)
+    _need(lse, "lse", torch.float32, dev)
+    if workspace is None:
+        n = dense_decode_workspace_size(T, H, max_ctx, D, interleave, rank)
+        workspace = torch.zeros(n, dtype=torch.uint8, device=dev) if n else None
+    widths = [0] * D
+    for d in used:
+        widths[d] = block_tables[d].shape[1] if bt_widths is None else int(bt_widths[d])
+    ptr = lambda t: t.data_ptr() if t is not None else None
+    pools = (ctypes.c_void_p * D)(*[ptr(kv_caches[d]) if d in used else None for d in range(D)])
+    nslots = (ctypes.c_int64 * D)(*[kv_caches[d].shape[0] if d in used else 0 for d in range(D)])
+    bts = (ctypes.c_void_p * D)(*[ptr(block_tables[d]) if d in used else None for d in range(D)])
+    strides = (ctypes.c_int64 * D)(*[block_tables[d].stride(0) if d in used else 0
+                                     for d in range(D)])
+    wids = (ctypes.c_int32 * D)(*widths)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().smla_dcp_dense_mla_decode(
+        q.data_ptr(), B, S, H, float(sm_scale), ctx_lens.data_ptr(), int(max_ctx), D, int(rank),
+        int(block_size), int(interleave), pools, nslots, bts, strides, wids, out.data_ptr(),
+        lse.data_ptr(), ws_ptr, ws_bytes, _stream_ptr(stream, dev))
+    _check("smla_dcp_dense_mla_decode", st)
     return out, lse
 
 

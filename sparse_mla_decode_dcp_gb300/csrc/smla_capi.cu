@@ -197,6 +197,79 @@ smla_status smla_dcp_sparse_mla_decode_fused(
   return from_cuda(smla::launch_decode_fused(a, static_cast<cudaStream_t>(stream)));
 }
 
+// Raw entries per row of the dense decode: positions 0..max_ctx-1, or the
+// largest count of them one rank holds.
+static int32_t dense_entries(int32_t max_ctx, int32_t D, int32_t interleave, int32_t rank) {
+  if (rank < 0) return max_ctx;
+  const int64_t id = int64_t(interleave) * D;
+  return int32_t(((int64_t(max_ctx) + id - 1) / id) * interleave);
+}
+
+size_t smla_dense_decode_workspace_size(int32_t T, int32_t H, int32_t max_ctx, int32_t D,
+                                        int32_t interleave, int32_t rank) {
+  if (T < 0 || H < 1 || H > SMLA_MAX_HEADS || max_ctx < 1 || D < 1 || interleave < 1 ||
+      rank < -1 || rank >= D)
+    return 0;
+  return smla::decode_workspace_bytes(T, H, dense_entries(max_ctx, D, interleave, rank));
+}
+
+smla_status smla_dcp_dense_mla_decode(
+    const uint16_t* q, int32_t B, int32_t S, int32_t H, float sm_scale,
+    const int32_t* ctx_lens, int32_t max_ctx, int32_t D, int32_t rank,
+    int32_t block_size, int32_t interleave, const uint8_t* const* kv_caches,
+    const int64_t* num_slots, const int32_t* const* block_tables,
+    const int64_t* bt_row_strides, const int32_t* bt_widths, uint16_t* out,
+    float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 0 || S < 1 || H < 1 || max_ctx < 1 || D < 1 || rank < -1 || rank >= D ||
+      block_size < 1 || interleave < 1 || !std::isfinite(sm_scale) || !(sm_scale > 0.f))
+    return SMLA_ERR_INVALID_ARG;
+  if (H > SMLA_MAX_HEADS || D > SMLA_MAX_DCP) return SMLA_ERR_UNSUPPORTED;
+  if (int64_t(B) * S > INT32_MAX) return SMLA_ERR_INVALID_ARG;
+  const int32_t T = B * S;
+  if (T == 0) return SMLA_OK;
+  if (!q || !ctx_lens || !out || !lse || !kv_caches || !num_slots || !block_tables ||
+      !bt_row_strides || !bt_widths)
+    return SMLA_ERR_INVALID_ARG;
+  if (misaligned(q, 16) || misaligned(out, 16) || misaligned(lse, 4) || misaligned(ctx_lens, 4))
+    return SMLA_ERR_INVALID_ARG;
+  smla::DecodeArgs a{};
+  for (int d = 0; d < D; ++d) {
+    const bool used = rank < 0 || d == rank;
+    if (used && (!kv_caches[d] || misaligned(kv_caches[d], 16) || num_slots[d] < 0 ||
+                 !block_tables[d] || misaligned(block_tables[d], 4) || bt_widths[d] < 1 ||
+                 bt_row_strides[d] < bt_widths[d]))
+      return SMLA_ERR_INVALID_ARG;
+    a.pools[d] = used ? kv_caches[d] : nullptr;
+    a.pool_slots[d] = used ? num_slots[d] : 0;
+    a.bts[d] = used ? block_tables[d] : nullptr;
+    a.bt_stride[d] = used ? bt_row_strides[d] : 0;
+    a.bt_width[d] = used ? bt_widths[d] : 0;
+  }
+  const int32_t K = dense_entries(max_ctx, D, interleave, rank);
+  const size_t need = smla::decode_workspace_bytes(T, H, K);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
+                   misaligned(workspace, 256)))
+    return SMLA_ERR_WORKSPACE;
+  a.q = q;
+  a.T = T;
+  a.H = H;
+  a.K = K;
+  a.sm_scale = sm_scale;
+  a.out = out;
+  a.lse = lse;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.D = D;
+  a.block_size = block_size;
+  a.interleave = interleave;
+  a.num_reqs = B;
+  a.ctx_lens = ctx_lens;
+  a.S = S;
+  a.dense_rank = rank;
+  a.max_ctx = max_ctx;
+  return from_cuda(smla::launch_decode_dense(a, static_cast<cudaStream_t>(stream)));
+}
+
 smla_status smla_dcp_lse_merge(const uint16_t* const* outs,
                                const float* const* lses, int32_t D, int32_t T,
                                int32_t H, uint16_t* out, float* lse,

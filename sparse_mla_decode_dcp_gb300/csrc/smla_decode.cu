@@ -62,6 +62,11 @@ using namespace sm100;
 
 __device__ unsigned int g_decode_error;
 
+// What a row's raw entries are: local slots of one pool (per-shard decode),
+// global top-k positions over D pools (fused DCP step), or the positions of
+// the row's whole causal context (dense decode).
+enum : int { kModeSlots = 0, kModeTopk = 1, kModeDense = 2 };
+
 constexpr int kTileN = 64;        // keys per tile (MMA N of QK^T, K of PV)
 constexpr int kThreads = 384;     // 12 warps
 constexpr int kStages = 4;        // fp16 operand tiles in flight
@@ -261,11 +266,11 @@ constexpr int kCodePerPart = 8;
 constexpr int kRopePerPart = 2;
 
 // Cache row of entry `idx` of the compacted list.
-template <bool kFused>
+template <int kMode>
 __device__ __forceinline__ const uint8_t* row_ptr(const DecodeArgs& a, const Ctl* ctl,
                                                   const int* list, const uint8_t* shard,
                                                   int idx) {
-  const uint8_t* pool = kFused ? ctl->pool[shard[idx]] : a.kv;
+  const uint8_t* pool = kMode != kModeSlots ? ctl->pool[shard[idx]] : a.kv;
   return pool + int64_t(list[idx]) * SMLA_ROW_BYTES;
 }
 
@@ -347,7 +352,7 @@ static_assert(kPiecesPerLoader * kLoaders == kTileN * kPiecesPerRow, "loaders sh
 static_assert(kTileN * kRawStride <= (1 << 15) && SMLA_ROW_BYTES <= (1 << 10) && kTileN <= (1 << 7),
               "packed piece offsets fit their fields");
 
-template <bool kFused>
+template <int kMode>
 __device__ void loader_loop(const DecodeArgs& a, Ctl* ctl, uint8_t* sm, int n, int ntiles, int c,
                             int ld, volatile int* abort) {
   const int* list = reinterpret_cast<const int*>(sm + kOffList);
@@ -373,7 +378,7 @@ __device__ void loader_loop(const DecodeArgs& a, Ctl* ctl, uint8_t* sm, int n, i
     for (int k = 0; k < kPiecesPerLoader; ++k) {
       const uint32_t r = pk[k] >> 25;
       if (r < rows) {
-        const uint8_t* row = row_ptr<kFused>(a, ctl, list, list_shard, base + int(r));
+        const uint8_t* row = row_ptr<kMode>(a, ctl, list, list_shard, base + int(r));
         buf[k] = ldg_stream(row + ((pk[k] >> 15) & 1023u));
       }
     }
@@ -606,7 +611,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tb, uint32_t op, bool accumula
     mma_ts(tb + kOCol, tb + kPCol + 8 * k, v + uint64_t(k * (2048 >> 4)), idesc, accumulate || k > 0);
 }
 
-template <bool kFused>
+template <int kMode>
 __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt& hr, int64_t t,
                         int split, uint32_t peer) {
   const int C = hr.c;
@@ -896,7 +901,7 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
     convert_loop(ctl, sm, n, ntiles, d & (kTileN - 1), C, d >> 6, lane, abort);
   } else if (warp >= kLoaderWarp0) {
     // ------------------------------------------------ stage cache rows
-    loader_loop<kFused>(a, ctl, sm, n, ntiles, C, tid - 32 * kLoaderWarp0, abort);
+    loader_loop<kMode>(a, ctl, sm, n, ntiles, C, tid - 32 * kLoaderWarp0, abort);
   } else if (lane == 0) {
     // ------------------------------------------------ QK^T issue (one thread)
     // QK(i) needs its operand stage converted and S(i - 1) read by the
@@ -925,19 +930,21 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
 }
 
 // Resolve raw entry v to (slot, shard).  Per-shard launch: the entry
-// already is a local slot.  Fused DCP step: the entry is a global position
-// v; with interleave size I, runs of I positions go to the shards in turn,
-// so v is owned by shard (v div I) mod D at local position
-// (v div (I D)) I + v mod I (I = 1: shard v mod D, position v div D), then
-// mapped through that shard's block-table row for this request (staged in
-// shared memory at `bt` when it fits, else read from global memory).
-// Returns false for -1 / foreign / invalid entries, recording input errors
-// in `err`.
-template <bool kFused>
+// already is a local slot.  Fused DCP step and merged dense decode: the
+// entry is a global position v; with interleave size I, runs of I positions
+// go to the shards in turn, so v is owned by shard (v div I) mod D at local
+// position (v div (I D)) I + v mod I (I = 1: shard v mod D, position
+// v div D).  Dense decode of one rank: the entry is that rank's local
+// position itself.  The local position then goes through that shard's
+// block-table row for this request (staged in shared memory at `bt` when it
+// fits, else read from global memory).  `limit` bounds the valid entries of
+// a dense row (its last position + 1, or the rank's count of them).  Returns
+// false for -1 / foreign / invalid entries, recording input errors in `err`.
+template <int kMode>
 __device__ __forceinline__ bool resolve_entry(const DecodeArgs& a, const Ctl* ctl, const int32_t* bt,
-                                              bool req_ok, int32_t v, int32_t& slot, int& shard,
-                                              unsigned& err) {
-  if (!kFused) {
+                                              bool req_ok, int32_t limit, int32_t v, int32_t& slot,
+                                              int& shard, unsigned& err) {
+  if (kMode == kModeSlots) {
     if (v >= a.num_slots) {
       err |= SMLA_DEVERR_SLOT_RANGE;
       return false;
@@ -947,10 +954,18 @@ __device__ __forceinline__ bool resolve_entry(const DecodeArgs& a, const Ctl* ct
     return v >= 0;
   }
   if (v < 0 || !req_ok) return false;
-  const uint32_t g = fastdiv(uint32_t(v), a.div_I);  // run of I positions
-  const uint32_t round = fastdiv(g, a.div_D);        // round of D runs
-  const int d = int(g - round * uint32_t(a.D));
-  const int32_t lp = int32_t(round) * a.interleave + (v - int32_t(g) * a.interleave);
+  if (kMode == kModeDense && v >= limit) return false;
+  int d;
+  int32_t lp;
+  if (kMode == kModeDense && a.dense_rank >= 0) {
+    d = a.dense_rank;
+    lp = v;
+  } else {
+    const uint32_t g = fastdiv(uint32_t(v), a.div_I);  // run of I positions
+    const uint32_t round = fastdiv(g, a.div_D);        // round of D runs
+    d = int(g - round * uint32_t(a.D));
+    lp = int32_t(round) * a.interleave + (v - int32_t(g) * a.interleave);
+  }
   const int32_t col = int32_t(fastdiv(uint32_t(lp), a.div_bs));
   if (col >= ctl->bt_width[d]) {
     err |= SMLA_DEVERR_BLOCK_TABLE;
@@ -971,9 +986,36 @@ __device__ __forceinline__ bool resolve_entry(const DecodeArgs& a, const Ctl* ct
   return true;
 }
 
-template <bool kFused>
+// Dense decode: the request of row t and the bound on its raw entries (its
+// own position + 1 in the merged form, that many positions' share of one
+// rank in the per-rank form); false for every row of a request (and an error
+// bit) when the request's context is shorter than its query tokens or runs
+// past the raw range.
+__device__ __forceinline__ bool dense_row(const DecodeArgs& a, int64_t t, int32_t& req,
+                                          int32_t& limit, unsigned& err) {
+  req = int32_t(t / a.S);
+  const int32_t ctx = a.ctx_lens[req];
+  if (ctx < a.S || ctx > a.max_ctx) {  // the request's query tokens are part of its context
+    err |= SMLA_DEVERR_CONTEXT;
+    limit = 0;
+    return false;
+  }
+  const int32_t n = ctx - a.S + int32_t(t - int64_t(req) * a.S) + 1;  // positions 0..n-1
+  if (a.dense_rank < 0) {
+    limit = n;
+  } else {
+    // whole rounds of I*D positions give I each, then the partial round
+    const int32_t ID = a.interleave * a.D;
+    const int32_t full = n / ID, rem = n - full * ID;
+    limit = full * a.interleave + min(max(rem - a.dense_rank * a.interleave, 0), a.interleave);
+  }
+  return true;
+}
+
+template <int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     sparse_mla_decode_kernel(const __grid_constant__ DecodeArgs a) {
+  constexpr bool kPools = kMode != kModeSlots;  // entries resolve through D pools
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1020,16 +1062,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // q lands in the (still idle) operand stages while the CTA sets up
     issue_q_tma(a, t, hr.c, smem_u32(sm + kOffOp), &ctl->q_tma);
   }
-  if (kFused && tid < a.D) {
+  if (kPools && tid < a.D) {
     // per-shard pointers of this row's request, read once
-    const int32_t r = a.req_id[t];
+    const int32_t r = kMode == kModeDense ? int32_t(t / a.S) : a.req_id[t];
     const bool ok = r >= 0 && r < a.num_reqs;
     ctl->pool[tid] = a.pools[tid];
     ctl->bt_row[tid] = a.bts[tid] + (ok ? int64_t(r) * a.bt_stride[tid] : 0);
     ctl->pool_slots[tid] = a.pool_slots[tid];
     ctl->bt_width[tid] = a.bt_width[tid];
   }
-  if (kFused && tid == 0) {
+  if (kPools && tid == 0) {
     // the request's block-table rows of all shards, staged in the exchange
     // buffers (idle until the tile loop) when they fit
     int off = 0;
@@ -1062,19 +1104,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     constexpr int kPer = kMaxList / 128;
     unsigned err = 0;
     bool req_ok = true;
-    if (kFused) {
+    int32_t limit = 0;
+    if (kMode == kModeTopk) {
       const int32_t r = a.req_id[t];
       req_ok = r >= 0 && r < a.num_reqs;
       if (!req_ok && d == 0) err |= SMLA_DEVERR_REQ_ID;
+    } else if (kMode == kModeDense) {
+      int32_t r;
+      unsigned e2 = 0;
+      req_ok = dense_row(a, t, r, limit, e2);
+      if (d == 0) err |= e2;
     }
     // 1) this thread's 16 raw entries, all loads in flight at once (four
-    //    16-byte loads when the row allows), and, for the fused step, the
-    //    request's block-table rows copied into shared memory by all 128
-    //    threads; one memory round trip for both
+    //    16-byte loads when the row allows; a dense row's entries are just
+    //    their indices), and, with D pools, the request's block-table rows
+    //    copied into shared memory by all 128 threads; one memory round trip
+    //    for both
     const int j0 = e_begin + d * kPer;
-    const int32_t* src = (kFused ? a.topk : a.slots) + t * a.K;
+    const int32_t* src = (kMode == kModeTopk ? a.topk : a.slots) + t * a.K;
     int32_t vs[kPer];
-    if (j0 + kPer <= e_end && (reinterpret_cast<uintptr_t>(src + j0) & 15u) == 0) {
+    if (kMode == kModeDense) {
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) vs[k] = j0 + k;
+    } else if (j0 + kPer <= e_end && (reinterpret_cast<uintptr_t>(src + j0) & 15u) == 0) {
 #pragma unroll
       for (int q4 = 0; q4 < kPer / 4; ++q4) {
         const int4 w = __ldg(reinterpret_cast<const int4*>(src + j0) + q4);
@@ -1088,7 +1140,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int k = 0; k < kPer; ++k) vs[k] = (j0 + k < e_end) ? __ldg(src + j0 + k) : -1;
     }
     int32_t* bt = reinterpret_cast<int32_t*>(sm + kOffX);
-    if (kFused && ctl->bt_staged) {
+    if (kPools && ctl->bt_staged) {
       const uint32_t bt0 = smem_u32(bt);
 #pragma unroll 1
       for (int sd = 0; sd < a.D; ++sd) {
@@ -1108,7 +1160,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int32_t v = vs[k];
       vs[k] = -1;
       shards[k] = 0;
-      if (j0 + k < e_end && resolve_entry<kFused>(a, ctl, bt, req_ok, v, vs[k], shards[k], err))
+      if (j0 + k < e_end && resolve_entry<kMode>(a, ctl, bt, req_ok, limit, v, vs[k], shards[k], err))
         keep |= 1u << k;
     }
     const int cnt = __popc(keep);
@@ -1144,7 +1196,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();  // peer barriers initialised before any remote arrive
   tc_fence_after();
 
-  run_cta<kFused>(a, sm, ctl, hr, t, split, peer);
+  run_cta<kMode>(a, sm, ctl, hr, t, split, peer);
 
   tc_fence_before();
   __syncthreads();
@@ -1239,7 +1291,7 @@ cudaError_t encode_q_maps(DecodeArgs& a) {
 // safe when several host threads make their first launch at once.
 constexpr int kMaxDevices = 64;
 
-template <bool kFused>
+template <int kMode>
 cudaError_t ensure_smem_attribute(int dev) {
   static std::atomic<bool> done[kMaxDevices];
   static std::mutex m;
@@ -1247,13 +1299,13 @@ cudaError_t ensure_smem_attribute(int dev) {
   if (tracked && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
   std::lock_guard<std::mutex> lock(m);
   if (tracked && done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(sparse_mla_decode_kernel<kFused>,
+  const cudaError_t e = cudaFuncSetAttribute(sparse_mla_decode_kernel<kMode>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e == cudaSuccess && tracked) done[dev].store(true, std::memory_order_release);
   return e;
 }
 
-template <bool kFused>
+template <int kMode>
 cudaError_t launch_impl(const DecodeArgs& args, cudaStream_t s) {
   DecodeArgs a = args;
   {
@@ -1269,23 +1321,33 @@ cudaError_t launch_impl(const DecodeArgs& args, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  e = ensure_smem_attribute<kFused>(dev);
+  e = ensure_smem_attribute<kMode>(dev);
   if (e != cudaSuccess) return e;
   const int64_t ctas = 2 * int64_t(a.T) * a.splits;
-  sparse_mla_decode_kernel<kFused><<<dim3(unsigned(ctas)), dim3(kThreads), kSmemBytes, s>>>(a);
+  sparse_mla_decode_kernel<kMode><<<dim3(unsigned(ctas)), dim3(kThreads), kSmemBytes, s>>>(a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) { return launch_impl<false>(a, s); }
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
+  return launch_impl<kModeSlots>(a, s);
+}
 
 cudaError_t launch_decode_fused(const DecodeArgs& args, cudaStream_t s) {
   DecodeArgs a = args;
   a.div_I = make_fastdiv(uint32_t(a.interleave));
   a.div_D = make_fastdiv(uint32_t(a.D));
   a.div_bs = make_fastdiv(uint32_t(a.block_size));
-  return launch_impl<true>(a, s);
+  return launch_impl<kModeTopk>(a, s);
+}
+
+cudaError_t launch_decode_dense(const DecodeArgs& args, cudaStream_t s) {
+  DecodeArgs a = args;
+  a.div_I = make_fastdiv(uint32_t(a.interleave));
+  a.div_D = make_fastdiv(uint32_t(a.D));
+  a.div_bs = make_fastdiv(uint32_t(a.block_size));
+  return launch_impl<kModeDense>(a, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -1337,7 +1399,7 @@ cudaError_t launch_decode_noalloc(const DecodeArgs& args, cudaStream_t s) {
     a.workspace = scratch;
     a.workspace_bytes = w.total;
   }
-  return launch_impl<false>(a, s);
+  return launch_impl<kModeSlots>(a, s);
 }
 
 cudaError_t decode_error_word(uint32_t* flags, bool clear) {

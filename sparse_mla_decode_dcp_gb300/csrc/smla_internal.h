@@ -68,7 +68,12 @@ struct DecodeArgs {
   // Fused DCP step only (D > 0): global top-k ids are converted per shard in
   // the kernel prologue and all shards' keys share one softmax.
   int32_t D, block_size, num_reqs, interleave;
-  FastDiv div_I, div_D, div_bs;  // set by the fused launcher
+  FastDiv div_I, div_D, div_bs;  // set by the fused and dense launchers
+  // Dense decode only: row t belongs to request t / S, whose context length
+  // is ctx_lens[t / S]; raw entries are positions (dense_rank < 0, all D
+  // pools) or dense_rank's local positions; max_ctx bounds the positions.
+  const int32_t* ctx_lens;
+  int32_t S, dense_rank, max_ctx;
   // q [T*H, 576] bf16 for TMA, set by the launcher: boxes of 64 dims x 128
   // head rows (128-byte swizzle) and 32 dims x 128 head rows (64-byte swizzle)
   CUtensorMap q_lat, q_rope;
@@ -92,6 +97,7 @@ struct MergeArgs {
 cudaError_t launch_filter_convert(const IndexArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_dense(const DecodeArgs& a, cudaStream_t s);
 // Library-owned split-K scratch (no allocation by anyone at call time).
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 cudaError_t launch_decode_noalloc(const DecodeArgs& a, cudaStream_t s);

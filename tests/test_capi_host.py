@@ -32,7 +32,8 @@ def test_header_declares_the_three_path_calls():
     names = _declared_functions()
     for n in ("smla_dcp_filter_convert_index", "smla_sparse_mla_decode",
               "smla_dcp_lse_merge", "smla_decode_workspace_size",
-              "smla_dcp_sparse_mla_decode_fused",
+              "smla_dcp_sparse_mla_decode_fused", "smla_dcp_dense_mla_decode",
+              "smla_dense_decode_workspace_size",
               "smla_status_string", "smla_get_device_error"):
         assert n in names
 
@@ -226,3 +227,53 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(capi, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         capi.load()
+
+
+def _dense(lib, D=2, **kw):
+    a = dict(q=FAKE, B=2, S=1, H=16, scale=0.07, ctx=FAKE, maxc=100, rank=-1, bs=16, I=1,
+             pools=[FAKE] * D, nslots=[100] * D, bts=[FAKE] * D, strides=[4] * D,
+             widths=[4] * D, out=FAKE, lse=FAKE, ws=None, wsb=0)
+    a.update(kw)
+    n = max(D, 1)
+    arr = lambda typ, xs: (typ * n)(*(list(xs) + [0] * (n - len(xs)))[:n])
+    return lib.smla_dcp_dense_mla_decode(
+        a["q"], a["B"], a["S"], a["H"], ctypes.c_float(a["scale"]), a["ctx"], a["maxc"], D,
+        a["rank"], a["bs"], a["I"], arr(ctypes.c_void_p, a["pools"]),
+        arr(ctypes.c_int64, a["nslots"]), arr(ctypes.c_void_p, a["bts"]),
+        arr(ctypes.c_int64, a["strides"]), arr(ctypes.c_int32, a["widths"]), a["out"], a["lse"],
+        a["ws"], a["wsb"], None)
+
+
+@pytest.mark.parametrize("D,kw,status", [
+    (0, {}, capi.SMLA_ERR_INVALID_ARG),
+    (17, {}, capi.SMLA_ERR_UNSUPPORTED),
+    (2, dict(H=129), capi.SMLA_ERR_UNSUPPORTED),
+    (2, dict(B=-1), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(S=0), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(maxc=0), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(rank=2), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(rank=-2), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(bs=0), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(I=0), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(scale=float("inf")), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(ctx=None), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(q=FAKE + 8), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(pools=[FAKE, None]), capi.SMLA_ERR_INVALID_ARG),
+    # rank >= 0 reads only its own pool and table: the others may be empty
+    # (the call passes every argument check and stops at the missing workspace)
+    (2, dict(rank=0, maxc=65536, pools=[FAKE, None], bts=[FAKE, None], widths=[4, 0]),
+     capi.SMLA_ERR_WORKSPACE),
+    (2, dict(rank=1, pools=[FAKE, None]), capi.SMLA_ERR_INVALID_ARG),
+    (2, dict(B=0, q=None, ctx=None, out=None, lse=None), capi.SMLA_OK),
+])
+def test_dense_argument_checks(lib, D, kw, status):
+    assert _dense(lib, D=D, **kw) == status
+
+
+def test_dense_workspace_size_is_a_function_of_the_shape(lib):
+    assert capi.dense_decode_workspace_size(2, 16, 0, 2) == 0
+    assert capi.dense_decode_workspace_size(2, 16, 100, 2, 1, 2) == 0
+    big = capi.dense_decode_workspace_size(8, 128, 65536, 4, 1, -1)
+    one = capi.dense_decode_workspace_size(8, 128, 65536, 4, 1, 0)
+    assert big > one > 0  # one rank holds a quarter of the positions
+    assert big == capi.decode_workspace_size(8, 128, 65536)

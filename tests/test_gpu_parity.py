@@ -631,3 +631,91 @@ def test_decode_forced_rescale_large_values(cuda_device):
     o = out.float().cpu().numpy().astype(np.float64)
     assert np.linalg.norm(o - ref_out) / np.linalg.norm(ref_out) < 1e-2
     _p_rounding_bound_check(out, ref_out, ref_lse, q, pool, s)
+
+
+# ---------------------------------------------------------------- dense decode
+def _dense_case(dev, B, S, D, I, lo, hi, seed):
+    spec = inputs.WorkloadSpec(
+        name=f"dense_{B}x{S}_D{D}_I{I}", num_reqs=B, tokens_per_req=S, heads=128, topk=64,
+        dcp=D, block_size=64, ctx_kind="uniform", ctx_lo=lo, ctx_hi=hi, interleave=I)
+    wl = inputs.make_workload(spec, seed=seed, device=dev)
+    pools = [s.pool for s in wl.shards]
+    bts = [torch.from_numpy(s.block_table).to(dev) for s in wl.shards]
+    ctx = torch.from_numpy(wl.ctx.astype(np.int32)).to(dev)
+    return wl, pools, bts, ctx, int(wl.ctx.max())
+
+
+@pytest.mark.parametrize("D,S,I", [(1, 1, 1), (2, 1, 1), (2, 2, 1), (4, 1, 1), (4, 2, 1),
+                                   (2, 2, 2), (4, 1, 4)])
+def test_dense_decode_matches_oracle(cuda_device, D, S, I):
+    """Every cached position of each request's causal context: one rank's
+    partial (rank = d) against the oracle's dense decode of that rank, and the
+    merged result (rank = -1, one launch over all pools) against the oracle's
+    LSE merge of the ranks' partials; rows in token order b*S + s, i.e. the
+    [batch, heads, seq_len] -> [tokens, heads] flattening of the LSE."""
+    dev = cuda_device
+    wl, pools, bts, ctx, max_ctx = _dense_case(dev, 5, S, D, I, 1, 4096, seed=10 * D + S + I)
+    spec = wl.spec
+    q_bits = _q_bits(wl.q)
+    capi.get_device_error(clear=True)
+    refs_o, refs_l = [], []
+    for d in range(D):
+        o, l = capi.dcp_dense_mla_decode(wl.q, ctx, max_ctx, S, pools, bts, spec.block_size,
+                                         spec.sm_scale, rank=d, interleave=I)
+        torch.cuda.synchronize()
+        ro, rl = oracle.dense_mla_decode(q_bits, wl.shards[d].pool.cpu().numpy(),
+                                         wl.shards[d].block_table, wl.ctx, S, D, d,
+                                         spec.block_size, spec.sm_scale, I)
+        compare_out_lse(o, l, ro, rl, where=f"dense rank {d}")
+        refs_o.append(ro)
+        refs_l.append(rl)
+    ref_out, ref_lse = oracle.lse_merge(refs_o, refs_l)
+    out, lse = capi.dcp_dense_mla_decode(wl.q, ctx, max_ctx, S, pools, bts, spec.block_size,
+                                         spec.sm_scale, rank=-1, interleave=I)
+    torch.cuda.synchronize()
+    assert capi.get_device_error(clear=True) == 0
+    compare_out_lse(out, lse, ref_out, ref_lse, where=f"dense merged D={D} S={S} I={I}")
+    # the flattening: [B, H, S] read back in token order equals the kernel's rows
+    B, H = len(wl.ctx), spec.heads
+    lse_bhs = lse.cpu().numpy().reshape(B, S, H).transpose(0, 2, 1)
+    assert np.array_equal(oracle.flatten_lse_bhs(lse_bhs), lse.cpu().numpy())
+
+
+def test_dense_decode_split_k_long_contexts(cuda_device):
+    """Enough rows that the split count is set by the 2048-key list limit and
+    contexts above it: several splits per row, combined in-kernel."""
+    dev = cuda_device
+    wl, pools, bts, ctx, max_ctx = _dense_case(dev, 40, 2, 2, 1, 2500, 4096, seed=77)
+    spec = wl.spec
+    assert capi.dense_decode_workspace_size(80, 128, max_ctx, 2, 1, -1) > 0
+    out, lse = capi.dcp_dense_mla_decode(wl.q, ctx, max_ctx, 2, pools, bts, spec.block_size,
+                                         spec.sm_scale)
+    torch.cuda.synchronize()
+    q_bits = _q_bits(wl.q)
+    refs = [oracle.dense_mla_decode(q_bits, wl.shards[d].pool.cpu().numpy(),
+                                    wl.shards[d].block_table, wl.ctx, 2, 2, d, spec.block_size,
+                                    spec.sm_scale) for d in range(2)]
+    ref_out, ref_lse = oracle.lse_merge([r[0] for r in refs], [r[1] for r in refs])
+    compare_out_lse(out, lse, ref_out, ref_lse, where="dense split-K")
+
+
+def test_dense_decode_context_out_of_range_is_flagged(cuda_device):
+    """A context shorter than its request's query tokens (or past max_ctx) is
+    an input error: those rows come out as (0, -inf) and the device error
+    word says so; the other rows are unaffected."""
+    dev = cuda_device
+    wl, pools, bts, ctx, max_ctx = _dense_case(dev, 3, 2, 2, 1, 100, 600, seed=5)
+    spec = wl.spec
+    good_out, good_lse = capi.dcp_dense_mla_decode(wl.q, ctx, max_ctx, 2, pools, bts,
+                                                   spec.block_size, spec.sm_scale)
+    torch.cuda.synchronize()
+    bad = ctx.clone()
+    bad[1] = 1  # request 1 has 2 query tokens but a context of 1
+    capi.get_device_error(clear=True)
+    out, lse = capi.dcp_dense_mla_decode(wl.q, bad, max_ctx, 2, pools, bts, spec.block_size,
+                                         spec.sm_scale)
+    torch.cuda.synchronize()
+    assert capi.get_device_error(clear=True) & capi.DEVERR_CONTEXT
+    assert torch.isneginf(lse[2:4]).all() and torch.all(out[2:4].view(torch.int16) == 0)
+    keep = torch.tensor([0, 1, 4, 5], device=dev)
+    assert torch.equal(out[keep], good_out[keep]) and torch.equal(lse[keep], good_lse[keep])
