@@ -21,6 +21,11 @@
  *
  *   smla_dcp_dense_mla_decode         per rank or merged over D pools
  *
+ * and the step before the path, the global top-k of indexer scores:
+ *
+ *   smla_topk_select                  per row (per rank: as global ids)
+ *   smla_dcp_topk_merge               top-k of the ranks' candidates
+ *
  * Sources (page title, then section):
  *   [P1] "[eldritch] attention: support DCP in SM120 FlashInfer sparse MLA"
  *   [P2] "[Bugfix][Attention] Stabilize sparse-MLA DCP for GLM PCP evals"
@@ -297,6 +302,43 @@ smla_status smla_dcp_dense_mla_decode(
     const int64_t* num_slots, const int32_t* const* block_tables,
     const int64_t* bt_row_strides, const int32_t* bt_widths, uint16_t* out,
     float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Global top-k selection of indexer scores: the step that produces the
+ * path's global top-k ids ["[eldritch] ..." Summary: global sparse top-k
+ * token ids; P3 related PRs: the DCP sparse indexer's global top-k merge].
+ * The pages print no rule; the rule taken: keep the K largest scores, ranked
+ * by score descending and then token id ascending, -1 padded when a row has
+ * fewer than K candidates; NaN ranks below every number, -0 equals +0.
+ *
+ * smla_topk_select: row i's candidates are the local positions
+ * j < n_cand[i] (clipped to [0, L]) of rank `rank`, with scores
+ * scores[i*row_stride + j]; the ids written are their global positions:
+ * local position j of rank r is global position (j div I)*I*D + r*I +
+ * j mod I, the inverse of smla_dcp_filter_convert_index's rule (D = 1,
+ * rank = 0: the plain top-k of positions 0..n-1).
+ *   scores      device fp32 [T, row_stride]
+ *   n_cand      device int32 [T]
+ *   out_ids     device int32 [T, K] output
+ *   out_scores  device fp32 [T, K] output (the kept scores) or NULL
+ *
+ * smla_dcp_topk_merge: row i's candidates are the entries j < M with
+ * cand_ids[i*row_stride + j] >= 0 (global ids, unique per row) and their
+ * cand_scores; writes the top K of the union by the same rule -- with each
+ * rank's smla_topk_select output concatenated, exactly the unsharded top-k.
+ *
+ * Errors: INVALID_ARG for null pointers (T > 0), T < 0, L < 0, M < 0,
+ * row_stride < L (or < M), D < 1, rank outside [0, D), interleave < 1,
+ * misaligned buffers; UNSUPPORTED for K outside [1, SMLA_MAX_TOPK].
+ */
+#define SMLA_MAX_TOPK 16384
+smla_status smla_topk_select(const float* scores, int64_t row_stride, int32_t L,
+                             const int32_t* n_cand, int32_t T, int32_t K, int32_t D,
+                             int32_t rank, int32_t interleave, int32_t* out_ids,
+                             float* out_scores, void* stream);
+smla_status smla_dcp_topk_merge(const int32_t* cand_ids, const float* cand_scores,
+                                int64_t row_stride, int32_t M, int32_t T, int32_t K,
+                                int32_t* out_ids, float* out_scores, void* stream);
 
 /*
  * Step 3 -- LSE-weighted merge of D partials [P1 Why, Scope / Limitations

@@ -58,6 +58,11 @@ SIGNATURES = {
     "smla_dcp_dense_mla_decode": (ctypes.c_int, [
         _c_vp, _c_i32, _c_i32, _c_i32, ctypes.c_float, _c_vp, _c_i32, _c_i32, _c_i32, _c_i32,
         _c_i32, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]),
+    "smla_topk_select": (ctypes.c_int, [
+        _c_vp, _c_i64, _c_i32, _c_vp, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_vp, _c_vp,
+        _c_vp]),
+    "smla_dcp_topk_merge": (ctypes.c_int, [
+        _c_vp, _c_vp, _c_i64, _c_i32, _c_i32, _c_i32, _c_vp, _c_vp, _c_vp]),
     "smla_dcp_lse_merge": (ctypes.c_int, [
         _c_vp, _c_vp, _c_i32, _c_i32, _c_i32, _c_vp, _c_vp, _c_vp]),
 }
@@ -354,6 +359,48 @@ def dcp_dense_mla_decode(q: torch.Tensor, ctx_lens: torch.Tensor, max_ctx: int, 
         lse.data_ptr(), ws_ptr, ws_bytes, _stream_ptr(stream, dev))
     _check("smla_dcp_dense_mla_decode", st)
     return out, lse
+
+
+MAX_TOPK = 16384
+
+
+def topk_select(scores: torch.Tensor, n_cand: torch.Tensor, K: int, *, D: int = 1, rank: int = 0,
+                interleave: int = 1, with_scores: bool = False,
+                stream: Optional[torch.cuda.Stream] = None):
+    """Top-K of each row's first n_cand local positions of `rank` (score
+    descending, id ascending), as global ids, -1 padded.  scores is
+    [T, L] fp32 with contiguous rows."""
+    dev = scores.device
+    if scores.dtype != torch.float32 or scores.dim() != 2 or scores.stride(1) != 1:
+        raise ValueError("scores must be a 2-D fp32 tensor with contiguous rows")
+    _need(n_cand, "n_cand", torch.int32, dev)
+    T, L = scores.shape
+    ids = torch.empty((T, K), dtype=torch.int32, device=dev)
+    sc = torch.empty((T, K), dtype=torch.float32, device=dev) if with_scores else None
+    st = load().smla_topk_select(scores.data_ptr(), scores.stride(0), L, n_cand.data_ptr(), T, K,
+                                 D, rank, interleave, ids.data_ptr(),
+                                 sc.data_ptr() if sc is not None else None,
+                                 _stream_ptr(stream, dev))
+    _check("smla_topk_select", st)
+    return (ids, sc) if with_scores else ids
+
+
+def dcp_topk_merge(cand_ids: torch.Tensor, cand_scores: torch.Tensor, K: int, *,
+                   with_scores: bool = False, stream: Optional[torch.cuda.Stream] = None):
+    """Top-K of each row's candidates (ids >= 0) by the same rule."""
+    dev = cand_ids.device
+    _need(cand_ids, "cand_ids", torch.int32, dev)
+    _need(cand_scores, "cand_scores", torch.float32, dev)
+    if cand_ids.shape != cand_scores.shape or cand_ids.dim() != 2:
+        raise ValueError("cand_ids and cand_scores must be [T, M]")
+    T, M = cand_ids.shape
+    ids = torch.empty((T, K), dtype=torch.int32, device=dev)
+    sc = torch.empty((T, K), dtype=torch.float32, device=dev) if with_scores else None
+    st = load().smla_dcp_topk_merge(cand_ids.data_ptr(), cand_scores.data_ptr(), M, M, T, K,
+                                    ids.data_ptr(), sc.data_ptr() if sc is not None else None,
+                                    _stream_ptr(stream, dev))
+    _check("smla_dcp_topk_merge", st)
+    return (ids, sc) if with_scores else ids
 
 
 def dcp_lse_merge(outs: Sequence[torch.Tensor], lses: Sequence[torch.Tensor], *,

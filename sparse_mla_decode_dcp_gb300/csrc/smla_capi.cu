@@ -270,6 +270,57 @@ smla_status smla_dcp_dense_mla_decode(
   return from_cuda(smla::launch_decode_dense(a, static_cast<cudaStream_t>(stream)));
 }
 
+smla_status smla_topk_select(const float* scores, int64_t row_stride, int32_t L,
+                             const int32_t* n_cand, int32_t T, int32_t K, int32_t D,
+                             int32_t rank, int32_t interleave, int32_t* out_ids,
+                             float* out_scores, void* stream) {
+  if (T < 0 || L < 0 || row_stride < L || D < 1 || rank < 0 || rank >= D || interleave < 1)
+    return SMLA_ERR_INVALID_ARG;
+  if (K < 1 || K > SMLA_MAX_TOPK) return SMLA_ERR_UNSUPPORTED;
+  if (T == 0) return SMLA_OK;
+  if (!scores || !n_cand || !out_ids) return SMLA_ERR_INVALID_ARG;
+  if (misaligned(scores, 4) || misaligned(n_cand, 4) || misaligned(out_ids, 4) ||
+      (out_scores && misaligned(out_scores, 4)))
+    return SMLA_ERR_INVALID_ARG;
+  smla::TopkArgs a{};
+  a.scores = scores;
+  a.n_cand = n_cand;
+  a.row_stride = row_stride;
+  a.L = L;
+  a.T = T;
+  a.K = K;
+  a.D = D;
+  a.rank = rank;
+  a.interleave = interleave;
+  a.out_ids = out_ids;
+  a.out_scores = out_scores;
+  return from_cuda(smla::launch_topk_select(a, static_cast<cudaStream_t>(stream)));
+}
+
+smla_status smla_dcp_topk_merge(const int32_t* cand_ids, const float* cand_scores,
+                                int64_t row_stride, int32_t M, int32_t T, int32_t K,
+                                int32_t* out_ids, float* out_scores, void* stream) {
+  if (T < 0 || M < 0 || row_stride < M) return SMLA_ERR_INVALID_ARG;
+  if (K < 1 || K > SMLA_MAX_TOPK) return SMLA_ERR_UNSUPPORTED;
+  if (T == 0) return SMLA_OK;
+  if (!cand_ids || !cand_scores || !out_ids) return SMLA_ERR_INVALID_ARG;
+  if (misaligned(cand_ids, 4) || misaligned(cand_scores, 4) || misaligned(out_ids, 4) ||
+      (out_scores && misaligned(out_scores, 4)))
+    return SMLA_ERR_INVALID_ARG;
+  smla::TopkArgs a{};
+  a.scores = cand_scores;
+  a.cand_ids = cand_ids;
+  a.row_stride = row_stride;
+  a.M = M;
+  a.T = T;
+  a.K = K;
+  a.D = 1;
+  a.interleave = 1;
+  a.out_ids = out_ids;
+  a.out_scores = out_scores;
+  return from_cuda(smla::launch_topk_merge(a, static_cast<cudaStream_t>(stream)));
+}
+
 smla_status smla_dcp_lse_merge(const uint16_t* const* outs,
                                const float* const* lses, int32_t D, int32_t T,
                                int32_t H, uint16_t* out, float* lse,

@@ -86,6 +86,18 @@ struct DecodeArgs {
   int32_t bt_width[kMaxMerge];
 };
 
+struct TopkArgs {
+  const float* scores;      // [T, row_stride]: select: by local position; merge: candidates
+  const int32_t* cand_ids;  // merge only: [T, row_stride] global ids, -1 = none
+  const int32_t* n_cand;    // select only: [T] candidates per row
+  int64_t row_stride;
+  int32_t L, M, T, K, kp;   // kp: the sort's size, a power of two >= K (set by the launcher)
+  int32_t D, rank, interleave;
+  FastDiv div_I;            // set by the launcher
+  int32_t* out_ids;         // [T, K]
+  float* out_scores;        // [T, K] or null
+};
+
 struct MergeArgs {
   const uint16_t* outs[kMaxMerge];
   const float* lses[kMaxMerge];
@@ -102,6 +114,8 @@ cudaError_t launch_decode_dense(const DecodeArgs& a, cudaStream_t s);
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 cudaError_t launch_decode_noalloc(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s);
+cudaError_t launch_topk_select(const TopkArgs& a, cudaStream_t s);
+cudaError_t launch_topk_merge(const TopkArgs& a, cudaStream_t s);
 size_t decode_workspace_bytes(int32_t T, int32_t H, int32_t K);
 
 // Each kernel translation unit owns one device error word.

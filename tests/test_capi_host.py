@@ -277,3 +277,51 @@ def test_dense_workspace_size_is_a_function_of_the_shape(lib):
     one = capi.dense_decode_workspace_size(8, 128, 65536, 4, 1, 0)
     assert big > one > 0  # one rank holds a quarter of the positions
     assert big == capi.decode_workspace_size(8, 128, 65536)
+
+
+def _topk_select(lib, **kw):
+    a = dict(scores=FAKE, stride=100, L=100, n=FAKE, T=2, K=16, D=1, rank=0, I=1, out=FAKE,
+             sc=None)
+    a.update(kw)
+    return lib.smla_topk_select(a["scores"], a["stride"], a["L"], a["n"], a["T"], a["K"], a["D"],
+                                a["rank"], a["I"], a["out"], a["sc"], None)
+
+
+def _topk_merge(lib, **kw):
+    a = dict(ids=FAKE, scores=FAKE, stride=64, M=64, T=2, K=16, out=FAKE, sc=None)
+    a.update(kw)
+    return lib.smla_dcp_topk_merge(a["ids"], a["scores"], a["stride"], a["M"], a["T"], a["K"],
+                                   a["out"], a["sc"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=-1), capi.SMLA_ERR_INVALID_ARG),
+    (dict(L=-1), capi.SMLA_ERR_INVALID_ARG),
+    (dict(stride=99), capi.SMLA_ERR_INVALID_ARG),
+    (dict(D=0), capi.SMLA_ERR_INVALID_ARG),
+    (dict(D=2, rank=2), capi.SMLA_ERR_INVALID_ARG),
+    (dict(I=0), capi.SMLA_ERR_INVALID_ARG),
+    (dict(K=0), capi.SMLA_ERR_UNSUPPORTED),
+    (dict(K=16385), capi.SMLA_ERR_UNSUPPORTED),
+    (dict(scores=None), capi.SMLA_ERR_INVALID_ARG),
+    (dict(n=None), capi.SMLA_ERR_INVALID_ARG),
+    (dict(out=None), capi.SMLA_ERR_INVALID_ARG),
+    (dict(out=FAKE + 2), capi.SMLA_ERR_INVALID_ARG),
+    (dict(T=0, scores=None, n=None, out=None), capi.SMLA_OK),
+])
+def test_topk_select_argument_checks(lib, kw, status):
+    assert _topk_select(lib, **kw) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=-1), capi.SMLA_ERR_INVALID_ARG),
+    (dict(M=-1), capi.SMLA_ERR_INVALID_ARG),
+    (dict(stride=63), capi.SMLA_ERR_INVALID_ARG),
+    (dict(K=0), capi.SMLA_ERR_UNSUPPORTED),
+    (dict(ids=None), capi.SMLA_ERR_INVALID_ARG),
+    (dict(scores=None), capi.SMLA_ERR_INVALID_ARG),
+    (dict(sc=FAKE + 1), capi.SMLA_ERR_INVALID_ARG),
+    (dict(T=0, ids=None, scores=None, out=None), capi.SMLA_OK),
+])
+def test_topk_merge_argument_checks(lib, kw, status):
+    assert _topk_merge(lib, **kw) == status

@@ -719,3 +719,76 @@ def test_dense_decode_context_out_of_range_is_flagged(cuda_device):
     assert torch.isneginf(lse[2:4]).all() and torch.all(out[2:4].view(torch.int16) == 0)
     keep = torch.tensor([0, 1, 4, 5], device=dev)
     assert torch.equal(out[keep], good_out[keep]) and torch.equal(lse[keep], good_lse[keep])
+
+
+# ------------------------------------------------------------ global top-k
+def _topk_vs_oracle(dev, scores64, n_cand, K, where):
+    s32 = np.asarray(scores64, dtype=np.float32)
+    got = capi.topk_select(torch.from_numpy(s32).to(dev),
+                           torch.from_numpy(np.asarray(n_cand, dtype=np.int32)).to(dev), K)
+    torch.cuda.synchronize()
+    want = oracle.topk_select(s32.astype(np.float64), n_cand, K)
+    assert np.array_equal(got.cpu().numpy(), want), where
+
+
+@pytest.mark.parametrize("L,K", [(97, 16), (5000, 2048), (131072, 2048), (40000, 16384)])
+def test_topk_select_matches_oracle(cuda_device, L, K):
+    """Random rows up to 128k candidates, some shorter than K: bit-exact ids."""
+    rng = np.random.default_rng(L + K)
+    T = 6
+    scores = rng.standard_normal((T, L))
+    n_cand = rng.integers(0, L + 1, size=T)
+    n_cand[0], n_cand[1] = L, min(L, K // 2)  # full row, and fewer than K candidates
+    _topk_vs_oracle(cuda_device, scores, n_cand, K, f"L={L} K={K}")
+
+
+@pytest.mark.parametrize("decimals", [0, 1])
+def test_topk_select_heavy_ties(cuda_device, decimals):
+    """Scores rounded to few decimals: thousands of equal scores straddle the
+    K-th place, and the ids among them must be the smallest positions."""
+    rng = np.random.default_rng(50 + decimals)
+    scores = np.round(rng.standard_normal((5, 30000)), decimals)
+    _topk_vs_oracle(cuda_device, scores, np.full(5, 30000), 2048, f"ties {decimals}")
+    _topk_vs_oracle(cuda_device, np.zeros((2, 5000)), [5000, 100], 2048, "all equal")
+
+
+def test_topk_select_nan_and_signed_zero(cuda_device):
+    """NaN ranks below every number (-inf included) and -0 ties with +0."""
+    row = np.array([0.0, -0.0, np.nan, 1.5, -np.inf, np.nan, -0.0, 2.0, np.inf, -1.0], np.float64)
+    scores = np.stack([row, row[::-1].copy()])
+    for K in (1, 3, 6, 10, 12):
+        _topk_vs_oracle(cuda_device, scores, [10, 10], K, f"special K={K}")
+
+
+@pytest.mark.parametrize("D,I,decimals", [(2, 1, 6), (4, 1, 1), (4, 2, 6), (3, 64, 0)])
+def test_dcp_topk_local_then_merge_equals_unsharded(cuda_device, D, I, decimals):
+    """Per rank: the top-k of the positions it holds, as global ids (one
+    launch per rank over its local score array); then the merge of the ranks'
+    candidates: bit-exact equal to the oracle's unsharded top-k, and to the
+    oracle's merge of the same candidates."""
+    dev = cuda_device
+    rng = np.random.default_rng(D * 100 + I + decimals)
+    T, L, K = 4, 20000, 2048
+    scores = np.round(rng.standard_normal((T, L)), decimals).astype(np.float32)
+    n_cand = rng.integers(1, L + 1, size=T)
+    n_cand[0] = 1500  # fewer candidates than K
+    want = oracle.topk_select(scores.astype(np.float64), n_cand, K)
+    ids, scs = [], []
+    for r in range(D):
+        n_loc = np.array([oracle.dcp_local_seq_len(int(n), D, r, I) for n in n_cand], np.int32)
+        Lr = oracle.dcp_local_seq_len(L, D, r, I)
+        gl = np.array([(j // I) * I * D + r * I + j % I for j in range(Lr)])
+        local = np.ascontiguousarray(scores[:, gl])
+        i_r, s_r = capi.topk_select(torch.from_numpy(local).to(dev),
+                                    torch.from_numpy(n_loc).to(dev), K, D=D, rank=r,
+                                    interleave=I, with_scores=True)
+        ids.append(i_r)
+        scs.append(s_r)
+    cand_ids = torch.cat(ids, dim=1).contiguous()
+    cand_sc = torch.cat(scs, dim=1).contiguous()
+    got = capi.dcp_topk_merge(cand_ids, cand_sc, K)
+    torch.cuda.synchronize()
+    assert np.array_equal(got.cpu().numpy(), want)
+    ref = oracle.dcp_topk_merge([x.cpu().numpy() for x in ids],
+                                [x.cpu().numpy().astype(np.float64) for x in scs], K)
+    assert np.array_equal(got.cpu().numpy(), ref)

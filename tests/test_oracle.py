@@ -624,3 +624,23 @@ def test_flatten_lse_matches_torch_permute_reshape():
     x = torch.arange(2 * 3 * 4, dtype=torch.float64).reshape(2, 3, 4)  # [batch, heads, seq_len]
     want = x.permute(0, 2, 1).reshape(2 * 4, 3)
     assert np.array_equal(oracle.flatten_lse_bhs(x.numpy()), want.numpy())
+
+
+@pytest.mark.parametrize("D,I", [(1, 1), (2, 1), (3, 2), (4, 4)])
+def test_rank_local_position_to_global_id_is_the_inverse_conversion(D, I):
+    """The global id the per-rank top-k reports for local position j of rank
+    r, (j div I) I D + r I + j mod I, must be the position the conversion
+    rule sends to rank r's local position j."""
+    for r in range(D):
+        for j in range(200):
+            t = (j // I) * I * D + r * I + j % I
+            assert (t // I) % D == r
+            assert (t // (I * D)) * I + t % I == j
+    # and the oracle's conversion agrees on a one-block-per-position table
+    ctx = 300
+    for r in range(D):
+        n = oracle.dcp_local_seq_len(ctx, D, r, I)
+        bt = np.arange(n, dtype=np.int32)[None]  # block j holds local position j (bs = 1)
+        ids = np.array([[(j // I) * I * D + r * I + j % I for j in range(n)]], dtype=np.int32)
+        slots, cnt = oracle.dcp_filter_convert_index(np.array([0]), bt, ids, D, r, 1, I)
+        assert slots[0].tolist() == list(range(n)) and cnt[0] == n
