@@ -167,6 +167,55 @@ def profile_traffic(kernel: str, workload: str):
         return None
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def blas_threads():
+    """Threads the BLAS library numpy loaded will use (queried from the
+    library itself), or None when it cannot be asked."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    import ctypes
+    try:
+        with open("/proc/self/maps") as f:
+            libs = {line.split()[-1] for line in f if "openblas" in line.lower() and ".so" in line}
+    except OSError:
+        return None
+    for path in sorted(libs):
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for name in ("openblas_get_num_threads", "openblas_get_num_threads64_",
+                     "scipy_openblas_get_num_threads64_", "scipy_openblas_get_num_threads"):
+            fn = getattr(lib, name, None)
+            if fn is not None:
+                fn.restype = ctypes.c_int
+                return int(fn())
+    return None
+
+
 def cpu_baseline(wl, sample_tokens: int, min_seconds: float = 10.0, max_passes: int = 200):
     """The float64 oracle as it stands, timed on this host on a bounded sample
     of the same workload: the first `sample_tokens` query rows, every shard's
@@ -184,7 +233,8 @@ def cpu_baseline(wl, sample_tokens: int, min_seconds: float = 10.0, max_passes: 
         outs, lses = [], []
         for d, s in enumerate(wl.shards):
             sl, _ = oracle.dcp_filter_convert_index(wl.req_id[:n], s.block_table, wl.topk[:n],
-                                                    wl.D, d, wl.spec.block_size)
+                                                    wl.D, d, wl.spec.block_size,
+                                                    wl.spec.interleave)
             o, l = oracle.sparse_mla_decode(q_bits, pools[d], sl, wl.spec.sm_scale)
             outs.append(o)
             lses.append(l)
@@ -193,11 +243,43 @@ def cpu_baseline(wl, sample_tokens: int, min_seconds: float = 10.0, max_passes: 
         dt = time.perf_counter() - t0
         if dt >= min_seconds or passes >= max_passes:
             break
-    cores = int(os.environ.get("OMP_NUM_THREADS", os.environ.get("OPENBLAS_NUM_THREADS",
-                                                                  os.cpu_count() or 1)))
-    return {"value": passes * n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+    threads = blas_threads()
+    return {"value": passes * n / dt, "unit": UNIT,
+            "cores": threads if threads is not None else (os.cpu_count() or 1),
+            "kind": "oracle", "host_cores": os.cpu_count(), "blas_threads": threads,
+            "cpu_model": cpu_model(),
             "sample": f"first {n} of {wl.T} query rows of {wl.spec.name}, all {wl.D} shards "
                       f"(convert + decode) + merge, float64 numpy, {passes} passes; {dt:.2f} s"}
+
+
+def cpu_baseline_single_thread(workload: str, seed: int, sample_tokens: int = 2,
+                               min_seconds: float = 8.0):
+    """The same oracle timing in a process of its own whose BLAS may use one
+    thread only (OMP/OpenBLAS/MKL thread counts set to 1 before numpy loads).
+    The child builds the workload on the CPU: the structure (contexts, top-k
+    ids, block tables) comes from the same seeded draws, the values from the
+    CPU generator -- the oracle's cost does not depend on them."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json, bench\n"
+            "from sparse_mla_decode_dcp_gb300 import inputs\n"
+            f"wl = inputs.make_workload({workload!r}, seed={seed}, device='cpu')\n"
+            f"print(json.dumps(bench.cpu_baseline(wl, {sample_tokens}, {min_seconds})))\n")
+    try:
+        p = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
+                           text=True, timeout=600)
+        return json.loads(p.stdout.strip().splitlines()[-1])
+    except (OSError, subprocess.SubprocessError, ValueError, IndexError) as e:
+        return {"unavailable": f"single-thread oracle run failed: {type(e).__name__}"}
+
+
+def workload_config(wl, args, world: int) -> dict:
+    """The `config` object both arms print for the same workload."""
+    return {"workload": args.workload, "path": args.path, "T": wl.T, "H": wl.H, "K": wl.K,
+            "D": wl.D, "interleave": wl.spec.interleave, "block_size": wl.spec.block_size,
+            "requests": wl.spec.num_reqs, "cached_tokens": int(sum(int(c) for c in wl.ctx)),
+            "l2": "flushed before every step (256 MiB write, outside the events)",
+            "parallelism": f"replicas x{world}" if world > 1 else
+                           "single GPU, D shards simulated as D pools"}
 
 
 # ------------------------------------------------------------ multi-rank
@@ -311,6 +393,62 @@ def _roofline(kernel, launch_ms, keys_per_launch, H, peaks, workload):
     return roof
 
 
+def _dense_path(step, wl, n, flush, stream, peaks, workload):
+    """The dense decode (every cached position of each row's causal context,
+    merged over the D pools in one launch) on the same caches."""
+    import torch
+
+    from sparse_mla_decode_dcp_gb300 import capi
+    dev = step.q.device
+    S = wl.spec.tokens_per_req
+    ctx = torch.from_numpy(wl.ctx.astype(np.int32)).to(dev)
+    max_ctx = int(wl.ctx.max())
+    n_ws = capi.dense_decode_workspace_size(wl.T, wl.H, max_ctx, wl.D, wl.spec.interleave, -1)
+    ws = torch.zeros(n_ws, dtype=torch.uint8, device=dev) if n_ws else None
+    out = torch.empty_like(step.out)
+    lse = torch.empty_like(step.lse)
+
+    def run():
+        capi.dcp_dense_mla_decode(step.q, ctx, max_ctx, S, step.pools, step.block_tables,
+                                  wl.spec.block_size, wl.spec.sm_scale,
+                                  interleave=wl.spec.interleave, bt_widths=step.bt_widths,
+                                  out=out, lse=lse, workspace=ws)
+    run()
+    ms = float(np.mean(_timed_steps(run, n, flush, stream)))
+    keys = int(sum(int(c) - S + s + 1 for c in wl.ctx for s in range(S)))
+    roof = _roofline("smla_dcp_dense_mla_decode", ms, keys, wl.H, peaks, workload)
+    roof["keys_per_launch"] = keys
+    del ws
+    return {"ms_per_step": ms, "value": wl.T / (ms * 1e-3), "launches_per_step": 1,
+            "roofline": roof}
+
+
+def _topk_path(wl, n, flush, stream, peaks, dev):
+    """Global top-K of synthetic indexer scores: one fp32 score per cached
+    position of each row (seeded normal draws), K = the workload's top-k."""
+    import torch
+
+    from sparse_mla_decode_dcp_gb300 import capi
+    S = wl.spec.tokens_per_req
+    L = int(wl.ctx.max())
+    gen = torch.Generator(device=dev).manual_seed(12345)
+    scores = torch.randn((wl.T, L), generator=gen, device=dev, dtype=torch.float32)
+    n_cand_np = np.array([int(wl.ctx[t // S]) - S + t % S + 1 for t in range(wl.T)], np.int32)
+    n_cand = torch.from_numpy(n_cand_np).to(dev)
+    ids = torch.empty((wl.T, wl.K), dtype=torch.int32, device=dev)
+
+    def run():
+        capi.load().smla_topk_select(scores.data_ptr(), scores.stride(0), L, n_cand.data_ptr(),
+                                     wl.T, wl.K, 1, 0, 1, ids.data_ptr(), None,
+                                     int(stream.cuda_stream))
+    run()
+    ms = float(np.mean(_timed_steps(run, n, flush, stream)))
+    nbytes = 4 * int(n_cand_np.sum()) + 4 * wl.T * wl.K
+    return {"ms_per_step": ms, "launches_per_step": 1,
+            "roofline": _hbm_roofline("smla_topk_select", ms, nbytes, peaks,
+                                      "4 B per candidate score read + 4 B per id written")}
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -400,6 +538,9 @@ def run_gpu(args):
     fused_ms = ms_per_step if args.path == "fused" else alt_ms
     per_shard_roof = _roofline("smla_sparse_mla_decode", float(dec_ms.mean()), total_keys / D, H,
                                peaks, args.workload)
+    dense_path = _dense_path(step, wl, max(3, min(n_aux, 10)), flush, stream, peaks,
+                             args.workload)
+    topk_path = _topk_path(wl, n_aux, flush, stream, peaks, dev)
     # index: read the top-k ids and write the slots (4 B each per entry),
     # read the row's request id and write its valid count
     index_roof = _hbm_roofline("smla_dcp_filter_convert_index", float(idx_ms.mean()),
@@ -434,12 +575,7 @@ def run_gpu(args):
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16xf16->f32 (MMA), f32 softmax", "data": "synthetic",
-        "config": {"workload": args.workload, "path": args.path, "T": T, "H": H, "K": K, "D": D,
-                   "block_size": wl.spec.block_size, "requests": wl.spec.num_reqs,
-                   "cached_tokens": int(sum(int(c) for c in wl.ctx)),
-                   "l2": "flushed before every step (256 MiB write, outside the events)",
-                   "parallelism": f"replicas x{world}" if world > 1 else
-                                  "single GPU, D shards simulated as D pools"},
+        "config": workload_config(wl, args, world),
         "roofline": roof,
         "paths": {
             "fused": {"ms_per_step": fused_ms, "value": world * T / (fused_ms * 1e-3),
@@ -452,6 +588,8 @@ def run_gpu(args):
                          "index_roofline": index_roof,
                          "merge_launch_us": float(mrg_ms.mean()) * 1e3,
                          "merge_roofline": merge_roof},
+            "dense": dense_path,
+            "topk": topk_path,
         },
         "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
@@ -461,6 +599,8 @@ def run_gpu(args):
     }
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, args.cpu_sample_tokens)
+        result["cpu_baseline"]["single_thread"] = cpu_baseline_single_thread(args.workload,
+                                                                             args.seed)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -494,15 +634,13 @@ def run_reference(args):
         times.append(n / b["value"])
     value = n * len(times) / sum(times)
     b["value"] = value
+    b["sample"] = f"{n} query rows per step: " + b["sample"]
     result = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": args.workload, "T": wl.T, "H": wl.H, "K": wl.K, "D": wl.D,
-                   "block_size": wl.spec.block_size, "requests": wl.spec.num_reqs,
-                   "cached_tokens": int(sum(int(c) for c in wl.ctx)),
-                   "sample_rows_per_step": n},
+        "config": workload_config(wl, args, world),
         "cpu_baseline": b,
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

@@ -78,9 +78,19 @@ enum {
   SMLA_DEVERR_REQ_ID = 2u,      /* req_id_per_token outside [0, num_reqs)      */
   SMLA_DEVERR_SLOT_RANGE = 4u,  /* local slot >= num_slots                     */
   SMLA_DEVERR_TIMEOUT = 8u,     /* a bounded wait inside a kernel gave up      */
-  SMLA_DEVERR_CONTEXT = 16u     /* dense decode: a context shorter than its
+  SMLA_DEVERR_CONTEXT = 16u,    /* dense decode: a context shorter than its
                                    request's query tokens or past max_ctx     */
+  SMLA_DEVERR_RANGE = 32u       /* a q or rope value, or a latent group scale,
+                                   that the fp16 keys cannot carry (below)    */
 };
+/* The decode kernels compute QK^T and PV on fp16 operands: q and the rope
+ * values are converted from bf16 and each latent value is dequantised as
+ * e4m3 code x scale, rounded once to fp16.  SMLA_DEVERR_RANGE is set when a
+ * q or rope value of a row has |x| >= 65536 (inf / NaN included), when a
+ * group scale exceeds 65504 / 448 (its dequantised values would overflow
+ * fp16), or when a nonzero scale is below 2^-22 (its keys would be fp16
+ * subnormals and lose precision).  The result is still written; the bit says
+ * it may be outside the stated tolerances. */
 /* With SMLA_DEVERR_TIMEOUT, bits 8..31 of the word tell which of the decode
  * kernel's internal waits gave up (a diagnostic bitmask, one bit per site). */
 

@@ -27,6 +27,7 @@ DEVERR_REQ_ID = 2
 DEVERR_SLOT_RANGE = 4
 DEVERR_TIMEOUT = 8
 DEVERR_CONTEXT = 16
+DEVERR_RANGE = 32
 
 MAX_HEADS = 128
 MAX_DCP = 16

@@ -178,6 +178,26 @@ __device__ __forceinline__ bool wait_bar_cluster(uint64_t* bar, uint32_t parity,
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
+// Nonzero when a bf16 of the pair in `w` would not fit fp16 (|x| >= 65536:
+// bf16 has no value between 65280 and 65536, and fp16's largest is 65504;
+// inf and NaN included): each 15-bit magnitude plus 0x3880 reaches bit 15
+// exactly when it is >= 0x4780, with no carry between the halves.
+__device__ __forceinline__ uint32_t bf16x2_over_fp16(uint32_t w) {
+  return ((w & 0x7FFF7FFFu) + 0x38803880u) & 0x80008000u;
+}
+
+__device__ __forceinline__ uint32_t bf16x8_over_fp16(const uint4& v) {
+  return bf16x2_over_fp16(v.x) | bf16x2_over_fp16(v.y) | bf16x2_over_fp16(v.z) |
+         bf16x2_over_fp16(v.w);
+}
+
+// A latent group scale the fp16 keys cannot carry: its dequantised values
+// (up to 448 x scale) overflow fp16, or a nonzero scale so small that
+// 2^8 x scale is an fp16 subnormal (the keys lose precision); NaN included.
+__device__ __forceinline__ bool scale_out_of_range(float s) {
+  return !(s <= 65504.f / 448.f) || (s != 0.f && s < 0x1p-22f);
+}
+
 // 8 bf16 -> 8 fp16 (exact for values in fp16 range)
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -326,7 +346,8 @@ __device__ __forceinline__ void read_row(uint32_t row, bool live, int c, int par
 
 // Convert the read pieces into the swizzled fp16 operand tile at `op` (the
 // same code path for both CTA ranks and parts).
-__device__ __forceinline__ void convert_row(const ConvRegs& r, uint32_t op, int key, int part) {
+// Returns true when the key's scale or rope values do not fit the fp16 keys.
+__device__ __forceinline__ bool convert_row(const ConvRegs& r, uint32_t op, int key, int part) {
   __half2 hi, lo;
   split_scale(r.scale, hi, lo);
 #pragma unroll
@@ -335,9 +356,13 @@ __device__ __forceinline__ void convert_row(const ConvRegs& r, uint32_t op, int 
     sts128(op_addr(op, key, ldim), e4m3x8_scaled(make_uint2(r.cur[k].x, r.cur[k].y), hi, lo));
     sts128(op_addr(op, key, ldim + 8), e4m3x8_scaled(make_uint2(r.cur[k].z, r.cur[k].w), hi, lo));
   }
+  uint32_t over = 0;
 #pragma unroll
-  for (int q = 0; q < kRopePerPart; ++q)
+  for (int q = 0; q < kRopePerPart; ++q) {
+    over |= bf16x8_over_fp16(r.cur[kCodePerPart + q]);
     sts128(op_addr(op, key, 256 + 16 * part + 8 * q), bf16x8_to_f16x8(r.cur[kCodePerPart + q]));
+  }
+  return over != 0 || scale_out_of_range(r.scale);
 }
 
 // The loader warps' loop.  Loader ld owns pieces ld + 96k (k < 14) of every
@@ -409,6 +434,7 @@ __device__ void convert_loop(Ctl* ctl, uint8_t* sm, int n, int ntiles, int key, 
                              int lane, volatile int* abort) {
   const uint32_t raw0 = smem_u32(sm + kOffRaw);
   const uint32_t op0 = smem_u32(sm + kOffOp);
+  bool out_of_range = false;
 #pragma unroll 1
   for (int i = 0; i < ntiles; ++i) {
     const int st = i % kRawStages;
@@ -423,10 +449,12 @@ __device__ void convert_loop(Ctl* ctl, uint8_t* sm, int n, int ntiles, int key, 
     if (i >= kStages &&
         !wait_bar(&ctl->freed[i % kStages], ((i - kStages) / kStages) & 1, abort, kWsFreed))
       break;
-    convert_row(r, op0 + (i % kStages) * kOpTileBytes, key, part);
+    out_of_range |= convert_row(r, op0 + (i % kStages) * kOpTileBytes, key, part) &&
+                    key < n - i * kTileN;
     fence_async_shared();
     mbar_arrive(&ctl->full[i % kStages]);
   }
+  if (out_of_range) atomicOr(&g_decode_error, SMLA_DEVERR_RANGE);
 }
 
 // Split-K epilogue: write this split's unnormalised O half, its log2-domain
@@ -563,8 +591,11 @@ __device__ __forceinline__ void issue_q_tma(const DecodeArgs& a, int64_t t, int 
 // Convert head row h of the staged q into tensor memory as fp16 pairs (the
 // A operand of QK^T), 64 dims per group of 32 columns; reads follow the
 // boxes' swizzles, so 8 consecutive rows hit 8 different bank groups.
-__device__ void q_to_tmem(uint32_t tb, int warp, int h, bool live, uint32_t src) {
+// Returns true when a q value of the row does not fit fp16 (the operand
+// precision of QK^T).
+__device__ bool q_to_tmem(uint32_t tb, int warp, int h, bool live, uint32_t src) {
   const uint32_t base = tmem_addr(tb, 32 * warp, kQCol);
+  uint32_t over = 0;
 #pragma unroll 1
   for (int grp = 0; grp < 5; ++grp) {
     uint4 g[8];
@@ -576,10 +607,12 @@ __device__ void q_to_tmem(uint32_t tb, int warp, int h, bool live, uint32_t src)
       else
         addr = src + 4 * kQLatBox + sw64_offset(h, v & 3);
       g[v] = (live && (grp < 4 || v < 4)) ? lds128(addr) : make_uint4(0, 0, 0, 0);
+      over |= bf16x8_over_fp16(g[v]);
     }
     q_store_group(g, base + 32 * grp, grp < 4);
   }
   tmem_st_wait();
+  return over != 0;
 }
 
 // MMA issue, fully unrolled: one thread issues a tcgen05.mma every few tens
@@ -1089,7 +1122,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // Q half -> TMEM, overlapping the compaction below
     // the whole q tile landed (issued by thread 0 before the set-up barrier)
     bool qok = wait_bar(&ctl->q_tma, 0, &ctl->abort, kWsQReady);
-    q_to_tmem(ctl->tbase, warp, tid, qok && tid < a.H, smem_u32(sm + kOffOp));
+    if (q_to_tmem(ctl->tbase, warp, tid, qok && tid < a.H, smem_u32(sm + kOffOp)))
+      atomicOr(&g_decode_error, SMLA_DEVERR_RANGE);
     tc_fence_before();
     mbar_arrive(&ctl->q_ready);
   } else if (warp < 8) {

@@ -792,3 +792,96 @@ def test_dcp_topk_local_then_merge_equals_unsharded(cuda_device, D, I, decimals)
     ref = oracle.dcp_topk_merge([x.cpu().numpy() for x in ids],
                                 [x.cpu().numpy().astype(np.float64) for x in scs], K)
     assert np.array_equal(got.cpu().numpy(), ref)
+
+
+# --------------------------------------------------- precision envelope, range
+def _envelope_case(dev, sigma):
+    """q ~ N(0, sigma^2): the rows' largest |score| grows as ~7.9 sigma nats
+    at sm_scale = 1/sqrt(192) over unit-variance latents."""
+    gen = torch.Generator(device=dev).manual_seed(3)
+    n = 6000
+    pool = inputs.random_rows(n, gen, dev)
+    rng = np.random.default_rng(3)
+    T, H, K = 4, 128, 2048
+    s = np.stack([rng.choice(n, K, replace=False) for _ in range(T)]).astype(np.int32)
+    s[1, 100:] = -1  # a row of 100 keys
+    s[2, 8:] = -1    # a row of 8 keys
+    g = torch.Generator(device=dev).manual_seed(1003)
+    q = (torch.randn((T, H, 576), generator=g, device=dev) * sigma).to(torch.bfloat16)
+    out, lse = capi.sparse_mla_decode(q, pool, torch.from_numpy(s).to(dev), 1 / math.sqrt(192))
+    torch.cuda.synchronize()
+    qb = _q_bits(q)
+    ref_out, ref_lse = oracle.sparse_mla_decode(qb, pool.cpu().numpy(), s, 1 / math.sqrt(192))
+    qf = oracle.bf16_bits_to_f64(qb)
+    smax = 0.0
+    for t in range(T):
+        nope, rope = oracle.parse_rows(pool.cpu().numpy()[s[t][s[t] >= 0]])
+        smax = max(smax, float(np.abs(qf[t] @ np.concatenate([nope, rope], 1).T).max()
+                               / math.sqrt(192)))
+    return out, lse, ref_out, ref_lse, smax
+
+
+@pytest.mark.parametrize("sigma", [1.0, 1.5])
+def test_precision_envelope_scores_up_to_12_nats(cuda_device, sigma):
+    """Keys are rounded once to fp16 (relative 2^-11) and q is bf16 on both
+    sides, so a score carries an absolute error of ~1.8e-4 per nat of score;
+    the LSE error follows the row's largest scores.  Rows whose scores reach
+    8-12 nats (q with 1-1.5x the workloads' spread) meet every tolerance."""
+    out, lse, ref_out, ref_lse, smax = _envelope_case(cuda_device, sigma)
+    assert 7 <= smax <= 12.5
+    compare_out_lse(out, lse, ref_out, ref_lse, where=f"envelope sigma={sigma}")
+
+
+def test_precision_beyond_the_envelope(cuda_device):
+    """With q at 4x the spread the largest scores reach ~31 nats: the LSE
+    error still follows the error model (<= 2.5e-4 per nat of the row's
+    largest |score|) but leaves the 2e-3 tolerance, which holds while those
+    scores stay below ~15 nats; out stays within its tolerances (a weighted
+    average of latents, it does not inherit the score offset)."""
+    out, lse, ref_out, ref_lse, smax = _envelope_case(cuda_device, 4.0)
+    err = np.abs(lse.cpu().numpy() - ref_lse).max()
+    assert smax > 25
+    assert 2e-3 < err <= 2.5e-4 * smax
+    o = out.float().cpu().numpy()
+    ob = oracle.compare.bf16_round(ref_out)
+    assert np.linalg.norm(o - ob) / np.linalg.norm(ob) <= 1e-2 and np.abs(o - ob).max() <= 2e-2
+
+
+def test_range_guard_flags_values_the_fp16_keys_cannot_carry(cuda_device):
+    """A q or rope value past fp16's range, a group scale whose values would
+    overflow fp16 and a nonzero scale below 2^-22 each set SMLA_DEVERR_RANGE;
+    in-range inputs (scales up to 65504/448, zero scales) do not."""
+    dev = cuda_device
+    gen = torch.Generator(device=dev).manual_seed(8)
+    pool = inputs.random_rows(64, gen, dev)
+    g = torch.Generator(device=dev).manual_seed(1008)
+    q = torch.randn((2, 16, 576), generator=g, device=dev).to(torch.bfloat16)
+    slots = torch.arange(64, dtype=torch.int32, device=dev).reshape(2, 32)
+
+    def flags(qq, pp):
+        capi.get_device_error(clear=True)
+        capi.sparse_mla_decode(qq, pp, slots, 0.07)
+        torch.cuda.synchronize()
+        return capi.get_device_error(clear=True)
+
+    assert flags(q, pool) == 0
+    ok = pool.clone()
+    sc = ok[:, 512:528].contiguous().view(torch.float32)
+    sc[3, 1] = 146.0   # largest values 448 x 146 = 65408: still fp16
+    sc[5, 2] = 0.0     # an all-zero group
+    ok[:, 512:528] = sc.view(torch.uint8)
+    assert flags(q, ok) == 0
+    big_q = q.clone()
+    big_q[1, 3, 200] = 70000.0
+    assert flags(big_q, pool) & capi.DEVERR_RANGE
+    for row, col, val in ((7, 0, 150.0), (40, 3, 1e-8)):
+        bad = pool.clone()
+        sc = bad[:, 512:528].contiguous().view(torch.float32)
+        sc[row, col] = val
+        bad[:, 512:528] = sc.view(torch.uint8)
+        assert flags(q, bad) & capi.DEVERR_RANGE, (row, col, val)
+    rope = pool.clone()
+    r = rope[:, 528:656].contiguous().view(torch.bfloat16)
+    r[20, 5] = float("inf")
+    rope[:, 528:656] = r.view(torch.uint8)
+    assert flags(q, rope) & capi.DEVERR_RANGE
