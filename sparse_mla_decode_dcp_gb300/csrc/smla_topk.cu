@@ -14,11 +14,20 @@
 //
 // Method: every candidate gets a unique 64-bit key -- an order-preserving
 // integer image of its score in the high half, the complement of its id in
-// the low half -- so "the K best" is "the K largest keys".  One CTA per row
-// finds the K-th largest key with a most-significant-digit radix select (8
-// bits per pass over the row, stopping as soon as the boundary bucket holds
-// exactly the keys still needed), gathers the keys at or above it into
-// shared memory and sorts them with a bitonic network.
+// the low half -- so "the K best" is "the K largest keys".  One CTA per row:
+//   1. one pass over the row builds a histogram of the keys' top 12 bits
+//      (sign, exponent and 3 mantissa bits of the score) in shared memory; a
+//      block-wide suffix scan gives each bin its first place in the
+//      descending order and finds the bin holding the K-th largest key;
+//   2. a second pass puts every key of a higher bin at its bin's next place
+//      (a counting sort by bin) and the boundary bin's keys in per-warp lists;
+//   3. a most-significant-digit radix select over the boundary bin's keys (8
+//      bits per step, in shared memory) picks those still needed;
+//   4. a bitonic network sorts the K selected keys (in registers and warp
+//      shuffles below 32 keys per warp apart).
+// Only when the boundary bin overflows the per-warp lists (scores tied far
+// beyond K) does step 3 read the row from global memory again, digit by
+// digit.
 #include "../../include/smla.h"
 #include "smla_internal.h"
 
@@ -26,6 +35,12 @@ namespace smla {
 namespace {
 
 constexpr int kThreads = 1024;
+constexpr int kBinBits = 12;
+constexpr int kBins = 1 << kBinBits;
+constexpr int kBinShift = 64 - kBinBits;
+constexpr int kSmemBytes = 226 * 1024;  // one CTA per SM: all of it but the static part
+constexpr int kHistBytes = kBins * 4;
+constexpr int kWarps = kThreads / 32;
 
 // Order-preserving image of a float: larger score, larger key; every NaN
 // maps to 0 (below -inf) and -0 to the key of +0.
@@ -40,134 +55,410 @@ __device__ __forceinline__ float key_score(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-__device__ __forceinline__ uint64_t make_key(float score, int32_t id) {
-  return (uint64_t(score_key(score)) << 32) | uint64_t(0xFFFFFFFFu - uint32_t(id));
+__device__ __forceinline__ uint64_t make_key(uint32_t skey, int32_t id) {
+  return (uint64_t(skey) << 32) | uint64_t(0xFFFFFFFFu - uint32_t(id));
 }
 
-// Candidate j of row i: its key, or false when j is not a candidate.
-template <bool kExplicit>
-__device__ __forceinline__ bool candidate(const TopkArgs& a, int64_t i, int j, int n,
-                                          uint64_t& key) {
-  if (kExplicit) {
-    const int32_t id = __ldg(a.cand_ids + i * a.row_stride + j);
-    if (id < 0) return false;
-    key = make_key(__ldg(a.scores + i * a.row_stride + j), id);
-    return true;
+// Warp-aggregated append of `key` (for lanes with `take`) to list[*count].
+// Returns nothing; entries at or past `cap` are dropped (the count still
+// grows, so an overflow is visible).
+__device__ __forceinline__ void append(bool take, uint64_t key, uint64_t* list, int* count, int cap) {
+  const uint32_t m = __ballot_sync(0xffffffffu, take);
+  if (m == 0) return;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(m) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(count, __popc(m));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  if (take) {
+    const int p = base + __popc(m & ((1u << lane) - 1u));
+    if (p < cap) list[p] = key;
   }
-  if (j >= n) return false;
-  // local position j of `rank` -> global position
-  const uint32_t g = fastdiv(uint32_t(j), a.div_I);
-  const int32_t id = int32_t(g) * a.interleave * a.D + a.rank * a.interleave +
-                     (j - int32_t(g) * a.interleave);
-  key = make_key(__ldg(a.scores + i * a.row_stride + j), id);
-  return true;
 }
 
-template <bool kExplicit>
-__global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
-  extern __shared__ uint64_t buf[];  // kp keys
-  __shared__ uint32_t hist[256];
-  __shared__ uint64_t s_prefix, s_mask;
-  __shared__ int s_need, s_done, s_count;
-  const int64_t i = blockIdx.x;
+// Global id of local position j of `rank` (select front end): runs of I
+// positions go to the ranks in turn.
+__device__ __forceinline__ int32_t global_id(const TopkArgs& a, int j) {
+  const uint32_t g = fastdiv(uint32_t(j), a.div_I);  // run of I positions
+  return int32_t(g) * a.interleave * a.D + a.rank * a.interleave + (j - int32_t(g) * a.interleave);
+}
+
+// Visit every candidate of row i, all lanes of a warp together: f(valid,
+// score key, x) is called by every lane, x the candidate's id (merge: entry
+// j < M, skipped when its id is -1) or its local position j < n (select:
+// global_id(x) is its id, computed only where needed).  A thread keeps
+// kUnroll loads in flight (16 bytes of scores each when the rows allow it,
+// kVec4): a gather's rate is set by the bytes in flight.  The loads are
+// issued unconditionally (at a clamped index, the result then masked): a
+// branch around a load would make each wait for the one before.
+template <bool kExplicit, bool kVec4, typename F>
+__device__ __forceinline__ void for_each_candidate(const TopkArgs& a, int64_t i, int span, F f) {
+  const float* srow = a.scores + i * a.row_stride;
+  const int32_t* irow = kExplicit ? a.cand_ids + i * a.row_stride : nullptr;
+  constexpr int kW = kVec4 ? 4 : 1;        // candidates per load
+  constexpr int kUnroll = kVec4 ? 4 : 8;   // loads in flight per thread
+  for (int j0 = kW * threadIdx.x; j0 - kW * int(threadIdx.x) < span; j0 += kW * kThreads * kUnroll) {
+    float sc[kUnroll][kW];
+    int32_t id[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (kVec4) {
+        const int jc = min(j0 + u * kW * kThreads, (span - 1) & ~3);
+        const float4 v = __ldg(reinterpret_cast<const float4*>(srow + jc));
+        sc[u][0] = v.x;
+        sc[u][kW > 1 ? 1 : 0] = v.y;
+        sc[u][kW > 2 ? 2 : 0] = v.z;
+        sc[u][kW > 3 ? 3 : 0] = v.w;
+      } else {
+        const int jc = min(j0 + u * kThreads, span - 1);
+        sc[u][0] = __ldg(srow + jc);
+        if (kExplicit) id[u] = __ldg(irow + jc);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+#pragma unroll
+      for (int e = 0; e < kW; ++e) {
+        const int j = j0 + u * kW * kThreads + e;
+        if (kExplicit)
+          f(j < span && id[u] >= 0, score_key(sc[u][e]), id[u]);
+        else
+          f(j < span, score_key(sc[u][e]), j);
+      }
+    }
+  }
+}
+
+// Warp 0 of the block: the bucket of `hist` (nb <= 256 buckets) holding the
+// need-th largest key counting from the top, the keys still needed inside it
+// and whether the whole bucket is needed.  Lane l owns buckets
+// nb - 1 - 8l .. nb - 8 - 8l (high to low).
+__device__ __forceinline__ void find_bucket(const uint32_t* hist, int nb, int need, int& pick,
+                                            int& need_in, bool& whole) {
+  const int lane = threadIdx.x & 31;
+  uint32_t c[8], own = 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int b = nb - 1 - 8 * lane - q;
+    c[q] = b >= 0 ? hist[b] : 0u;
+    own += c[q];
+  }
+  uint32_t inc = own;  // inclusive prefix over lanes 0..l (higher buckets first)
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += y;
+  }
+  const uint32_t before = inc - own;
+  int p = -1, nd = 0, wh = 0;
+  if (before < uint32_t(need) && inc >= uint32_t(need)) {
+    uint32_t acc = before;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (p < 0 && acc + c[q] >= uint32_t(need)) {
+        p = nb - 1 - 8 * lane - q;
+        nd = need - int(acc);
+        wh = (int(c[q]) == nd);
+      }
+      acc += c[q];
+    }
+  }
+  const uint32_t m = __ballot_sync(0xffffffffu, p >= 0);
+  if (m == 0) {  // fewer keys than needed (cannot happen for distinct keys): stop here
+    pick = 0;
+    need_in = need;
+    whole = true;
+    return;
+  }
+  const int src = __ffs(m) - 1;
+  pick = __shfl_sync(0xffffffffu, p, src);
+  need_in = __shfl_sync(0xffffffffu, nd, src);
+  whole = __shfl_sync(0xffffffffu, wh, src) != 0;
+}
+
+// Bitonic sort (descending) of the kp = E * 1024 keys at `sel` (E >= 2):
+// strides of 32 E or more compare across warps in shared memory; the smaller
+// ones run in registers (thread t holds keys E t .. E t + E - 1) and warp
+// shuffles, without block barriers.
+template <int E>
+__device__ void bitonic_sort_regs(uint64_t* sel, int kp) {
   const int tid = threadIdx.x;
-  const int n = kExplicit ? a.M : min(max(__ldg(a.n_cand + i), 0), a.L);
-  const int span = kExplicit ? a.M : n;  // entries to scan
-
-  // How many candidates: all of them are kept when they fit in K.
-  if (tid == 0) {
-    s_count = 0;
-    s_prefix = 0;
-    s_mask = 0;
-    s_need = a.K;
-    s_done = 0;
-  }
-  __syncthreads();
-  int mine = 0;
-  for (int j = tid; j < span; j += kThreads) {
-    uint64_t k;
-    mine += candidate<kExplicit>(a, i, j, n, k);
-  }
-  atomicAdd(&s_count, mine);
-  __syncthreads();
-  const bool select = s_count > a.K;
-  __syncthreads();
-
-  // Radix select of the K-th largest key, most significant 8 bits first.
-  if (select) {
-#pragma unroll 1
-    for (int shift = 56; shift >= 0 && !s_done; shift -= 8) {
-      for (int b = tid; b < 256; b += kThreads) hist[b] = 0;
-      __syncthreads();
-      const uint64_t prefix = s_prefix, mask = s_mask;
-      for (int j = tid; j < span; j += kThreads) {
-        uint64_t k;
-        if (candidate<kExplicit>(a, i, j, n, k) && (k & mask) == prefix)
-          atomicAdd(&hist[(k >> shift) & 255u], 1u);
-      }
-      __syncthreads();
-      if (tid == 0) {
-        // the bucket holding the need-th largest remaining key, from the top
-        int need = s_need, sel = 0;
-        for (int b = 255; b >= 0; --b) {
-          const int c = int(hist[b]);
-          if (c >= need) {
-            sel = b;
-            break;
-          }
-          need -= c;
-        }
-        s_prefix = prefix | (uint64_t(sel) << shift);
-        s_mask = mask | (uint64_t(255) << shift);
-        s_need = need;
-        s_done = (int(hist[sel]) == need);  // the whole bucket is in
-      }
-      __syncthreads();
-    }
-  }
-
-  // Gather the kept keys: every candidate when they fit, else those whose
-  // key is at or above the boundary in the bits the select fixed (exactly K:
-  // the keys are distinct).
-  if (tid == 0) s_count = 0;
-  __syncthreads();
-  const uint64_t prefix = s_prefix, mask = s_mask;
-  for (int j = tid; j < span; j += kThreads) {
-    uint64_t k;
-    if (candidate<kExplicit>(a, i, j, n, k) && (!select || (k & mask) >= prefix)) {
-      const int p = atomicAdd(&s_count, 1);
-      if (p < a.K) buf[p] = k;
-    }
-  }
-  __syncthreads();
-  const int kept = min(s_count, a.K);
-  for (int p = kept + tid; p < a.kp; p += kThreads) buf[p] = 0;  // below every candidate
-  __syncthreads();
-
-  // Bitonic sort of the kp keys, descending.
-#pragma unroll 1
-  for (int size = 2; size <= a.kp; size <<= 1) {
-#pragma unroll 1
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int p = tid; p < a.kp / 2; p += kThreads) {
+  for (int size = 2; size <= kp; size <<= 1) {
+    int stride = size >> 1;
+    for (; stride >= 32 * E; stride >>= 1) {
+      for (int p = tid; p < kp / 2; p += kThreads) {
         const int lo = 2 * p - (p & (stride - 1));
         const int hi = lo + stride;
         const bool desc = (lo & size) == 0;
-        const uint64_t x = buf[lo], y = buf[hi];
+        const uint64_t x = sel[lo], y = sel[hi];
         if ((x < y) == desc) {
-          buf[lo] = y;
-          buf[hi] = x;
+          sel[lo] = y;
+          sel[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+    uint64_t v[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] = sel[E * tid + e];
+    for (; stride >= E; stride >>= 1) {
+      // partner in lane ^ (stride / E), same slot
+      const int lm = stride / E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const int g = E * tid + e;
+        const uint64_t w = __shfl_xor_sync(0xffffffffu, v[e], lm);
+        const bool desc = (g & size) == 0;
+        const bool lower = (g & stride) == 0;
+        // the lower index keeps the larger key when descending
+        const bool keep_max = (lower == desc);
+        v[e] = keep_max ? (v[e] > w ? v[e] : w) : (v[e] < w ? v[e] : w);
+      }
+    }
+    // strides below E: both keys in this thread (compile-time indices)
+#pragma unroll
+    for (int st = E / 2; st > 0; st >>= 1) {
+      if (st <= stride) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          if ((e & st) == 0) {
+            const int g = E * tid + e;
+            const bool desc = (g & size) == 0;
+            const uint64_t x = v[e], y = v[e + st];
+            if ((x < y) == desc) {
+              v[e] = y;
+              v[e + st] = x;
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) sel[E * tid + e] = v[e];
+    __syncthreads();
+  }
+}
+
+// The plain shared-memory network, for kp < 2048 and kp = 16384 (whose 16
+// keys per thread would not fit the registers).
+__device__ void bitonic_sort_smem(uint64_t* sel, int kp) {
+  const int tid = threadIdx.x;
+  for (int size = 2; size <= kp; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int p = tid; p < kp / 2; p += kThreads) {
+        const int lo = 2 * p - (p & (stride - 1));
+        const int hi = lo + stride;
+        const bool desc = (lo & size) == 0;
+        const uint64_t x = sel[lo], y = sel[hi];
+        if ((x < y) == desc) {
+          sel[lo] = y;
+          sel[hi] = x;
         }
       }
       __syncthreads();
     }
   }
+}
 
-  for (int p = tid; p < a.K; p += kThreads) {
-    const bool live = p < kept;
-    const uint64_t k = buf[p];
-    a.out_ids[i * a.K + p] = live ? int32_t(0xFFFFFFFFu - uint32_t(k)) : -1;
-    if (a.out_scores) a.out_scores[i * a.K + p] = live ? key_score(uint32_t(k >> 32)) : 0.f;
+template <bool kExplicit, bool kVec4>
+__global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem);                  // bin counts
+  uint32_t* cur = hist + kBins;                                        // bin cursors
+  uint64_t* sel = reinterpret_cast<uint64_t*>(smem + 2 * kHistBytes);  // kp keys
+  uint64_t* bnd = sel + a.kp;  // boundary bin: one region of `reg` keys per warp
+  const int reg = cap / kWarps;
+  __shared__ uint32_t warp_sum[kWarps];
+  __shared__ int wcount[kWarps];
+  __shared__ int s_nsel, s_need, s_bin, s_done;
+  __shared__ uint64_t s_prefix, s_mask;
+  const int64_t i = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int n = kExplicit ? a.M : min(max(__ldg(a.n_cand + i), 0), a.L);
+  const int span = n;
+  const int K = a.K;
+
+  // 1) histogram of the keys' top 12 bits
+  for (int b = tid; b < kBins; b += kThreads) hist[b] = 0;
+  __syncthreads();
+  for_each_candidate<kExplicit, kVec4>(a, i, span, [&](bool ok, uint32_t sk, int32_t) {
+    if (ok) atomicAdd(&hist[sk >> (32 - kBinBits)], 1u);
+  });
+  __syncthreads();
+  // suffix sums over bins: thread t owns bins 4t .. 4t + 3
+  static_assert(kBins == 4 * kThreads, "four bins per thread");
+  uint32_t own[4], own_sum = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    own[q] = hist[4 * tid + q];
+    own_sum += own[q];
+  }
+  uint32_t suf = own_sum;  // inclusive suffix within the warp (lanes >= this one)
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t y = __shfl_down_sync(0xffffffffu, suf, off);
+    if (lane + off < 32) suf += y;
+  }
+  if (lane == 0) warp_sum[warp] = suf;  // the warp's total
+  __syncthreads();
+  uint32_t higher = 0, total = 0;  // keys in warps above this one; all keys
+  for (int w = 0; w < kWarps; ++w) {
+    const uint32_t x = warp_sum[w];
+    total += x;
+    if (w > warp) higher += x;
+  }
+  const bool select = total > uint32_t(K);
+  {
+    // keys strictly above each of this thread's bins: each bin's first place
+    // in the descending order (its cursor); the boundary bin holds the K-th
+    uint32_t above = higher + suf - own_sum;
+#pragma unroll
+    for (int q = 3; q >= 0; --q) {
+      cur[4 * tid + q] = above;
+      if (select && above < uint32_t(K) && above + own[q] >= uint32_t(K)) {
+        s_bin = 4 * tid + q;
+        s_need = K - int(above);
+      }
+      above += own[q];
+    }
+  }
+  __syncthreads();
+  const int bin = select ? s_bin : -1;
+  const int need = select ? s_need : 0;
+  const int nabove = select ? K - need : int(total);  // keys above the boundary bin
+  // 2) keys of higher bins -> their bin's places in `sel`; the boundary bin ->
+  //    this warp's region of `bnd` (most keys lie below the boundary: one
+  //    ballot skips them)
+  int wc = 0;  // this warp's boundary keys (warp-uniform)
+  for_each_candidate<kExplicit, kVec4>(a, i, span, [&](bool ok, uint32_t sk, int32_t x) {
+    const int kb = int(sk >> (32 - kBinBits));
+    const bool take = ok && kb >= bin;
+    if (__ballot_sync(0xffffffffu, take) == 0) return;
+    const uint64_t key = make_key(sk, kExplicit ? x : (take ? global_id(a, x) : 0));
+    if (take && kb > bin) sel[atomicAdd(&cur[kb], 1u)] = key;
+    const uint32_t m = __ballot_sync(0xffffffffu, take && kb == bin);
+    if (take && kb == bin) {
+      const int q = wc + __popc(m & ((1u << lane) - 1u));
+      if (q < reg) bnd[warp * reg + q] = key;
+    }
+    wc += __popc(m);
+  });
+  if (lane == 0) wcount[warp] = wc;
+  __syncthreads();
+  bool overflow = false;
+  int nb = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    overflow |= wcount[w] > reg;
+    nb += wcount[w];
+  }
+  const int kept = min(int(total), K);
+  int32_t* out_ids = a.out_ids + i * K;
+  float* out_scores = a.out_scores ? a.out_scores + i * K : nullptr;
+  auto emit = [&](int pos, uint64_t k) {
+    out_ids[pos] = int32_t(0xFFFFFFFFu - uint32_t(k));
+    if (out_scores) out_scores[pos] = key_score(uint32_t(k >> 32));
+  };
+
+  // 3) the `need` largest keys of the boundary bin by a radix select over
+  //    its keys, gathered into one list (a pass over global memory replaces
+  //    the list when the bin overflowed the warps' regions: ties far beyond
+  //    K), then a bitonic sort of `sel`
+  if (tid == 0) s_nsel = nabove;
+  if (select) {
+    const bool in_smem = !overflow;
+    if (in_smem) {
+      // compact the regions in place, 1024 keys at a time: a key's place in
+      // the list is never past its slot, and keys are read before written
+      for (int c0 = 0; c0 < nb; c0 += kThreads) {
+        const int u = c0 + tid;
+        uint64_t x = 0;
+        if (u < nb) {
+          int w = 0, base = 0;
+          while (base + wcount[w] <= u) base += wcount[w++];
+          x = bnd[w * reg + (u - base)];
+        }
+        __syncthreads();
+        if (u < nb) bnd[u] = x;
+        __syncthreads();
+      }
+    }
+    if (tid == 0) {
+      s_prefix = uint64_t(bin) << kBinShift;
+      s_mask = ~uint64_t(0) << kBinShift;
+      s_need = need;
+      s_done = (nb == need);  // the whole bin is in
+    }
+    __syncthreads();
+    // radix steps over the bits below the bin, 8 at a time (4 last); the
+    // keys are distinct, so the last step leaves one key per bucket (the
+    // bound on `shift` only matters for duplicate merge input)
+#pragma unroll 1
+    for (int shift = kBinShift - 8; !s_done && shift > -8; shift -= 8) {
+      const int sh = max(shift, 0);
+      const int bits = shift >= 0 ? 8 : 8 + shift;
+      const uint32_t nbk = 1u << bits;
+      for (int b = tid; b < 256; b += kThreads) hist[b] = 0;
+      __syncthreads();
+      const uint64_t prefix = s_prefix, mask = s_mask;
+      auto count = [&](uint64_t key) {
+        if ((key & mask) == prefix) atomicAdd(&hist[(key >> sh) & (nbk - 1)], 1u);
+      };
+      if (in_smem) {
+        for (int u = tid; u < nb; u += kThreads) count(bnd[u]);
+      } else {
+        for_each_candidate<kExplicit, false>(a, i, span, [&](bool ok, uint32_t sk, int32_t x) {
+          if (ok && int(sk >> (32 - kBinBits)) == bin)
+            count(make_key(sk, kExplicit ? x : global_id(a, x)));
+        });
+      }
+      __syncthreads();
+      if (warp == 0) {
+        int pick, nd;
+        bool whole;
+        find_bucket(hist, int(nbk), s_need, pick, nd, whole);
+        if (lane == 0) {
+          s_prefix = prefix | (uint64_t(pick) << sh);
+          s_mask = mask | (uint64_t(nbk - 1) << sh);
+          s_need = nd;
+          s_done = whole;  // the whole bucket is in
+        }
+      }
+      __syncthreads();
+    }
+    // append the boundary bin's keys at or above the selected prefix
+    // (exactly `need` of them: the keys are distinct)
+    const uint64_t prefix = s_prefix, mask = s_mask;
+    if (in_smem) {
+      for (int u0 = 0; u0 < nb; u0 += kThreads) {
+        const int u = u0 + tid;
+        const uint64_t key = u < nb ? bnd[u] : 0;
+        append(u < nb && (key & mask) >= prefix, key, sel, &s_nsel, a.kp);
+      }
+    } else {
+      for_each_candidate<kExplicit, false>(a, i, span, [&](bool ok, uint32_t sk, int32_t x) {
+        const bool inbin = ok && int(sk >> (32 - kBinBits)) == bin;
+        const uint64_t key = make_key(sk, kExplicit ? x : (inbin ? global_id(a, x) : 0));
+        append(inbin && (key & mask) >= prefix, key, sel, &s_nsel, a.kp);
+      });
+    }
+  }
+  __syncthreads();
+  for (int p = kept + tid; p < a.kp; p += kThreads) sel[p] = 0;  // below every candidate
+  __syncthreads();
+  switch (a.kp) {
+    case 2048: bitonic_sort_regs<2>(sel, a.kp); break;
+    case 4096: bitonic_sort_regs<4>(sel, a.kp); break;
+    case 8192: bitonic_sort_regs<8>(sel, a.kp); break;
+    default: bitonic_sort_smem(sel, a.kp); break;
+  }
+  for (int p = tid; p < K; p += kThreads) {
+    if (p < kept) {
+      emit(p, sel[p]);
+    } else {
+      out_ids[p] = -1;
+      if (out_scores) out_scores[p] = 0.f;
+    }
   }
 }
 
@@ -177,25 +468,34 @@ int pow2_at_least(int x) {
   return p;
 }
 
-template <bool kExplicit>
-cudaError_t launch(TopkArgs a, cudaStream_t s) {
-  a.kp = pow2_at_least(a.K);
-  const size_t smem = size_t(a.kp) * sizeof(uint64_t);
-  cudaError_t e = cudaFuncSetAttribute(topk_kernel<kExplicit>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+template <bool kExplicit, bool kVec4>
+cudaError_t launch(TopkArgs a, int cap, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(topk_kernel<kExplicit, kVec4>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  topk_kernel<kExplicit><<<dim3(unsigned(a.T)), dim3(kThreads), smem, s>>>(a);
+  topk_kernel<kExplicit, kVec4><<<dim3(unsigned(a.T)), dim3(kThreads), kSmemBytes, s>>>(a, cap);
   return cudaGetLastError();
 }
+
+// Shared memory: the histogram and the bin cursors, the selection (kp keys),
+// the boundary bin's regions.
+int boundary_cap(const TopkArgs& a) { return (kSmemBytes - 2 * kHistBytes) / 8 - a.kp; }
 
 }  // namespace
 
 cudaError_t launch_topk_select(const TopkArgs& args, cudaStream_t s) {
   TopkArgs a = args;
   a.div_I = make_fastdiv(uint32_t(a.interleave));
-  return launch<false>(a, s);
+  a.kp = pow2_at_least(a.K);
+  // 16-byte score loads when every row starts on a 16-byte boundary
+  const bool vec = (reinterpret_cast<uintptr_t>(a.scores) % 16 == 0) && (a.row_stride % 4 == 0);
+  return vec ? launch<false, true>(a, boundary_cap(a), s) : launch<false, false>(a, boundary_cap(a), s);
 }
 
-cudaError_t launch_topk_merge(const TopkArgs& args, cudaStream_t s) { return launch<true>(args, s); }
+cudaError_t launch_topk_merge(const TopkArgs& args, cudaStream_t s) {
+  TopkArgs a = args;
+  a.kp = pow2_at_least(a.K);
+  return launch<true, false>(a, boundary_cap(a), s);
+}
 
 }  // namespace smla

@@ -752,6 +752,17 @@ def test_topk_select_heavy_ties(cuda_device, decimals):
     _topk_vs_oracle(cuda_device, np.zeros((2, 5000)), [5000, 100], 2048, "all equal")
 
 
+@pytest.mark.parametrize("L,K", [(60000, 2048), (40000, 16384)])
+def test_topk_select_boundary_bin_past_shared_memory(cuda_device, L, K):
+    """More equal scores at the K-th place than the kernel's shared-memory
+    list holds (its radix select then reads the row again from global
+    memory): still the smallest ids among the ties, in order."""
+    rng = np.random.default_rng(L)
+    scores = np.zeros((3, L))
+    scores[2, rng.integers(0, L, 500)] = 1.0  # a few larger scores ahead of the ties
+    _topk_vs_oracle(cuda_device, scores, [L, L // 2, L], K, f"ties past shared memory L={L}")
+
+
 def test_topk_select_nan_and_signed_zero(cuda_device):
     """NaN ranks below every number (-inf included) and -0 ties with +0."""
     row = np.array([0.0, -0.0, np.nan, 1.5, -np.inf, np.nan, -0.0, 2.0, np.inf, -1.0], np.float64)
