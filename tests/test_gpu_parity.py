@@ -479,6 +479,23 @@ def test_merge_random_vs_oracle(cuda_device, D):
     compare_out_lse(out, lse, ref_out, ref_lse, where=f"merge D={D}")
 
 
+@pytest.mark.parametrize("D,T", [(4, 40), (8, 20), (16, 10)])
+def test_merge_more_rows_than_warps(cuda_device, D, T):
+    """Thousands of (token, head) rows at D = 4, 8 and 16: every CTA of the
+    merge grid, the last one partly filled, and an empty row at the end."""
+    dev = cuda_device
+    H = 128
+    g = torch.Generator(device=dev).manual_seed(100 + D)
+    outs = [torch.randn((T, H, 512), generator=g, device=dev).to(torch.bfloat16)
+            for _ in range(D)]
+    lses = [torch.randn((T, H), generator=g, device=dev) * 3 for _ in range(D)]
+    lses[D - 1][T - 1] = -math.inf
+    out, lse = capi.dcp_lse_merge(outs, lses)
+    ref_out, ref_lse = oracle.lse_merge([oracle.compare.to_f64(x) for x in outs],
+                                        [oracle.compare.to_f64(x) for x in lses])
+    compare_out_lse(out, lse, ref_out, ref_lse, where=f"merge D={D} T={T}")
+
+
 # ---------------------------------------------------------------- spec decode
 def test_spec_decode_rows_equal_single_token_calls(cuda_device):
     """The MTP step's batched rows (b*2 + s) equal per-token calls."""
