@@ -257,6 +257,18 @@ def build_shard(ctx: np.ndarray, D: int, d: int, block_size: int,
     return Shard(pool=pool, block_table=bt, width=width, live_rows=n_live)
 
 
+def draw_topk(spec: WorkloadSpec, ctx: np.ndarray, rng: np.random.Generator) -> np.ndarray:
+    """The top-k rows of every query token, in row order (b * S + s): token s
+    of request b sits at position ctx[b] - S + s and its ids are <= it."""
+    S = spec.tokens_per_req
+    topk = np.empty((spec.num_tokens, spec.topk), dtype=np.int32)
+    for b in range(spec.num_reqs):
+        for s in range(S):
+            pos = int(ctx[b]) - S + s  # query position; top-k ids <= pos
+            topk[b * S + s] = draw_topk_row(rng, pos + 1, spec.topk, spec.neg_frac)
+    return topk
+
+
 def make_workload(spec: WorkloadSpec | str, seed: int = 0, device="cpu",
                   row_stride_pad: int = 0, ctx_override: Optional[Sequence[int]] = None
                   ) -> Workload:
@@ -275,11 +287,7 @@ def make_workload(spec: WorkloadSpec | str, seed: int = 0, device="cpu",
     S = spec.tokens_per_req
     T = spec.num_tokens
     req_id = np.repeat(np.arange(spec.num_reqs, dtype=np.int32), S)
-    topk = np.empty((T, spec.topk), dtype=np.int32)
-    for b in range(spec.num_reqs):
-        for s in range(S):
-            pos = int(ctx[b]) - S + s  # query position; top-k ids <= pos
-            topk[b * S + s] = draw_topk_row(rng, pos + 1, spec.topk, spec.neg_frac)
+    topk = draw_topk(spec, ctx, rng)
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     shards = [build_shard(ctx, spec.dcp, d, spec.block_size, spec.spare_frac,
