@@ -106,6 +106,13 @@ constexpr int kOffCtl = kOffListShard + kMaxList;
 constexpr int kCtlBytes = 1024;
 constexpr int kSmemBytes = kOffCtl + kCtlBytes + 1024;  // + control block + alignment slack
 
+// Per shard: its staged block-table row's offset in the staging area, the
+// row's meaningful columns and the pool's slot count (one 16-byte read).
+struct __align__(16) ShardMeta {
+  int32_t bt_off, bt_width;
+  int64_t pool_slots;
+};
+
 struct Ctl {
   uint64_t q_tma, q_ready, full[kStages], freed[kStages], raw_full[kRawStages], raw_empty[kRawStages],
       s_full, s_free, pv_done, xa[2], xb[2], end, end_pv;
@@ -117,9 +124,7 @@ struct Ctl {
   // fused step: per shard, its pool and this row's request row of its table
   const uint8_t* pool[kMaxMerge];
   const int32_t* bt_row[kMaxMerge];
-  int64_t pool_slots[kMaxMerge];
-  int32_t bt_width[kMaxMerge];
-  int32_t bt_off[kMaxMerge];  // each shard's staged block-table row in the prologue
+  ShardMeta meta[kMaxMerge];
   int bt_staged;              // the rows fit the staging area
 };
 static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
@@ -975,8 +980,8 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
 // false for -1 / foreign / invalid entries, recording input errors in `err`.
 template <int kMode>
 __device__ __forceinline__ bool resolve_entry(const DecodeArgs& a, const Ctl* ctl, const int32_t* bt,
-                                              bool req_ok, int32_t limit, int32_t v, int32_t& slot,
-                                              int& shard, unsigned& err) {
+                                              bool staged, bool req_ok, int32_t limit, int32_t v,
+                                              int32_t& slot, int& shard, unsigned& err) {
   if (kMode == kModeSlots) {
     if (v >= a.num_slots) {
       err |= SMLA_DEVERR_SLOT_RANGE;
@@ -986,37 +991,33 @@ __device__ __forceinline__ bool resolve_entry(const DecodeArgs& a, const Ctl* ct
     shard = 0;
     return v >= 0;
   }
-  if (v < 0 || !req_ok) return false;
-  if (kMode == kModeDense && v >= limit) return false;
+  // Pools: every entry takes the same straight-line path (no branch per
+  // check), so the 16 entries of a thread overlap their shared-memory reads.
+  const bool live = v >= 0 && req_ok && !(kMode == kModeDense && v >= limit);
+  const int32_t vv = live ? v : 0;
   int d;
   int32_t lp;
   if (kMode == kModeDense && a.dense_rank >= 0) {
     d = a.dense_rank;
-    lp = v;
+    lp = vv;
   } else {
-    const uint32_t g = fastdiv(uint32_t(v), a.div_I);  // run of I positions
-    const uint32_t round = fastdiv(g, a.div_D);        // round of D runs
+    const uint32_t g = fastdiv(uint32_t(vv), a.div_I);  // run of I positions
+    const uint32_t round = fastdiv(g, a.div_D);         // round of D runs
     d = int(g - round * uint32_t(a.D));
-    lp = int32_t(round) * a.interleave + (v - int32_t(g) * a.interleave);
+    lp = int32_t(round) * a.interleave + (vv - int32_t(g) * a.interleave);
   }
+  const ShardMeta m = ctl->meta[d];
   const int32_t col = int32_t(fastdiv(uint32_t(lp), a.div_bs));
-  if (col >= ctl->bt_width[d]) {
-    err |= SMLA_DEVERR_BLOCK_TABLE;
-    return false;
-  }
-  const int32_t blk = ctl->bt_staged ? bt[ctl->bt_off[d] + col] : __ldg(ctl->bt_row[d] + col);
-  if (blk < 0) {
-    err |= SMLA_DEVERR_BLOCK_TABLE;
-    return false;
-  }
+  const bool in_table = col < m.bt_width;
+  const int32_t colc = in_table ? col : 0;  // every table has a column 0
+  const int32_t blk = staged ? bt[m.bt_off + colc] : __ldg(ctl->bt_row[d] + colc);
   const int64_t s64 = int64_t(blk) * a.block_size + (lp - col * a.block_size);
-  if (s64 >= ctl->pool_slots[d]) {
-    err |= SMLA_DEVERR_SLOT_RANGE;
-    return false;
-  }
+  const bool in_pool = s64 < m.pool_slots;
+  err |= (live && (!in_table || blk < 0)) ? unsigned(SMLA_DEVERR_BLOCK_TABLE) : 0u;
+  err |= (live && in_table && blk >= 0 && !in_pool) ? unsigned(SMLA_DEVERR_SLOT_RANGE) : 0u;
   slot = int32_t(s64);
   shard = d;
-  return true;
+  return live && in_table && blk >= 0 && in_pool;
 }
 
 // Dense decode: the request of row t and the bound on its raw entries (its
@@ -1095,21 +1096,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // q lands in the (still idle) operand stages while the CTA sets up
     issue_q_tma(a, t, hr.c, smem_u32(sm + kOffOp), &ctl->q_tma);
   }
+  // The converter warps' raw entries (their 16 each of the row's split, see
+  // the compaction below) are loaded before the set-up barrier, so that
+  // their memory round trip overlaps the request id's.
+  constexpr int kPer = kMaxList / 128;
+  int32_t vs[kPer];
+  if (kMode != kModeDense && warp >= 4 && warp < 8) {
+    const int j0 = e_begin + (tid - 128) * kPer;
+    const int32_t* src = (kMode == kModeTopk ? a.topk : a.slots) + t * a.K;
+    if (j0 + kPer <= e_end && (reinterpret_cast<uintptr_t>(src + j0) & 15u) == 0) {
+#pragma unroll
+      for (int q4 = 0; q4 < kPer / 4; ++q4) {
+        const int4 w = __ldg(reinterpret_cast<const int4*>(src + j0) + q4);
+        vs[4 * q4] = w.x;
+        vs[4 * q4 + 1] = w.y;
+        vs[4 * q4 + 2] = w.z;
+        vs[4 * q4 + 3] = w.w;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) vs[k] = (j0 + k < e_end) ? __ldg(src + j0 + k) : -1;
+    }
+  }
   if (kPools && tid < a.D) {
     // per-shard pointers of this row's request, read once
     const int32_t r = kMode == kModeDense ? int32_t(t / a.S) : a.req_id[t];
     const bool ok = r >= 0 && r < a.num_reqs;
     ctl->pool[tid] = a.pools[tid];
     ctl->bt_row[tid] = a.bts[tid] + (ok ? int64_t(r) * a.bt_stride[tid] : 0);
-    ctl->pool_slots[tid] = a.pool_slots[tid];
-    ctl->bt_width[tid] = a.bt_width[tid];
   }
   if (kPools && tid == 0) {
     // the request's block-table rows of all shards, staged in the exchange
     // buffers (idle until the tile loop) when they fit
     int off = 0;
     for (int d = 0; d < a.D; ++d) {
-      ctl->bt_off[d] = off;
+      ctl->meta[d].bt_off = off;
+      ctl->meta[d].bt_width = a.bt_width[d];
+      ctl->meta[d].pool_slots = a.pool_slots[d];
       off += a.bt_width[d];
     }
     ctl->bt_staged = off <= kBtStageMax;
@@ -1135,7 +1158,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int d = tid - 128;
     int* list = reinterpret_cast<int*>(sm + kOffList);
     uint8_t* list_shard = sm + kOffListShard;
-    constexpr int kPer = kMaxList / 128;
     unsigned err = 0;
     bool req_ok = true;
     int32_t limit = 0;
@@ -1149,38 +1171,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       req_ok = dense_row(a, t, r, limit, e2);
       if (d == 0) err |= e2;
     }
-    // 1) this thread's 16 raw entries, all loads in flight at once (four
-    //    16-byte loads when the row allows; a dense row's entries are just
-    //    their indices), and, with D pools, the request's block-table rows
-    //    copied into shared memory by all 128 threads; one memory round trip
-    //    for both
+    // 1) this thread's 16 raw entries (loaded before the set-up barrier,
+    //    four 16-byte loads when the row allows; a dense row's entries are
+    //    just their indices), and, with D pools, the request's block-table
+    //    rows copied into shared memory by all 128 threads
     const int j0 = e_begin + d * kPer;
-    const int32_t* src = (kMode == kModeTopk ? a.topk : a.slots) + t * a.K;
-    int32_t vs[kPer];
     if (kMode == kModeDense) {
 #pragma unroll
       for (int k = 0; k < kPer; ++k) vs[k] = j0 + k;
-    } else if (j0 + kPer <= e_end && (reinterpret_cast<uintptr_t>(src + j0) & 15u) == 0) {
-#pragma unroll
-      for (int q4 = 0; q4 < kPer / 4; ++q4) {
-        const int4 w = __ldg(reinterpret_cast<const int4*>(src + j0) + q4);
-        vs[4 * q4] = w.x;
-        vs[4 * q4 + 1] = w.y;
-        vs[4 * q4 + 2] = w.z;
-        vs[4 * q4 + 3] = w.w;
-      }
-    } else {
-#pragma unroll
-      for (int k = 0; k < kPer; ++k) vs[k] = (j0 + k < e_end) ? __ldg(src + j0 + k) : -1;
     }
     int32_t* bt = reinterpret_cast<int32_t*>(sm + kOffX);
-    if (kPools && ctl->bt_staged) {
+    const bool staged = kPools && ctl->bt_staged;
+    if (staged) {
       const uint32_t bt0 = smem_u32(bt);
 #pragma unroll 1
       for (int sd = 0; sd < a.D; ++sd) {
 #pragma unroll 1
-        for (int col = d; col < ctl->bt_width[sd]; col += 128)
-          cp_async_4(bt0 + 4u * uint32_t(ctl->bt_off[sd] + col), ctl->bt_row[sd] + col);
+        for (int col = d; col < ctl->meta[sd].bt_width; col += 128)
+          cp_async_4(bt0 + 4u * uint32_t(ctl->meta[sd].bt_off + col), ctl->bt_row[sd] + col);
       }
       cp_async_commit();
       cp_async_wait<0>();
@@ -1194,8 +1202,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int32_t v = vs[k];
       vs[k] = -1;
       shards[k] = 0;
-      if (j0 + k < e_end && resolve_entry<kMode>(a, ctl, bt, req_ok, limit, v, vs[k], shards[k], err))
-        keep |= 1u << k;
+      const bool ok = resolve_entry<kMode>(a, ctl, bt, staged, req_ok, limit,
+                                           j0 + k < e_end ? v : -1, vs[k], shards[k], err);
+      keep |= unsigned(ok) << k;
     }
     const int cnt = __popc(keep);
     int incl = cnt;  // inclusive warp scan
