@@ -120,7 +120,7 @@ struct Ctl {
   int n_list;
   int abort;
   int is_last;
-  int warp_cnt[8];
+  int warp_cnt[8];  // the compacting warps' valid counts
   // fused step: per shard, its pool and this row's request row of its table
   const uint8_t* pool[kMaxMerge];
   const int32_t* bt_row[kMaxMerge];
@@ -1096,12 +1096,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // q lands in the (still idle) operand stages while the CTA sets up
     issue_q_tma(a, t, hr.c, smem_u32(sm + kOffOp), &ctl->q_tma);
   }
-  // The converter warps' raw entries (their 16 each of the row's split, see
-  // the compaction below) are loaded before the set-up barrier, so that
-  // their memory round trip overlaps the request id's.
-  constexpr int kPer = kMaxList / 128;
+  // The compacting warps' raw entries (kPer each of the row's split, see the
+  // compaction below) are loaded before the set-up barrier, so that their
+  // memory round trip overlaps the request id's.
+  constexpr int kListThreads = kThreads - 128;  // every warp but the softmax warps
+  constexpr int kPer = kMaxList / kListThreads;
   int32_t vs[kPer];
-  if (kMode != kModeDense && warp >= 4 && warp < 8) {
+  if (kMode != kModeDense && warp >= 4) {
     const int j0 = e_begin + (tid - 128) * kPer;
     const int32_t* src = (kMode == kModeTopk ? a.topk : a.slots) + t * a.K;
     if (j0 + kPer <= e_end && (reinterpret_cast<uintptr_t>(src + j0) & 15u) == 0) {
@@ -1149,12 +1150,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       atomicOr(&g_decode_error, SMLA_DEVERR_RANGE);
     tc_fence_before();
     mbar_arrive(&ctl->q_ready);
-  } else if (warp < 8) {
-    // Ordered compaction of the split's valid entries: thread d owns the
-    // contiguous entries [e_begin + 16d, e_begin + 16d + 16), resolves them
-    // with all loads in flight at once, and a block scan gives each thread
-    // its output offset.  Both CTAs of the pair build the same list, so
-    // their tiles hold the same keys.
+  } else {
+    // Ordered compaction of the split's valid entries by the 256 threads of
+    // warps 4-11 (idle until the tile loop): thread d owns the contiguous
+    // entries [e_begin + 8d, e_begin + 8d + 8), resolves them with all loads
+    // in flight at once, and a block scan gives each thread its output
+    // offset.  Both CTAs of the pair build the same list, so their tiles hold
+    // the same keys.
     const int d = tid - 128;
     int* list = reinterpret_cast<int*>(sm + kOffList);
     uint8_t* list_shard = sm + kOffListShard;
@@ -1171,10 +1173,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       req_ok = dense_row(a, t, r, limit, e2);
       if (d == 0) err |= e2;
     }
-    // 1) this thread's 16 raw entries (loaded before the set-up barrier,
+    // 1) this thread's kPer raw entries (loaded before the set-up barrier,
     //    four 16-byte loads when the row allows; a dense row's entries are
     //    just their indices), and, with D pools, the request's block-table
-    //    rows copied into shared memory by all 128 threads
+    //    rows copied into shared memory by all the compacting threads
     const int j0 = e_begin + d * kPer;
     if (kMode == kModeDense) {
 #pragma unroll
@@ -1187,12 +1189,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int sd = 0; sd < a.D; ++sd) {
 #pragma unroll 1
-        for (int col = d; col < ctl->meta[sd].bt_width; col += 128)
+        for (int col = d; col < ctl->meta[sd].bt_width; col += kListThreads)
           cp_async_4(bt0 + 4u * uint32_t(ctl->meta[sd].bt_off + col), ctl->bt_row[sd] + col);
       }
       cp_async_commit();
       cp_async_wait<0>();
-      named_bar_sync(3, 128);  // every thread's copies are visible
+      named_bar_sync(3, kListThreads);  // every thread's copies are visible
     }
     // 2) resolve the 16 entries from registers and shared memory
     int shards[kPer];
@@ -1214,10 +1216,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane >= off) incl += y;
     }
     if (lane == 31) ctl->warp_cnt[warp - 4] = incl;
-    named_bar_sync(3, 128);
+    named_bar_sync(3, kListThreads);
     int wbase = 0, total = 0;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
+    for (int w = 0; w < kListThreads / 32; ++w) {
       const int x = ctl->warp_cnt[w];
       wbase += (w < warp - 4) ? x : 0;
       total += x;
