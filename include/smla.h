@@ -187,6 +187,13 @@ size_t smla_decode_workspace_size(int32_t T, int32_t H, int32_t K);
  *               that sets SMLA_DEVERR_TIMEOUT, leaves its arrival counters
  *               zero again); may be NULL when that size is 0.  Calls that
  *               run concurrently need distinct workspaces.
+ * When the size is not 0 the rows are split over several key ranges
+ * (split-K) and each range's partial goes through the workspace.  The
+ * partials are merged by their LSE in the decode kernel (the last range of
+ * a row to finish merges it) when the decode grid is larger than one wave
+ * on the GPU or there are fewer than four ranges per row; otherwise by a
+ * second kernel launched on `stream` with programmatic stream
+ * serialisation.  Without split-K the call is a single kernel launch.
  * Errors: INVALID_ARG for null pointers, T < 0, K < 1, H < 1, num_slots < 0,
  * sm_scale not finite and positive, misaligned q/kv_cache/out; UNSUPPORTED
  * for H > SMLA_MAX_HEADS; WORKSPACE
@@ -228,7 +235,9 @@ smla_status smla_sparse_mla_decode_noalloc(
     float sm_scale, uint16_t* out, float* lse, void* stream);
 
 /*
- * Steps 1-3 in one launch (fused DCP step for D shards held by one GPU).
+ * Steps 1-3 in one launch (fused DCP step for D shards held by one GPU; with
+ * split-K, a second launch may merge the key ranges, as for
+ * smla_sparse_mla_decode).
  *
  * Computes exactly what the three calls above compute for D shard pools --
  * filter + convert per shard, sparse MLA decode per shard, LSE merge -- in a

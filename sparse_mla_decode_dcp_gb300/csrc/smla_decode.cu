@@ -133,6 +133,15 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Programmatic dependent launch: a grid launched after this one with
+// programmatic stream serialisation may be scheduled once every CTA here has
+// signalled (or exited); it waits for this grid's completion and memory in
+// griddepcontrol.wait.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -462,12 +471,14 @@ __device__ void convert_loop(Ctl* ctl, uint8_t* sm, int n, int ntiles, int key, 
   if (out_of_range) atomicOr(&g_decode_error, SMLA_DEVERR_RANGE);
 }
 
-// Split-K epilogue: write this split's unnormalised O half, its log2-domain
-// reference maximum and its sum; the last split of the row to arrive (per
-// value half) combines all of them and resets the row's arrival counter.
-// A split whose CTA gave up on a wait (`ok` false, SMLA_DEVERR_TIMEOUT set)
-// still arrives, contributing nothing, so the counter always returns to zero
-// and the workspace stays valid for the next call.
+// Split-K epilogue (softmax warps): write this split's unnormalised O half,
+// its log2-domain reference maximum and its sum (-inf and 0 when it holds
+// no partial).  With the in-kernel combine the split then counts itself in:
+// the CTA whose split arrives last for its row and value half learns so in
+// `ctl->is_last` and combines the row once all its warps are free (see
+// combine_splits).  A split whose CTA gave up on a wait (`ok` false,
+// SMLA_DEVERR_TIMEOUT set) still arrives, contributing nothing, so the
+// counter always completes and the workspace stays valid for the next call.
 __device__ void split_epilogue(const DecodeArgs& a, Ctl* ctl, int C, int64_t t, int split, int ntiles,
                                float m_ref, float l, uint32_t tb, int warp, int h, bool ok) {
   const int S = a.splits;
@@ -494,67 +505,168 @@ __device__ void split_epilogue(const DecodeArgs& a, Ctl* ctl, int C, int64_t t, 
     ml[h] = has ? m_ref : -INFINITY;
     ml[a.H + h] = has ? l : 0.f;
   }
+  if (!a.combine_in_kernel) {  // split_combine_kernel merges after this grid
+    if (h == 0) ctl->is_last = 0;
+    return;
+  }
   __threadfence();
   named_bar_sync(2, 128);
   if (h == 0) ctl->is_last = (atomicAdd(a.ws_tick + t * 2 + C, 1) == S - 1);
-  named_bar_sync(2, 128);
-  if (!ctl->is_last) return;
+}
+
+// Split-K combine of one row's value half, run by all 384 threads of the CTA
+// whose split arrived last, after the roles have finished (TMEM released,
+// the peer no longer writing into this CTA's shared memory).  With m_s and
+// l_s the splits' log2-domain maxima and sums, M = max m_s over the splits
+// that hold a partial, L = sum l_s 2^(m_s - M), out = sum 2^(m_s - M) O_s / L
+// and LSE = (M + log2 L) ln 2: the same split merge as across shards, here
+// over the key ranges of one shard.
+//
+// A split holds a partial for every head or for none (a split with a valid
+// key has l >= 1 for each head: its largest key contributes 2^0), so the
+// non-empty splits are listed once, from head 0's sums.  Each thread owns
+// fixed float4 columns of the output (a warp covers 512 contiguous bytes of
+// one head row) and accumulates them over the listed splits with independent
+// loads, 11 columns per pass, two passes; the per-(split, head) weights sit
+// in the operand stages, per head M and 1 / L beside the exchange buffers.
+// Splits are taken kCombChunk at a time.  The sums run in split order, as
+// the per-head M and L do.
+constexpr int kCombItems = 11;                                      // float4 columns per pass
+constexpr int kCombChunk = (kStages * kOpTileBytes) / (128 * 4);  // splits whose weights fit
+static_assert(2 * kCombItems * kThreads >= 128 * (SMLA_V_DIM / 2) / 4, "two passes cover a value half");
+static_assert(kCombChunk * 4 + 1024 + 16 <= 2 * kXBytes, "split list and head stats fit");
+
+__device__ void combine_splits(const DecodeArgs& a, uint8_t* sm, int C, int64_t t) {
+  const int S = a.splits;
+  const int H = a.H;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  float* s_m = reinterpret_cast<float*>(sm + kOffX);  // per head: M
+  float* s_inv = s_m + 128;                           // per head: 1 / L (0 when empty)
+  int* s_n = reinterpret_cast<int*>(s_m + 256);       // listed splits in this chunk
+  int* s_list = s_n + 4;                              // the non-empty splits of the chunk
+  float* s_w = reinterpret_cast<float*>(sm + kOffOp); // [listed split][head] weights
+  const float* ml_row = a.ws_ml + (t * S * 2 + C) * 2 * H;  // split sp at + sp * 4H
   __threadfence();
-  if (live) {
+  if (tid < H) {
+    const float* ms = ml_row + tid;
     float M = -INFINITY;
-    for (int sp = 0; sp < S; ++sp) {
-      const float* mls = a.ws_ml + ((t * S + sp) * 2 + C) * 2 * a.H;
-      const float ms = __ldcg(mls + h), ls = __ldcg(mls + a.H + h);
-      if (ls != 0.f && (ms > M || ms != ms)) M = ms;  // NaN propagates
+    int sp = 0;
+    for (; sp + 8 <= S; sp += 8) {
+      float m8[8], l8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        m8[k] = __ldcg(ms + int64_t(sp + k) * 4 * H);
+        l8[k] = __ldcg(ms + int64_t(sp + k) * 4 * H + H);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (l8[k] != 0.f && (m8[k] > M || m8[k] != m8[k])) M = m8[k];  // NaN propagates
     }
-    uint4* dst = reinterpret_cast<uint4*>(a.out + (t * a.H + h) * SMLA_V_DIM + C * 256);
-    if (M == -INFINITY) {
-#pragma unroll 1
-      for (int k = 0; k < 32; ++k) dst[k] = make_uint4(0, 0, 0, 0);
-      if (C == 0) a.lse[t * a.H + h] = -INFINITY;
-    } else {
-      float L = 0.f;
-      for (int sp = 0; sp < S; ++sp) {
-        const float* mls = a.ws_ml + ((t * S + sp) * 2 + C) * 2 * a.H;
-        const float ls = __ldcg(mls + a.H + h);
-        if (ls != 0.f) L += ls * ex2(__ldcg(mls + h) - M);
+    for (; sp < S; ++sp) {
+      const float m1 = __ldcg(ms + int64_t(sp) * 4 * H), l1 = __ldcg(ms + int64_t(sp) * 4 * H + H);
+      if (l1 != 0.f && (m1 > M || m1 != m1)) M = m1;
+    }
+    float L = 0.f;
+    if (M != -INFINITY) {
+      sp = 0;
+      for (; sp + 8 <= S; sp += 8) {
+        float m8[8], l8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          m8[k] = __ldcg(ms + int64_t(sp + k) * 4 * H);
+          l8[k] = __ldcg(ms + int64_t(sp + k) * 4 * H + H);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (l8[k] != 0.f) L += l8[k] * ex2(m8[k] - M);
       }
-      const float invL = 1.f / L;
+      for (; sp < S; ++sp) {
+        const float l1 = __ldcg(ms + int64_t(sp) * 4 * H + H);
+        if (l1 != 0.f) L += l1 * ex2(__ldcg(ms + int64_t(sp) * 4 * H) - M);
+      }
+    }
+    s_m[tid] = M;
+    s_inv[tid] = (M == -INFINITY) ? 0.f : 1.f / L;
+    if (C == 0) a.lse[t * H + tid] = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
+  }
+  const int n_items = H * (SMLA_V_DIM / 2) / 4;  // float4 columns of the value half
+  const int n_chunks = (S + kCombChunk - 1) / kCombChunk;
+  const float* o_row = a.ws_o + t * S * H * SMLA_V_DIM + C * 256;
 #pragma unroll 1
-      for (int cc = 0; cc < 8; ++cc) {
-        float acc[32];
+  for (int pass = 0; pass < 2; ++pass) {
+    const int it0 = pass * kCombItems * kThreads + tid;
+    if (pass * kCombItems * kThreads >= n_items) break;  // uniform
+    int32_t off[kCombItems];  // float offset of the column in a split's O rows (head = off / 512)
 #pragma unroll
-        for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-        for (int sp = 0; sp < S; ++sp) {
-          const float* mls = a.ws_ml + ((t * S + sp) * 2 + C) * 2 * a.H;
-          const float ls = __ldcg(mls + a.H + h);
-          if (ls == 0.f) continue;
-          const float w = ex2(__ldcg(mls + h) - M) * invL;
-          const float4* src = reinterpret_cast<const float4*>(
-              a.ws_o + ((t * S + sp) * a.H + h) * SMLA_V_DIM + C * 256 + cc * 32);
+    for (int k = 0; k < kCombItems; ++k) {
+      const int it = it0 + k * kThreads;
+      const int itc = it < n_items ? it : 0;
+      off[k] = (itc >> 6) * SMLA_V_DIM + (itc & 63) * 4;
+    }
+    float4 acc[kCombItems];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float4 v = __ldcg(src + k);
-            acc[4 * k] = fmaf(w, v.x, acc[4 * k]);
-            acc[4 * k + 1] = fmaf(w, v.y, acc[4 * k + 1]);
-            acc[4 * k + 2] = fmaf(w, v.z, acc[4 * k + 2]);
-            acc[4 * k + 3] = fmaf(w, v.w, acc[4 * k + 3]);
+    for (int k = 0; k < kCombItems; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+    for (int ch = 0; ch < n_chunks; ++ch) {
+      const int sp0 = ch * kCombChunk;
+      if (pass == 0 || n_chunks > 1) {
+        __syncthreads();  // head stats written; the previous chunk's list and weights consumed
+        if (warp == 0) {
+          // non-empty splits of the chunk, in split order
+          const int sp_end = min(S, sp0 + kCombChunk);
+          int cnt = 0;
+          for (int sb = sp0; sb < sp_end; sb += 32) {
+            const int sp = sb + lane;
+            const bool ne = sp < sp_end && __ldcg(ml_row + int64_t(sp) * 4 * H + H) != 0.f;
+            const unsigned m = __ballot_sync(0xffffffffu, ne);
+            if (ne) s_list[cnt + __popc(m & ((1u << lane) - 1u))] = sp;
+            cnt += __popc(m);
           }
+          if (lane == 0) *s_n = cnt;
         }
-        uint32_t o[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          __nv_bfloat162 v = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
-          o[j] = *reinterpret_cast<uint32_t*>(&v);
+        __syncthreads();
+        const int n = *s_n;
+        for (int idx = tid; idx < n * H; idx += kThreads) {
+          const int j = idx / H;
+          const int hh = idx - j * H;
+          const float* p = ml_row + int64_t(s_list[j]) * 4 * H + hh;
+          const float m1 = __ldcg(p), l1 = __ldcg(p + H);
+          s_w[idx] = (l1 != 0.f) ? ex2(m1 - s_m[hh]) * s_inv[hh] : 0.f;
         }
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          dst[cc * 4 + k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+        __syncthreads();
       }
-      if (C == 0) a.lse[t * a.H + h] = (M + log2f(L)) * kLn2;
+      const int n = *s_n;
+#pragma unroll 1
+      for (int j = 0; j < n; ++j) {
+        const float* src = o_row + int64_t(s_list[j]) * H * SMLA_V_DIM;
+        const float* wj = s_w + j * H;
+#pragma unroll
+        for (int k = 0; k < kCombItems; ++k) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(src + off[k]));
+          const float w = wj[off[k] >> 9];
+          acc[k].x = fmaf(w, v.x, acc[k].x);
+          acc[k].y = fmaf(w, v.y, acc[k].y);
+          acc[k].z = fmaf(w, v.z, acc[k].z);
+          acc[k].w = fmaf(w, v.w, acc[k].w);
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kCombItems; ++k) {
+      const int it = it0 + k * kThreads;
+      if (it < n_items) {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc[k].x, acc[k].y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(acc[k].z, acc[k].w);
+        uint2 o;
+        o.x = *reinterpret_cast<uint32_t*>(&lo);
+        o.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(a.out + (t * H + (it >> 6)) * SMLA_V_DIM + C * 256 + (it & 63) * 4) = o;
+      }
     }
   }
-  if (h == 0) a.ws_tick[t * 2 + C] = 0;
+  if (tid == 0) a.ws_tick[t * 2 + C] = 0;
 }
 
 // Store 8 q loads (64 dims) as fp16 pairs into 32 (or 16) TMEM columns.
@@ -1067,6 +1179,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int e_end = min(a.K, e_begin + per_split);
 
   const HalfRt hr = half_of(c);
+  // a separate split combine (if any) may be scheduled on SMs this grid
+  // leaves idle
+  griddep_launch_dependents();
   if (warp == kMmaWarp) {
     tmem_alloc(&ctl->tbase, kTmemCols);
     tmem_relinquish();
@@ -1250,6 +1365,121 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(ctl->tbase, kTmemCols);
   }
+  if (a.splits > 1 && ctl->is_last) combine_splits(a, sm, hr.c, t);
+}
+
+// Split-K combine of one row's value half for eight heads, one warp per
+// head, launched after the decode grid with programmatic stream
+// serialisation.  With m_s and l_s the splits' log2-domain maxima and sums,
+// M = max m_s over the splits that hold a partial (l_s != 0), L = sum l_s
+// 2^(m_s - M), out = sum_s 2^(m_s - M) O_s / L, LSE = (M + log2 L) ln 2: the
+// merge of "partial attention results" by their LSE, here over the key ranges
+// of one row.  A row whose splits all hold nothing comes out as the merge
+// identity (0, -inf).  Lanes own float4 columns lane and lane + 32 of the
+// head's value half (two 512-byte coalesced reads per split) and take the
+// splits in ascending order, eight at a time, each load independent.
+constexpr int kCombHeads = 8;
+
+__device__ __forceinline__ float max_nan(float x, float y) {
+  return (x != x || y != y) ? __int_as_float(0x7fc00000) : fmaxf(x, y);
+}
+
+__global__ void __launch_bounds__(kCombHeads * 32)
+    split_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_ml,
+                         uint16_t* __restrict__ out, float* __restrict__ lse, int32_t H, int32_t S) {
+  griddep_wait();  // the decode grid's partials are complete and visible
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = (H + kCombHeads - 1) / kCombHeads;
+  const int64_t t = blockIdx.x / (2 * G);
+  const int r = int(blockIdx.x - t * 2 * G);
+  const int C = r / G;
+  const int h = (r - C * G) * kCombHeads + warp;
+  if (h >= H) return;
+  const int64_t ml_stride = 4 * int64_t(H);  // floats from one split's stats to the next
+  const float* ml = ws_ml + (t * S * 2 + C) * 2 * int64_t(H) + h;  // split sp: m at sp * 4H, l at + H
+  float M = -INFINITY;
+  for (int sp = lane; sp < S; sp += 32) {
+    const float m1 = __ldcg(ml + sp * ml_stride), l1 = __ldcg(ml + sp * ml_stride + H);
+    if (l1 != 0.f) M = max_nan(M, m1);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = max_nan(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float L = 0.f;
+  if (M != -INFINITY) {
+    for (int sp = lane; sp < S; sp += 32) {
+      const float m1 = __ldcg(ml + sp * ml_stride), l1 = __ldcg(ml + sp * ml_stride + H);
+      if (l1 != 0.f) L += l1 * ex2(m1 - M);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  }
+  const float inv = (M == -INFINITY) ? 0.f : 1.f / L;
+  const float4* o_row =
+      reinterpret_cast<const float4*>(ws_o + (t * S * H + h) * SMLA_V_DIM + C * 256) + lane;
+  const int64_t o_stride = int64_t(H) * SMLA_V_DIM / 4;  // float4s from one split's row to the next
+  float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+  for (int base = 0; base < S; base += 32) {
+    const int sp = base + lane;
+    float m1 = 0.f, l1 = 0.f;
+    if (sp < S) {
+      m1 = __ldcg(ml + sp * ml_stride);
+      l1 = __ldcg(ml + sp * ml_stride + H);
+    }
+    const bool held = l1 != 0.f;  // this split wrote its partial
+    const float w_lane = held ? ex2(m1 - M) * inv : 0.f;
+    unsigned mask = __ballot_sync(0xffffffffu, held);
+    while (mask) {
+      int idx[8];
+      float w[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        idx[k] = mask ? __ffs(mask) - 1 : -1;
+        w[k] = __shfl_sync(0xffffffffu, w_lane, idx[k] < 0 ? 0 : idx[k]);
+        mask &= mask - 1u;
+      }
+      float4 v0[8], v1[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float4* src = o_row + (base + (idx[k] < 0 ? idx[0] : idx[k])) * o_stride;
+        v0[k] = __ldcg(src);
+        v1[k] = __ldcg(src + 32);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (idx[k] >= 0) {
+          a0.x = fmaf(w[k], v0[k].x, a0.x);
+          a0.y = fmaf(w[k], v0[k].y, a0.y);
+          a0.z = fmaf(w[k], v0[k].z, a0.z);
+          a0.w = fmaf(w[k], v0[k].w, a0.w);
+          a1.x = fmaf(w[k], v1[k].x, a1.x);
+          a1.y = fmaf(w[k], v1[k].y, a1.y);
+          a1.z = fmaf(w[k], v1[k].z, a1.z);
+          a1.w = fmaf(w[k], v1[k].w, a1.w);
+        }
+      }
+    }
+  }
+  auto pack = [](float4 v) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+    return make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+  };
+  uint2* dst = reinterpret_cast<uint2*>(out + (t * H + h) * SMLA_V_DIM + C * 256) + lane;
+  dst[0] = pack(a0);
+  dst[32] = pack(a1);
+  if (C == 0 && lane == 0) lse[t * H + h] = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
+}
+
+// Which combine merges a row's splits.  The in-kernel one overlaps the CTAs
+// still running, but one CTA reads every split's partial with a bounded
+// number of loads in flight (two rounds of loads per split); the separate
+// kernel spreads the reads over (row, half, 8 heads) CTAs for a fixed cost
+// (its launch and the wait for this grid to drain).  So the separate kernel
+// is taken when the decode grid fits in one wave on the GPU's SMs, whose
+// other SMs then sit idle, and there are at least four splits per row.
+bool combine_in_kernel(int64_t decode_ctas, int splits, int sms) {
+  return decode_ctas > sms || splits < 4;
 }
 
 // Split-K policy, a function of the shape alone: enough clusters to cover the
@@ -1369,8 +1599,26 @@ cudaError_t launch_impl(const DecodeArgs& args, cudaStream_t s) {
   e = ensure_smem_attribute<kMode>(dev);
   if (e != cudaSuccess) return e;
   const int64_t ctas = 2 * int64_t(a.T) * a.splits;
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  a.combine_in_kernel = combine_in_kernel(ctas, a.splits, sms) ? 1 : 0;
   sparse_mla_decode_kernel<kMode><<<dim3(unsigned(ctas)), dim3(kThreads), kSmemBytes, s>>>(a);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e != cudaSuccess || a.splits == 1 || a.T == 0 || a.combine_in_kernel) return e;
+  // the separate split combine, scheduled while the decode grid drains
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(int64_t(a.T) * 2 * ((a.H + kCombHeads - 1) / kCombHeads)));
+  cfg.blockDim = dim3(kCombHeads * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, split_combine_kernel, static_cast<const float*>(a.ws_o),
+                            static_cast<const float*>(a.ws_ml), a.out, a.lse, a.H, a.splits);
 }
 
 }  // namespace

@@ -65,6 +65,7 @@ struct DecodeArgs {
   float* ws_o;       // [T, splits, H, 512] unnormalised partial O
   float* ws_ml;      // [T, splits, 2 halves, 2, H]: log2-domain max, then sum
   int32_t* ws_tick;  // [T, 2] arrival counters, left at zero by every call
+  int32_t combine_in_kernel;  // 1: the last split to arrive merges the row; 0: a second kernel
   // Fused DCP step only (D > 0): global top-k ids are converted per shard in
   // the kernel prologue and all shards' keys share one softmax.
   int32_t D, block_size, num_reqs, interleave;

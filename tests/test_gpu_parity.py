@@ -298,7 +298,7 @@ def test_fused_bad_inputs_masked_and_flagged(cuda_device):
 @pytest.mark.parametrize("K", [64, 2048, 4096])
 def test_fused_small_batches_split_k(cuda_device, K):
     """Few query rows: the fused step splits each row over several clusters
-    and combines the splits in-kernel."""
+    and a second kernel combines the splits."""
     dev = cuda_device
     spec = inputs.WorkloadSpec(
         name="fused_small", num_reqs=3, tokens_per_req=1, heads=128, topk=K, dcp=4,
@@ -516,17 +516,20 @@ def test_spec_decode_rows_equal_single_token_calls(cuda_device):
 
 
 # ------------------------------------------------------- workspace and graphs
-def test_split_k_workspace_reused_across_calls(cuda_device):
+@pytest.mark.parametrize("T,K", [(4, 2048), (40, 4096)])
+def test_split_k_workspace_reused_across_calls(cuda_device, T, K):
     """Split-K arrival counters return to zero after every call, so one
-    workspace serves any number of calls and results repeat bit for bit."""
+    workspace serves any number of calls and results repeat bit for bit.
+    4 rows x 8 key ranges fit one wave (the separate split combine); 40 rows
+    x 2 ranges do not (the in-kernel combine, which counts arrivals)."""
     dev = cuda_device
-    pool = _small_pool(3000, dev, seed=31)
+    pool = _small_pool(5000, dev, seed=31)
     g = torch.Generator(device=dev).manual_seed(1000 + 31)  # independent of the pool
-    T, H, K = 4, 128, 2048
+    H = 128
     assert capi.decode_workspace_size(T, H, K) > 0
     q = torch.randn((T, H, 576), generator=g, device=dev).to(torch.bfloat16)
     rng = np.random.default_rng(31)
-    s = torch.from_numpy(np.stack([rng.choice(3000, K, replace=False)
+    s = torch.from_numpy(np.stack([rng.choice(5000, K, replace=False)
                                    for _ in range(T)]).astype(np.int32)).to(dev)
     ws = capi.alloc_decode_workspace(T, H, K, dev)
     first = capi.sparse_mla_decode(q, pool, s, 0.07, workspace=ws)
@@ -537,6 +540,109 @@ def test_split_k_workspace_reused_across_calls(cuda_device):
         assert torch.equal(o, first[0]) and torch.equal(l, first[1])
     tick = ws[-256:]  # the counters sit in the last 256-byte block
     assert torch.count_nonzero(tick).item() == 0
+    ref_out, ref_lse = oracle.sparse_mla_decode(_q_bits(q), pool.cpu().numpy(),
+                                                s.cpu().numpy(), 0.07)
+    compare_out_lse(first[0], first[1], ref_out, ref_lse, where=f"split-K T={T} K={K}")
+
+
+@pytest.mark.parametrize("T,K", [(2, 1024), (40, 4096)])
+@pytest.mark.parametrize("H", [1, 7, 33, 100])
+def test_split_k_head_counts(cuda_device, H, T, K):
+    """Split-K rows with head counts that leave the separate combine's last
+    8-head group part-empty (2 rows x 4 key ranges) and the in-kernel
+    combine's last columns unused (40 rows x 2 ranges)."""
+    dev = cuda_device
+    pool = _small_pool(5000, dev, seed=50 + H)
+    g = torch.Generator(device=dev).manual_seed(2000 + H)
+    assert capi.decode_workspace_size(T, H, K) > 0
+    q = torch.randn((T, H, 576), generator=g, device=dev).to(torch.bfloat16)
+    rng = np.random.default_rng(50 + H)
+    s = np.stack([rng.choice(5000, K, replace=False) for _ in range(T)]).astype(np.int32)
+    s[1, 300:] = -1  # the later key ranges of row 1 hold nothing
+    _decode_vs_oracle(q, pool, torch.from_numpy(s).to(dev), 0.07, f"split-K H={H} T={T}")
+
+
+def test_split_k_combine_many_key_ranges(cuda_device):
+    """300 key ranges of 2048 entries per row, mostly -1 (a grid of several
+    waves: the in-kernel combine, which takes its per-range weights 288
+    ranges at a time): row 0 has partials in both weight chunks, row 1 only
+    past the first (one in its last range), and the all -1 row comes out as
+    the merge identity."""
+    dev = cuda_device
+    n_pool = 4096
+    pool = _small_pool(n_pool, dev, seed=41)
+    g = torch.Generator(device=dev).manual_seed(1000 + 41)
+    T, H, K = 3, 128, 300 * 2048
+    q = torch.randn((T, H, 576), generator=g, device=dev).to(torch.bfloat16)
+    rng = np.random.default_rng(41)
+    s = np.full((T, K), -1, dtype=np.int32)
+    # row 0: a few keys in every 7th key range
+    for sp in range(0, 300, 7):
+        pos = sp * 2048 + rng.choice(2048, 5, replace=False)
+        s[0, pos] = rng.choice(n_pool, 5, replace=False)
+    # row 1: keys only in key ranges 288.. (the second chunk), one in the last range
+    for sp in (288, 290, 299):
+        pos = sp * 2048 + rng.choice(2048, 40, replace=False)
+        s[1, pos] = rng.choice(n_pool, 40, replace=False)
+    s[1, K - 1] = 17
+    # row 2: no valid entry at all
+    slots = torch.from_numpy(s).to(dev)
+    out, lse = _decode_vs_oracle(q, pool, slots, 0.07, where="split combine over 300 key ranges")
+    assert torch.count_nonzero(out[2]).item() == 0
+    assert torch.isneginf(lse[2]).all()
+
+
+def test_split_k_separate_combine_many_key_ranges(cuda_device):
+    """One row over 76 key ranges (one wave of 152 CTAs: the separate split
+    combine), mostly -1: the combine takes the ranges 32 per lane group
+    (three groups, the last ragged) and the held ones 8 at a time."""
+    dev = cuda_device
+    n_pool = 4096
+    pool = _small_pool(n_pool, dev, seed=43)
+    g = torch.Generator(device=dev).manual_seed(1000 + 43)
+    T, H, K = 1, 128, 40 * 2048
+    q = torch.randn((T, H, 576), generator=g, device=dev).to(torch.bfloat16)
+    rng = np.random.default_rng(43)
+    s = np.full((T, K), -1, dtype=np.int32)
+    per = -(-K // 76)  # entries per key range
+    held = [0, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 31, 32, 40, 63, 64, 70, 75]
+    for sp in held:
+        lo, hi = sp * per, min(K, (sp + 1) * per)
+        pos = lo + rng.choice(hi - lo, 6, replace=False)
+        s[0, pos] = rng.choice(n_pool, 6, replace=False)
+    _decode_vs_oracle(q, pool, torch.from_numpy(s).to(dev), 0.07, where="separate combine, 76 ranges")
+
+
+def test_split_k_decode_replays_in_cuda_graph(cuda_device):
+    """A split-K call -- the decode kernel and the split combine launched
+    programmatically dependent on it -- captured in a CUDA graph replays to
+    the same bits as the call made directly."""
+    dev = cuda_device
+    pool = _small_pool(3000, dev, seed=61)
+    g = torch.Generator(device=dev).manual_seed(1061)
+    T, H, K = 2, 128, 2048
+    q = torch.randn((T, H, 576), generator=g, device=dev).to(torch.bfloat16)
+    rng = np.random.default_rng(61)
+    slots = torch.from_numpy(np.stack([rng.choice(3000, K, replace=False)
+                                       for _ in range(T)]).astype(np.int32)).to(dev)
+    ws = capi.alloc_decode_workspace(T, H, K, dev)
+    assert ws is not None
+    ref_out, ref_lse = capi.sparse_mla_decode(q, pool, slots, 0.07, workspace=ws)
+    ref_out, ref_lse = ref_out.clone(), ref_lse.clone()
+    out = torch.empty_like(ref_out)
+    lse = torch.empty_like(ref_lse)
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            capi.sparse_mla_decode(q, pool, slots, 0.07, out=out, lse=lse, workspace=ws)
+    for _ in range(2):
+        out.fill_(7)
+        lse.fill_(7)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
 
 
 @pytest.mark.parametrize("path", ["fused", "pipeline"])
@@ -700,7 +806,7 @@ def test_dense_decode_matches_oracle(cuda_device, D, S, I):
 
 def test_dense_decode_split_k_long_contexts(cuda_device):
     """Enough rows that the split count is set by the 2048-key list limit and
-    contexts above it: several splits per row, combined in-kernel."""
+    contexts above it: several splits per row, combined by the split merge."""
     dev = cuda_device
     wl, pools, bts, ctx, max_ctx = _dense_case(dev, 40, 2, 2, 1, 2500, 4096, seed=77)
     spec = wl.spec

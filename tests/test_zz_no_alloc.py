@@ -60,7 +60,7 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(cuda_device):
         _within_tolerance(out, lse, ref_out, ref_lse)
         # the same kernel on the same inputs, combining its split-K partials
         # in the same fixed order: the results agree bit for bit, so a scratch
-        # layout or stale-counter mistake cannot hide inside the tolerance
+        # layout mistake cannot hide inside the tolerance
         assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
         assert torch.all(out[3].view(torch.int16) == 0)
 
