@@ -1158,6 +1158,37 @@ __device__ __forceinline__ bool dense_row(const DecodeArgs& a, int64_t t, int32_
   return true;
 }
 
+// A dense split with no position of its row (a short context under a long
+// max_ctx) skips the set-up and publishes what the full path would: the
+// row's (0, -inf) half without split-K, else an empty partial (-inf, 0)
+// that counts in like any other split.  Both CTAs of the pair take this path
+// together (the test depends only on the row and the split); it touches no
+// tensor memory and no peer shared memory.
+__device__ void publish_empty_split(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, int64_t t, int split,
+                                    int C) {
+  const int tid = threadIdx.x;
+  if (a.splits == 1) {
+    for (int idx = tid; idx < a.H * 32; idx += kThreads) {  // 32 x 16 bytes per head half
+      uint4* dst = reinterpret_cast<uint4*>(a.out + (t * a.H + (idx >> 5)) * SMLA_V_DIM + C * 256);
+      dst[idx & 31] = make_uint4(0, 0, 0, 0);
+    }
+    if (C == 0)
+      for (int h = tid; h < a.H; h += kThreads) a.lse[t * a.H + h] = -INFINITY;
+    return;
+  }
+  float* ml = a.ws_ml + ((t * a.splits + split) * 2 + C) * 2 * a.H;
+  for (int h = tid; h < a.H; h += kThreads) {
+    ml[h] = -INFINITY;
+    ml[a.H + h] = 0.f;
+  }
+  if (!a.combine_in_kernel) return;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) ctl->is_last = (atomicAdd(a.ws_tick + t * 2 + C, 1) == a.splits - 1);
+  __syncthreads();
+  if (ctl->is_last) combine_splits(a, sm, C, t);
+}
+
 template <int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     sparse_mla_decode_kernel(const __grid_constant__ DecodeArgs a) {
@@ -1182,6 +1213,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // a separate split combine (if any) may be scheduled on SMs this grid
   // leaves idle
   griddep_launch_dependents();
+  if (kMode == kModeDense) {
+    int32_t r, limit = 0;
+    unsigned e2 = 0;
+    const bool row_ok = dense_row(a, t, r, limit, e2);
+    if (!row_ok || min(e_end, limit) <= e_begin) {
+      if (tid == 0 && e2) atomicOr(&g_decode_error, e2);
+      publish_empty_split(a, sm, ctl, t, split, hr.c);
+      return;
+    }
+  }
   if (warp == kMmaWarp) {
     tmem_alloc(&ctl->tbase, kTmemCols);
     tmem_relinquish();

@@ -804,6 +804,49 @@ def test_dense_decode_matches_oracle(cuda_device, D, S, I):
     assert np.array_equal(oracle.flatten_lse_bhs(lse_bhs), lse.cpu().numpy())
 
 
+def test_dense_decode_skips_empty_key_ranges(cuda_device):
+    """Dense grids of several waves (the in-kernel split combine) whose short
+    rows leave key ranges -- for rank 1 of the shortest, every range --
+    without a position: those splits skip the set-up and publish empty
+    partials, and such a split may be its row's last arrival and combine it.
+    Merged (4 ranges per row) and per rank (2 ranges per row)."""
+    dev = cuda_device
+    rng = np.random.default_rng(91)
+    ctx_fixed = tuple(int(c) for c in np.concatenate(
+        [[2, 2, 3, 4, 5, 1000, 2049, 2050, 2051, 4097, 4098, 8192], rng.integers(2, 8193, 28)]))
+    spec = inputs.WorkloadSpec(
+        name="dense_short_rows", num_reqs=40, tokens_per_req=2, heads=128, topk=64, dcp=2,
+        block_size=64, ctx_kind="fixed", ctx_fixed=ctx_fixed, interleave=1)
+    wl = inputs.make_workload(spec, seed=91, device=dev)
+    pools = [sh.pool for sh in wl.shards]
+    bts = [torch.from_numpy(sh.block_table).to(dev) for sh in wl.shards]
+    ctx = torch.from_numpy(wl.ctx.astype(np.int32)).to(dev)
+    max_ctx = int(wl.ctx.max())
+    q_bits = _q_bits(wl.q)
+    capi.get_device_error(clear=True)
+    refs_o, refs_l = [], []
+    for d in range(2):
+        o, l = capi.dcp_dense_mla_decode(wl.q, ctx, max_ctx, 2, pools, bts, spec.block_size,
+                                         spec.sm_scale, rank=d)
+        torch.cuda.synchronize()
+        ro, rl = oracle.dense_mla_decode(q_bits, wl.shards[d].pool.cpu().numpy(),
+                                         wl.shards[d].block_table, wl.ctx, 2, 2, d,
+                                         spec.block_size, spec.sm_scale)
+        compare_out_lse(o, l, ro, rl, where=f"dense short rows rank {d}")
+        empty = np.isneginf(rl).all(axis=1)
+        if d == 1:
+            assert empty.any()  # token 0 of a context of 2 has only position 0, on rank 0
+        assert torch.all(o[torch.from_numpy(empty).to(dev)].view(torch.int16) == 0)
+        refs_o.append(ro)
+        refs_l.append(rl)
+    out, lse = capi.dcp_dense_mla_decode(wl.q, ctx, max_ctx, 2, pools, bts, spec.block_size,
+                                         spec.sm_scale)
+    torch.cuda.synchronize()
+    assert capi.get_device_error(clear=True) == 0
+    ref_out, ref_lse = oracle.lse_merge(refs_o, refs_l)
+    compare_out_lse(out, lse, ref_out, ref_lse, where="dense short rows merged")
+
+
 def test_dense_decode_split_k_long_contexts(cuda_device):
     """Enough rows that the split count is set by the 2048-key list limit and
     contexts above it: several splits per row, combined by the split merge."""
