@@ -9,10 +9,13 @@
  *                                     returning out and the softmax LSE
  *   3. smla_dcp_lse_merge             LSE-weighted merge of D partials
  *
- * and two more entry points run it differently:
+ * and three more entry points run it differently:
  *
  *   smla_dcp_sparse_mla_decode_fused  steps 1-3 for D pools held by one GPU,
  *                                     in a single launch
+ *   smla_dcp_sparse_mla_decode_fused_host
+ *                                     the same from and to pinned host
+ *                                     memory, copies overlapping the decode
  *   smla_sparse_mla_decode_noalloc    step 2 with library-owned split-K
  *                                     scratch (no workspace argument)
  *
@@ -35,13 +38,16 @@
  *   - Pointers marked "device" point to memory of the current CUDA device;
  *     the caller allocates and owns all of it.  The library never allocates,
  *     frees or synchronises, and keeps no pointer after a call returns, with
- *     one exception: smla_sparse_mla_decode_noalloc's split-K scratch is a
+ *     two exceptions: smla_sparse_mla_decode_noalloc's split-K scratch is a
  *     library-owned device array of SMLA_NOALLOC_SCRATCH_BYTES per GPU, whose
- *     device address the library looks up once per device and keeps.
+ *     device address the library looks up once per device and keeps, and
+ *     smla_dcp_sparse_mla_decode_fused_host creates its streams and events
+ *     once per device and keeps them.
  *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*,
  *     NULL = legacy default stream) and takes every scalar by value, so no
- *     call issues a host->device copy or a host sync [P2 "DCP decode rank
- *     scalar"].
+ *     call issues a host->device copy of its own or a host sync [P2 "DCP
+ *     decode rank scalar"]; smla_dcp_sparse_mla_decode_fused_host copies
+ *     only the caller's host buffers it is given, asynchronously.
  *   - Arguments are checked on the host before any launch; a failing check
  *     returns a status and launches nothing.  A failed launch returns
  *     SMLA_ERR_CUDA.  No C++ exception crosses this boundary.
@@ -273,6 +279,51 @@ smla_status smla_dcp_sparse_mla_decode_fused(
     const int64_t* num_slots, const int32_t* const* block_tables,
     const int64_t* bt_row_strides, const int32_t* bt_widths, uint16_t* out,
     float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The fused DCP step for callers whose q, top-k ids and results live in
+ * host memory (the pages have no counterpart: it is the same step,
+ * smla_dcp_sparse_mla_decode_fused, with its host<->device copies).
+ *
+ * The rows are cut into `chunks` contiguous groups (1 <= chunks <=
+ * SMLA_MAX_HOST_CHUNKS, at most T).  Group g's q rows and top-k ids are
+ * copied into the device staging buffers, its decode is launched as soon as
+ * they have landed, and its out and lse rows are copied back as soon as its
+ * decode ends, so the copies of some groups overlap the decode of others.
+ * With chunks > 1 each group's decode runs without split-K (every group
+ * keeps its own SM pairs, side by side with the others), which needs
+ * K <= 2048; with chunks == 1 the copies, the decode (the usual split-K
+ * policy and workspace) and the copies back run one after the other.
+ *
+ *   q_host, topk_host       pinned host bf16 [T, H, 576], int32 [T, K]
+ *   out_host, lse_host      pinned host bf16 [T, H, 512], fp32 [T, H] outputs
+ *   q_dev, topk_dev,        device staging buffers of the same shapes (16-byte
+ *   out_dev, lse_dev        aligned; 4 for lse_dev), owned by the caller;
+ *                           they hold the step's device copies afterwards
+ *   other arguments         as for smla_dcp_sparse_mla_decode_fused
+ *                           (req_id_per_token, pools, block tables and
+ *                           workspace in device memory)
+ * Everything is ordered after the work already queued on `stream`, and work
+ * queued on `stream` after the call waits for the whole step, including the
+ * copies back: the host buffers hold the results once `stream` has reached
+ * that point.  The groups run on library-owned streams and events (created
+ * on a device's first call, kept until the process exits); the call is
+ * serialised per device, so concurrent calls from several host threads
+ * queue one after the other.
+ * Errors: as smla_dcp_sparse_mla_decode_fused, plus INVALID_ARG for a null
+ * or misaligned host or staging buffer or chunks outside [1,
+ * SMLA_MAX_HOST_CHUNKS]; UNSUPPORTED for chunks > 1 with K > 2048.
+ */
+#define SMLA_MAX_HOST_CHUNKS 8
+smla_status smla_dcp_sparse_mla_decode_fused_host(
+    const uint16_t* q_host, const int32_t* topk_host, uint16_t* out_host, float* lse_host,
+    uint16_t* q_dev, int32_t* topk_dev, uint16_t* out_dev, float* lse_dev,
+    int32_t T, int32_t H, int32_t K, float sm_scale, const int32_t* req_id_per_token,
+    int32_t num_reqs, int32_t D, int32_t block_size, int32_t interleave,
+    const uint8_t* const* kv_caches, const int64_t* num_slots,
+    const int32_t* const* block_tables, const int64_t* bt_row_strides,
+    const int32_t* bt_widths, void* workspace, size_t workspace_bytes, int32_t chunks,
+    void* stream);
 
 /*
  * Dense MLA decode with LSE return under DCP [P3 key snippets: the dense

@@ -54,6 +54,10 @@ SIGNATURES = {
     "smla_dcp_sparse_mla_decode_fused": (ctypes.c_int, [
         _c_vp, _c_i32, _c_i32, _c_i32, ctypes.c_float, _c_vp, _c_vp, _c_i32, _c_i32, _c_i32,
         _c_i32, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]),
+    "smla_dcp_sparse_mla_decode_fused_host": (ctypes.c_int, [
+        _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i32, _c_i32, _c_i32,
+        ctypes.c_float, _c_vp, _c_i32, _c_i32, _c_i32, _c_i32, _c_vp, _c_vp, _c_vp, _c_vp,
+        _c_vp, _c_vp, _c_sz, _c_i32, _c_vp]),
     "smla_dense_decode_workspace_size": (_c_sz, [_c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                                                  _c_i32]),
     "smla_dcp_dense_mla_decode": (ctypes.c_int, [
@@ -296,6 +300,86 @@ def dcp_sparse_mla_decode_fused(q: torch.Tensor, req_id_per_token: torch.Tensor,
         out.data_ptr(), lse.data_ptr(), ws_ptr, ws_bytes, _stream_ptr(stream, dev))
     _check("smla_dcp_sparse_mla_decode_fused", st)
     return out, lse
+
+
+MAX_HOST_CHUNKS = 8
+
+
+def _need_host(t: torch.Tensor, name: str, dtype, shape):
+    if t.dtype != dtype or t.device.type != "cpu" or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} host tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def dcp_sparse_mla_decode_fused_host(q_host: torch.Tensor, topk_host: torch.Tensor,
+                                     out_host: torch.Tensor, lse_host: torch.Tensor,
+                                     req_id_per_token: torch.Tensor,
+                                     kv_caches: Sequence[torch.Tensor],
+                                     block_tables: Sequence[torch.Tensor], block_size: int,
+                                     sm_scale: float, *, interleave: int = 1,
+                                     bt_widths: Optional[Sequence[int]] = None,
+                                     q_dev: Optional[torch.Tensor] = None,
+                                     topk_dev: Optional[torch.Tensor] = None,
+                                     out_dev: Optional[torch.Tensor] = None,
+                                     lse_dev: Optional[torch.Tensor] = None,
+                                     workspace: Optional[torch.Tensor] = None,
+                                     chunks: int = 4,
+                                     stream: Optional[torch.cuda.Stream] = None
+                                     ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """The fused step from and to (pinned) host memory: q and the top-k ids
+    are copied in and out/lse back by the library, row groups pipelined
+    (smla_dcp_sparse_mla_decode_fused_host).  Returns (out_host, lse_host),
+    which hold the results once `stream` has reached the end of the call."""
+    dev = req_id_per_token.device
+    _need(req_id_per_token, "req_id_per_token", torch.int32, dev)
+    T, H, Dq = q_host.shape
+    K = topk_host.shape[1]
+    _need_host(q_host, "q_host", torch.bfloat16, (T, H, QK_DIM))
+    _need_host(topk_host, "topk_host", torch.int32, (T, K))
+    _need_host(out_host, "out_host", torch.bfloat16, (T, H, V_DIM))
+    _need_host(lse_host, "lse_host", torch.float32, (T, H))
+    D = len(kv_caches)
+    if D != len(block_tables) or D < 1:
+        raise ValueError("need one block table per KV pool (>= 1)")
+    num_reqs = None
+    for kv, bt in zip(kv_caches, block_tables):
+        _need(kv, "kv_caches[d]", torch.uint8, dev)
+        if kv.dim() != 2 or kv.shape[1] != ROW_BYTES:
+            raise ValueError(f"kv_caches[d] must be [num_slots, {ROW_BYTES}] uint8")
+        if bt.dtype != torch.int32 or bt.device != dev or bt.dim() != 2 or bt.stride(1) != 1:
+            raise ValueError("block_tables[d] must be 2-D int32 with contiguous rows")
+        num_reqs = bt.shape[0] if num_reqs is None else min(num_reqs, bt.shape[0])
+    if q_dev is None:
+        q_dev = torch.empty((T, H, QK_DIM), dtype=torch.bfloat16, device=dev)
+    if topk_dev is None:
+        topk_dev = torch.empty((T, K), dtype=torch.int32, device=dev)
+    if out_dev is None:
+        out_dev = torch.empty((T, H, V_DIM), dtype=torch.bfloat16, device=dev)
+    if lse_dev is None:
+        lse_dev = torch.empty((T, H), dtype=torch.float32, device=dev)
+    _need(q_dev, "q_dev", torch.bfloat16, dev)
+    _need(topk_dev, "topk_dev", torch.int32, dev)
+    _need(out_dev, "out_dev", torch.bfloat16, dev)
+    _need(lse_dev, "lse_dev", torch.float32, dev)
+    if workspace is None and min(chunks, T) == 1:
+        workspace = alloc_decode_workspace(T, H, K, dev)
+    widths = [bt.shape[1] for bt in block_tables] if bt_widths is None else list(bt_widths)
+    pools = (ctypes.c_void_p * D)(*[kv.data_ptr() for kv in kv_caches])
+    nslots = (ctypes.c_int64 * D)(*[kv.shape[0] for kv in kv_caches])
+    bts = (ctypes.c_void_p * D)(*[bt.data_ptr() for bt in block_tables])
+    strides = (ctypes.c_int64 * D)(*[bt.stride(0) for bt in block_tables])
+    wids = (ctypes.c_int32 * D)(*widths)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().smla_dcp_sparse_mla_decode_fused_host(
+        q_host.data_ptr(), topk_host.data_ptr(), out_host.data_ptr(), lse_host.data_ptr(),
+        q_dev.data_ptr(), topk_dev.data_ptr(), out_dev.data_ptr(), lse_dev.data_ptr(),
+        T, H, K, float(sm_scale), req_id_per_token.data_ptr(), num_reqs, D, block_size,
+        int(interleave), pools, nslots, bts, strides, wids, ws_ptr, ws_bytes, int(chunks),
+        _stream_ptr(stream, dev))
+    _check("smla_dcp_sparse_mla_decode_fused_host", st)
+    return out_host, lse_host
 
 
 def dense_decode_workspace_size(T: int, H: int, max_ctx: int, D: int, interleave: int = 1,

@@ -1,6 +1,7 @@
-// C ABI of the library: host-side argument checks, then one launch per call.
-// Every check runs before anything touches the GPU, so a rejected call has
-// no side effect and needs no device.
+// C ABI of the library: host-side argument checks, then one launch per call
+// (the host-buffer form of the fused step: its copies and a launch per row
+// group).  Every check runs before anything touches the GPU, so a rejected
+// call has no side effect and needs no device.
 #include <cmath>
 #include <cstdint>
 
@@ -145,13 +146,15 @@ smla_status smla_sparse_mla_decode_noalloc(
   return from_cuda(smla::launch_decode_noalloc(a, static_cast<cudaStream_t>(stream)));
 }
 
-smla_status smla_dcp_sparse_mla_decode_fused(
-    const uint16_t* q, int32_t T, int32_t H, int32_t K, float sm_scale,
-    const int32_t* req_id_per_token, const int32_t* topk_global, int32_t num_reqs,
-    int32_t D, int32_t block_size, int32_t interleave, const uint8_t* const* kv_caches,
+// Checks of the fused step's arguments shared by its device and host forms;
+// fills `a` with everything but the staging of q and the top-k ids.
+static smla_status fused_args(
+    const void* q, int32_t T, int32_t H, int32_t K, float sm_scale,
+    const int32_t* req_id_per_token, const void* topk_global, int32_t num_reqs, int32_t D,
+    int32_t block_size, int32_t interleave, const uint8_t* const* kv_caches,
     const int64_t* num_slots, const int32_t* const* block_tables,
-    const int64_t* bt_row_strides, const int32_t* bt_widths, uint16_t* out,
-    float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+    const int64_t* bt_row_strides, const int32_t* bt_widths, const void* out, const void* lse,
+    smla::DecodeArgs& a) {
   if (T < 0 || K < 1 || H < 1 || D < 1 || block_size < 1 || interleave < 1 || num_reqs < 1 ||
       !std::isfinite(sm_scale) || !(sm_scale > 0.f))
     return SMLA_ERR_INVALID_ARG;
@@ -163,7 +166,7 @@ smla_status smla_dcp_sparse_mla_decode_fused(
   if (misaligned(q, 16) || misaligned(out, 16) || misaligned(lse, 4) ||
       misaligned(req_id_per_token, 4) || misaligned(topk_global, 4))
     return SMLA_ERR_INVALID_ARG;
-  smla::DecodeArgs a{};
+  a = smla::DecodeArgs{};
   for (int d = 0; d < D; ++d) {
     if (!kv_caches[d] || misaligned(kv_caches[d], 16) || num_slots[d] < 0 ||
         !block_tables[d] || misaligned(block_tables[d], 4) || bt_widths[d] < 1 ||
@@ -175,26 +178,78 @@ smla_status smla_dcp_sparse_mla_decode_fused(
     a.bt_stride[d] = bt_row_strides[d];
     a.bt_width[d] = bt_widths[d];
   }
-  const size_t need = smla::decode_workspace_bytes(T, H, K);
-  if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
-                   misaligned(workspace, 256)))
-    return SMLA_ERR_WORKSPACE;
-  a.q = q;
   a.T = T;
   a.H = H;
   a.K = K;
   a.sm_scale = sm_scale;
-  a.out = out;
-  a.lse = lse;
-  a.workspace = workspace;
-  a.workspace_bytes = workspace_bytes;
   a.D = D;
   a.block_size = block_size;
   a.interleave = interleave;
   a.num_reqs = num_reqs;
   a.req_id = req_id_per_token;
+  return SMLA_OK;
+}
+
+smla_status smla_dcp_sparse_mla_decode_fused(
+    const uint16_t* q, int32_t T, int32_t H, int32_t K, float sm_scale,
+    const int32_t* req_id_per_token, const int32_t* topk_global, int32_t num_reqs,
+    int32_t D, int32_t block_size, int32_t interleave, const uint8_t* const* kv_caches,
+    const int64_t* num_slots, const int32_t* const* block_tables,
+    const int64_t* bt_row_strides, const int32_t* bt_widths, uint16_t* out,
+    float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  smla::DecodeArgs a;
+  const smla_status st =
+      fused_args(q, T, H, K, sm_scale, req_id_per_token, topk_global, num_reqs, D, block_size,
+                 interleave, kv_caches, num_slots, block_tables, bt_row_strides, bt_widths, out,
+                 lse, a);
+  if (st != SMLA_OK || T == 0) return st;
+  const size_t need = smla::decode_workspace_bytes(T, H, K);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
+                   misaligned(workspace, 256)))
+    return SMLA_ERR_WORKSPACE;
+  a.q = q;
   a.topk = topk_global;
+  a.out = out;
+  a.lse = lse;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
   return from_cuda(smla::launch_decode_fused(a, static_cast<cudaStream_t>(stream)));
+}
+
+smla_status smla_dcp_sparse_mla_decode_fused_host(
+    const uint16_t* q_host, const int32_t* topk_host, uint16_t* out_host, float* lse_host,
+    uint16_t* q_dev, int32_t* topk_dev, uint16_t* out_dev, float* lse_dev,
+    int32_t T, int32_t H, int32_t K, float sm_scale, const int32_t* req_id_per_token,
+    int32_t num_reqs, int32_t D, int32_t block_size, int32_t interleave,
+    const uint8_t* const* kv_caches, const int64_t* num_slots,
+    const int32_t* const* block_tables, const int64_t* bt_row_strides,
+    const int32_t* bt_widths, void* workspace, size_t workspace_bytes, int32_t chunks,
+    void* stream) {
+  smla::DecodeArgs a;
+  smla_status st =
+      fused_args(q_dev, T, H, K, sm_scale, req_id_per_token, topk_dev, num_reqs, D, block_size,
+                 interleave, kv_caches, num_slots, block_tables, bt_row_strides, bt_widths,
+                 out_dev, lse_dev, a);
+  if (st != SMLA_OK) return st;
+  if (chunks < 1 || chunks > SMLA_MAX_HOST_CHUNKS) return SMLA_ERR_INVALID_ARG;
+  if (T == 0) return SMLA_OK;
+  if (!q_host || !topk_host || !out_host || !lse_host) return SMLA_ERR_INVALID_ARG;
+  const int groups = chunks < T ? chunks : T;
+  if (groups > 1 && K > smla::kDecodeMaxList) return SMLA_ERR_UNSUPPORTED;
+  if (groups == 1) {
+    const size_t need = smla::decode_workspace_bytes(T, H, K);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
+                     misaligned(workspace, 256)))
+      return SMLA_ERR_WORKSPACE;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+  }
+  a.q = q_dev;
+  a.topk = topk_dev;
+  a.out = out_dev;
+  a.lse = lse_dev;
+  smla::HostBuffers h{q_host, topk_host, out_host, lse_host, q_dev, topk_dev};
+  return from_cuda(smla::launch_fused_host(a, h, groups, static_cast<cudaStream_t>(stream)));
 }
 
 // Raw entries per row of the dense decode: positions 0..max_ctx-1, or the

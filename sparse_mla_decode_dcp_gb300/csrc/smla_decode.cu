@@ -74,7 +74,7 @@ constexpr int kRawStages = 1;     // raw cache-row tiles in shared memory (one m
 constexpr int kMmaWarp = 8;
 constexpr int kLoaderWarp0 = 9;   // warps 9..11 stage cache rows
 constexpr int kLoaders = 96;
-constexpr int kMaxList = 2048;    // compacted slots one cluster handles
+constexpr int kMaxList = kDecodeMaxList;  // compacted slots one cluster handles
 
 // tensor-memory columns (512 allocated)
 constexpr uint32_t kOCol = 0;     // O half: 256 fp32 columns
@@ -1628,8 +1628,8 @@ cudaError_t launch_impl(const DecodeArgs& args, cudaStream_t s) {
     const cudaError_t e = encode_q_maps(a);
     if (e != cudaSuccess) return e;
   }
-  a.splits = decode_splits(a.T, a.K);
-  const WsLayout w = ws_layout(a.T, a.H, a.K);
+  a.splits = a.single_split ? 1 : decode_splits(a.T, a.K);
+  const WsLayout w = a.splits > 1 ? ws_layout(a.T, a.H, a.K) : WsLayout{0, 0, 0, 0};
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   a.ws_o = w.total ? reinterpret_cast<float*>(ws + w.o_off) : nullptr;
   a.ws_ml = w.total ? reinterpret_cast<float*>(ws + w.ml_off) : nullptr;

@@ -66,6 +66,7 @@ struct DecodeArgs {
   float* ws_ml;      // [T, splits, 2 halves, 2, H]: log2-domain max, then sum
   int32_t* ws_tick;  // [T, 2] arrival counters, left at zero by every call
   int32_t combine_in_kernel;  // 1: the last split to arrive merges the row; 0: a second kernel
+  int32_t single_split;       // set by the caller: no split-K whatever T (needs K <= 2048)
   // Fused DCP step only (D > 0): global top-k ids are converted per shard in
   // the kernel prologue and all shards' keys share one softmax.
   int32_t D, block_size, num_reqs, interleave;
@@ -113,11 +114,28 @@ cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_dense(const DecodeArgs& a, cudaStream_t s);
 // Library-owned split-K scratch (no allocation by anyone at call time).
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+// compacted entries one decode cluster handles (the key list in its shared
+// memory): a decode without split-K needs K at most this
+constexpr int32_t kDecodeMaxList = 2048;
 cudaError_t launch_decode_noalloc(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s);
 cudaError_t launch_topk_select(const TopkArgs& a, cudaStream_t s);
 cudaError_t launch_topk_merge(const TopkArgs& a, cudaStream_t s);
 size_t decode_workspace_bytes(int32_t T, int32_t H, int32_t K);
+
+// The fused step from and to host memory (smla_host.cu): the caller's host
+// buffers and the device staging buffers their copies fill (the decode's q
+// and topk point at the same staging memory).
+struct HostBuffers {
+  const void* q;        // host bf16 [T, H, 576]
+  const int32_t* topk;  // host [T, K]
+  void* out;            // host bf16 [T, H, 512]
+  float* lse;           // host [T, H]
+  uint16_t* q_dev;      // device staging [T, H, 576]
+  int32_t* topk_dev;    // device staging [T, K]
+};
+cudaError_t launch_fused_host(const DecodeArgs& a, const HostBuffers& h, int groups,
+                              cudaStream_t s);
 
 // Each kernel translation unit owns one device error word.
 cudaError_t index_error_word(uint32_t* flags, bool clear);

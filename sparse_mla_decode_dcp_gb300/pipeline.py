@@ -66,6 +66,18 @@ class DcpDecodeStep:
             bt_widths=self.bt_widths,
             out=self.out, lse=self.lse, workspace=self.workspace, stream=self.stream)
 
+    def run_fused_from_host(self, q_host: torch.Tensor, topk_host: torch.Tensor,
+                            out_host: torch.Tensor, lse_host: torch.Tensor, chunks: int = 4):
+        """The fused step with q and the top-k ids in pinned host memory and
+        out/lse returned there: the library copies them in and out through
+        this step's device buffers, row groups pipelined."""
+        wl = self.wl
+        return capi.dcp_sparse_mla_decode_fused_host(
+            q_host, topk_host, out_host, lse_host, self.req_id, self.pools, self.block_tables,
+            wl.spec.block_size, wl.spec.sm_scale, interleave=wl.spec.interleave,
+            bt_widths=self.bt_widths, q_dev=self.q, topk_dev=self.topk, out_dev=self.out,
+            lse_dev=self.lse, workspace=self.workspace, chunks=chunks, stream=self.stream)
+
     def run(self):
         for d in range(self.wl.D):
             self.run_shard(d)

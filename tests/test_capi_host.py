@@ -32,7 +32,8 @@ def test_header_declares_the_three_path_calls():
     names = _declared_functions()
     for n in ("smla_dcp_filter_convert_index", "smla_sparse_mla_decode",
               "smla_dcp_lse_merge", "smla_decode_workspace_size",
-              "smla_dcp_sparse_mla_decode_fused", "smla_dcp_dense_mla_decode",
+              "smla_dcp_sparse_mla_decode_fused", "smla_dcp_sparse_mla_decode_fused_host",
+              "smla_dcp_dense_mla_decode",
               "smla_dense_decode_workspace_size",
               "smla_status_string", "smla_get_device_error"):
         assert n in names
@@ -193,6 +194,45 @@ def test_fused_workspace_checks(lib):
     assert need > 0
     assert _fused(lib, T=3, H=128, K=2048) == capi.SMLA_ERR_WORKSPACE
     assert _fused(lib, T=3, H=128, K=2048, ws=FAKE, wsb=need - 1) == capi.SMLA_ERR_WORKSPACE
+
+
+def _fused_host(lib, D=2, **kw):
+    a = dict(qh=FAKE, th=FAKE, oh=FAKE, lh=FAKE, q=FAKE, topk=FAKE, out=FAKE, lse=FAKE, T=2,
+             H=16, K=64, scale=0.07, req=FAKE, nreq=2, bs=16, I=1, pools=[FAKE] * D,
+             nslots=[100] * D, bts=[FAKE] * D, strides=[4] * D, widths=[4] * D, ws=None, wsb=0,
+             chunks=2)
+    a.update(kw)
+    arr = lambda typ, xs: (typ * D)(*xs)
+    return lib.smla_dcp_sparse_mla_decode_fused_host(
+        a["qh"], a["th"], a["oh"], a["lh"], a["q"], a["topk"], a["out"], a["lse"], a["T"],
+        a["H"], a["K"], ctypes.c_float(a["scale"]), a["req"], a["nreq"], D, a["bs"], a["I"],
+        arr(ctypes.c_void_p, a["pools"]), arr(ctypes.c_int64, a["nslots"]),
+        arr(ctypes.c_void_p, a["bts"]), arr(ctypes.c_int64, a["strides"]),
+        arr(ctypes.c_int32, a["widths"]), a["ws"], a["wsb"], a["chunks"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(chunks=0), capi.SMLA_ERR_INVALID_ARG),
+    (dict(chunks=capi.MAX_HOST_CHUNKS + 1), capi.SMLA_ERR_INVALID_ARG),
+    (dict(qh=None), capi.SMLA_ERR_INVALID_ARG),
+    (dict(th=None), capi.SMLA_ERR_INVALID_ARG),
+    (dict(oh=None), capi.SMLA_ERR_INVALID_ARG),
+    (dict(lh=None), capi.SMLA_ERR_INVALID_ARG),
+    (dict(q=FAKE + 8), capi.SMLA_ERR_INVALID_ARG),    # staging buffers as the fused step's
+    (dict(out=FAKE + 4), capi.SMLA_ERR_INVALID_ARG),
+    (dict(topk=None), capi.SMLA_ERR_INVALID_ARG),
+    (dict(H=129), capi.SMLA_ERR_UNSUPPORTED),
+    (dict(scale=0.0), capi.SMLA_ERR_INVALID_ARG),
+    # row groups decode without split-K: one cluster's list holds 2048 keys
+    (dict(K=2049), capi.SMLA_ERR_UNSUPPORTED),
+    # one group (chunks = 1, or above T): the usual split-K policy and workspace
+    (dict(T=3, H=128, K=2048, chunks=1), capi.SMLA_ERR_WORKSPACE),
+    (dict(T=1, H=128, K=4096, chunks=4), capi.SMLA_ERR_WORKSPACE),
+    (dict(T=0, qh=None, th=None, oh=None, lh=None, q=None, topk=None, out=None, lse=None,
+          req=None), capi.SMLA_OK),
+])
+def test_fused_host_argument_checks(lib, kw, status):
+    assert _fused_host(lib, **kw) == status
 
 
 def _merge(lib, D=2, T=3, H=4, outs=None, lses=None, out=FAKE, lse=FAKE):

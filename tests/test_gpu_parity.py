@@ -515,6 +515,68 @@ def test_spec_decode_rows_equal_single_token_calls(cuda_device):
             assert (l[0] - step.part_lse[d][i]).abs().max().item() < 2e-3
 
 
+# ------------------------------------------------- fused step from host memory
+def _pinned(t):
+    return t.detach().cpu().contiguous().pin_memory()
+
+
+@pytest.mark.parametrize("chunks", [1, 4, 8])
+def test_fused_host_equals_device_step(cuda_device, chunks):
+    """The host-buffer form (copies in, row groups decoded as their inputs
+    land, copies back) gives the device form's results bit for bit: each row
+    runs the same code whichever launch holds it (64 rows: no split-K either
+    way)."""
+    dev = cuda_device
+    wl = inputs.make_workload("dcp4_long", seed=3, device=dev)
+    step = DcpDecodeStep(wl, device=dev)
+    ref_out, ref_lse = step.run_fused()
+    torch.cuda.synchronize()
+    ref_out, ref_lse = ref_out.cpu(), ref_lse.cpu()
+    q_host, topk_host = _pinned(step.q), _pinned(step.topk)
+    out_host = torch.full(tuple(ref_out.shape), 7, dtype=torch.bfloat16).pin_memory()
+    lse_host = torch.full(tuple(ref_lse.shape), 7.0, dtype=torch.float32).pin_memory()
+    step.q.zero_()
+    step.topk.fill_(-1)
+    step.out.zero_()
+    for _ in range(2):
+        step.run_fused_from_host(q_host, topk_host, out_host, lse_host, chunks=chunks)
+        torch.cuda.synchronize()
+        assert torch.equal(out_host, ref_out) and torch.equal(lse_host, ref_lse)
+        out_host.fill_(7)
+    # the staging buffers hold the step's device copies afterwards
+    assert torch.equal(step.q.cpu(), q_host) and torch.equal(step.topk.cpu(), topk_host)
+
+
+def test_fused_host_ragged_groups_match_oracle(cuda_device):
+    """5 rows in 3 groups (2, 2, 1), each decoded without split-K, against
+    the oracle's per-shard decode and merge; one row's ids all -1."""
+    dev = cuda_device
+    spec = inputs.WorkloadSpec(
+        name="host_ragged", num_reqs=5, tokens_per_req=1, heads=128, topk=2048, dcp=2,
+        block_size=64, ctx_kind="uniform", ctx_lo=1500, ctx_hi=9000)
+    wl = inputs.make_workload(spec, seed=17, device=dev)
+    wl.topk[3] = -1
+    step = DcpDecodeStep(wl, device=dev)
+    q_host, topk_host = _pinned(wl.q), torch.from_numpy(wl.topk).contiguous().pin_memory()
+    out_host = torch.empty((wl.T, wl.H, 512), dtype=torch.bfloat16).pin_memory()
+    lse_host = torch.empty((wl.T, wl.H), dtype=torch.float32).pin_memory()
+    capi.get_device_error(clear=True)
+    step.run_fused_from_host(q_host, topk_host, out_host, lse_host, chunks=3)
+    torch.cuda.synchronize()
+    assert capi.get_device_error(clear=True) == 0
+    q = _q_bits(wl.q)
+    outs, lses = [], []
+    for d, sh in enumerate(wl.shards):
+        sl, _ = oracle.dcp_filter_convert_index(wl.req_id, sh.block_table, wl.topk, wl.D, d,
+                                                spec.block_size)
+        o, l = oracle.sparse_mla_decode(q, sh.pool.cpu().numpy(), sl, spec.sm_scale)
+        outs.append(o)
+        lses.append(l)
+    ref_out, ref_lse = oracle.lse_merge(outs, lses)
+    compare_out_lse(out_host, lse_host, ref_out, ref_lse, where="fused from host, 3 groups")
+    assert torch.all(out_host[3].view(torch.int16) == 0) and torch.isneginf(lse_host[3]).all()
+
+
 # ------------------------------------------------------- workspace and graphs
 @pytest.mark.parametrize("T,K", [(4, 2048), (40, 4096)])
 def test_split_k_workspace_reused_across_calls(cuda_device, T, K):
