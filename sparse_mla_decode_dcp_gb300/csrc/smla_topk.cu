@@ -87,44 +87,62 @@ __device__ __forceinline__ int32_t global_id(const TopkArgs& a, int j) {
 // score key, x) is called by every lane, x the candidate's id (merge: entry
 // j < M, skipped when its id is -1) or its local position j < n (select:
 // global_id(x) is its id, computed only where needed).  A thread keeps
-// kUnroll loads in flight (16 bytes of scores each when the rows allow it,
-// kVec4): a gather's rate is set by the bytes in flight.  The loads are
-// issued unconditionally (at a clamped index, the result then masked): a
-// branch around a load would make each wait for the one before.
+// kUnroll loads in flight: a gather's rate is set by the bytes in flight.
+// The loads are issued unconditionally (at a clamped index, the result then
+// masked): a branch around a load would make each wait for the one before.
+// With kVec4 (select) the row's aligned middle is read 16 bytes at a time
+// and its up to 3 leading and 3 trailing scores, outside any aligned quad,
+// by warp 0 one per lane, so no load leaves the row whatever its alignment.
 template <bool kExplicit, bool kVec4, typename F>
 __device__ __forceinline__ void for_each_candidate(const TopkArgs& a, int64_t i, int span, F f) {
   const float* srow = a.scores + i * a.row_stride;
+  if (kVec4) {
+    constexpr int kUnroll = 4;  // 16-byte loads in flight per thread
+    const int head = min(span, int((4u - ((reinterpret_cast<uintptr_t>(srow) >> 2) & 3u)) & 3u));
+    const int nq = (span - head) >> 2;  // whole aligned quads
+    const int tail = span - head - 4 * nq;
+    const float4* quads = reinterpret_cast<const float4*>(srow + head);
+    for (int q0 = threadIdx.x; q0 - int(threadIdx.x) < nq; q0 += kThreads * kUnroll) {
+      float4 v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) v[u] = __ldg(quads + min(q0 + u * kThreads, nq - 1));
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int q = q0 + u * kThreads;
+        const int j = head + 4 * q;
+        f(q < nq, score_key(v[u].x), j);
+        f(q < nq, score_key(v[u].y), j + 1);
+        f(q < nq, score_key(v[u].z), j + 2);
+        f(q < nq, score_key(v[u].w), j + 3);
+      }
+    }
+    if (threadIdx.x < 32 && head + tail > 0) {
+      const int l = int(threadIdx.x);
+      const bool ok = l < head + tail;
+      const int j = l < head ? l : head + 4 * nq + (l - head);
+      const float sc = ok ? __ldg(srow + j) : 0.f;
+      f(ok, score_key(sc), ok ? j : 0);
+    }
+    return;
+  }
   const int32_t* irow = kExplicit ? a.cand_ids + i * a.row_stride : nullptr;
-  constexpr int kW = kVec4 ? 4 : 1;        // candidates per load
-  constexpr int kUnroll = kVec4 ? 4 : 8;   // loads in flight per thread
-  for (int j0 = kW * threadIdx.x; j0 - kW * int(threadIdx.x) < span; j0 += kW * kThreads * kUnroll) {
-    float sc[kUnroll][kW];
+  constexpr int kUnroll = 8;  // 4-byte loads in flight per thread
+  for (int j0 = threadIdx.x; j0 - int(threadIdx.x) < span; j0 += kThreads * kUnroll) {
+    float sc[kUnroll];
     int32_t id[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      if (kVec4) {
-        const int jc = min(j0 + u * kW * kThreads, (span - 1) & ~3);
-        const float4 v = __ldg(reinterpret_cast<const float4*>(srow + jc));
-        sc[u][0] = v.x;
-        sc[u][kW > 1 ? 1 : 0] = v.y;
-        sc[u][kW > 2 ? 2 : 0] = v.z;
-        sc[u][kW > 3 ? 3 : 0] = v.w;
-      } else {
-        const int jc = min(j0 + u * kThreads, span - 1);
-        sc[u][0] = __ldg(srow + jc);
-        if (kExplicit) id[u] = __ldg(irow + jc);
-      }
+      const int jc = min(j0 + u * kThreads, span - 1);
+      sc[u] = __ldg(srow + jc);
+      if (kExplicit) id[u] = __ldg(irow + jc);
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-#pragma unroll
-      for (int e = 0; e < kW; ++e) {
-        const int j = j0 + u * kW * kThreads + e;
-        if (kExplicit)
-          f(j < span && id[u] >= 0, score_key(sc[u][e]), id[u]);
-        else
-          f(j < span, score_key(sc[u][e]), j);
-      }
+      const int j = j0 + u * kThreads;
+      if (kExplicit)
+        f(j < span && id[u] >= 0, score_key(sc[u]), id[u]);
+      else
+        f(j < span, score_key(sc[u]), j);
     }
   }
 }
@@ -487,9 +505,8 @@ cudaError_t launch_topk_select(const TopkArgs& args, cudaStream_t s) {
   TopkArgs a = args;
   a.div_I = make_fastdiv(uint32_t(a.interleave));
   a.kp = pow2_at_least(a.K);
-  // 16-byte score loads when every row starts on a 16-byte boundary
-  const bool vec = (reinterpret_cast<uintptr_t>(a.scores) % 16 == 0) && (a.row_stride % 4 == 0);
-  return vec ? launch<false, true>(a, boundary_cap(a), s) : launch<false, false>(a, boundary_cap(a), s);
+  // 16-byte score loads over each row's aligned middle, whatever the stride
+  return launch<false, true>(a, boundary_cap(a), s);
 }
 
 cudaError_t launch_topk_merge(const TopkArgs& args, cudaStream_t s) {

@@ -991,6 +991,20 @@ def test_topk_select_boundary_bin_past_shared_memory(cuda_device, L, K):
     _topk_vs_oracle(cuda_device, scores, [L, L // 2, L], K, f"ties past shared memory L={L}")
 
 
+@pytest.mark.parametrize("L", [5, 6, 7, 19])
+def test_topk_select_row_alignments(cuda_device, L):
+    """Row strides that start rows at every offset within 16 bytes, and row
+    lengths shorter than, equal to and past a few aligned quads: the scores
+    before a row's first aligned quad and after its last one are read one by
+    one, and every candidate is seen exactly once."""
+    rng = np.random.default_rng(70 + L)
+    T = 8
+    scores = rng.standard_normal((T, L))
+    n_cand = [min(L, x) for x in (0, 1, 2, 3, 4, 5, 7, L)]
+    for K in (4, 16):
+        _topk_vs_oracle(cuda_device, scores, n_cand, K, f"L={L} K={K}")
+
+
 def test_topk_select_nan_and_signed_zero(cuda_device):
     """NaN ranks below every number (-inf included) and -0 ties with +0."""
     row = np.array([0.0, -0.0, np.nan, 1.5, -np.inf, np.nan, -0.0, 2.0, np.inf, -1.0], np.float64)
