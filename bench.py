@@ -43,6 +43,14 @@ HOST_CHUNKS = 4  # row groups of the host-buffer step (fastest of 1-8 on dcp4_lo
 # hashed to decide whether a committed ncu traffic figure still applies
 DECODE_SOURCES = ["sparse_mla_decode_dcp_gb300/csrc/smla_decode.cu",
                   "sparse_mla_decode_dcp_gb300/csrc/smla_sm100.cuh"]
+KERNEL_SOURCES = {
+    "smla_dcp_sparse_mla_decode_fused": DECODE_SOURCES,
+    "smla_sparse_mla_decode": DECODE_SOURCES,
+    "smla_dcp_dense_mla_decode": DECODE_SOURCES,
+    "smla_dcp_filter_convert_index": ["sparse_mla_decode_dcp_gb300/csrc/smla_index.cu"],
+    "smla_dcp_lse_merge": ["sparse_mla_decode_dcp_gb300/csrc/smla_merge.cu"],
+    "smla_topk_select": ["sparse_mla_decode_dcp_gb300/csrc/smla_topk.cu"],
+}
 
 
 def parse_args(argv=None):
@@ -139,18 +147,23 @@ def algorithmic_units(step):
     return [int(v.sum().item()) for v in step.valid_count]
 
 
-def decode_source_sha256() -> str:
+def source_sha256(sources=DECODE_SOURCES) -> str:
     h = hashlib.sha256()
-    for src in DECODE_SOURCES:
+    for src in sources:
         with open(os.path.join(ROOT, src), "rb") as g:
             h.update(g.read())
     return h.hexdigest()
 
 
+def decode_source_sha256() -> str:
+    return source_sha256(DECODE_SOURCES)
+
+
 def profile_traffic(kernel: str, workload: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary
-    profiles/<kernel>_<workload>.md, if that summary was taken on the decode
-    source as it is now (its `source_sha256:` line); else None."""
+    profiles/<kernel>_<workload>.md, if that summary was taken on the
+    kernel's source as it is now (its `source_sha256:` line, the hash of
+    KERNEL_SOURCES[kernel]); else None."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(path):
         return None
@@ -160,7 +173,8 @@ def profile_traffic(kernel: str, workload: str):
             m = re.match(r"^\s*-?\s*`?([a-z_0-9]+)`?\s*:\s*`?([^`\s]+)`?", line)
             if m:
                 fields.setdefault(m.group(1), m.group(2))
-    if fields.get("source_sha256") != decode_source_sha256():
+    if kernel not in KERNEL_SOURCES or fields.get("source_sha256") != source_sha256(
+            KERNEL_SOURCES[kernel]):
         return None
     try:
         return float(fields["dram_bytes_per_launch"])
@@ -424,12 +438,13 @@ def _e2e_overlapped(step, wl, q_host, n, stream, sets=4):
     return t0.elapsed_time(t1) / n, h2d, d2h
 
 
-def _hbm_roofline(kernel, launch_ms, nbytes, peaks, unit_note):
+def _hbm_roofline(kernel, launch_ms, nbytes, peaks, unit_note, workload):
     """HBM roofline of a memory-bound kernel: algorithmic bytes per launch
     over its mean launch time, against the measured copy bandwidth."""
     achieved = nbytes / (launch_ms * 1e-3) / 1e9
     return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": kernel,
+            "frac": achieved / peaks["hbm_gbs"], "traffic": profile_traffic(kernel, workload),
+            "kernel": kernel,
             "launch_us": launch_ms * 1e3, "algorithmic_bytes_per_launch": nbytes,
             "bytes": unit_note,
             "peak_source": f"{peaks['source']} MEASURED_PEAKS.json copy bandwidth"}
@@ -490,7 +505,7 @@ def _dense_path(step, wl, n, flush, stream, peaks, workload):
             "roofline": roof}
 
 
-def _topk_path(wl, n, flush, stream, peaks, dev):
+def _topk_path(wl, n, flush, stream, peaks, dev, workload):
     """Global top-K of synthetic indexer scores: one fp32 score per cached
     position of each row (seeded normal draws), K = the workload's top-k."""
     import torch
@@ -513,7 +528,8 @@ def _topk_path(wl, n, flush, stream, peaks, dev):
     nbytes = 4 * int(n_cand_np.sum()) + 4 * wl.T * wl.K
     return {"ms_per_step": ms, "launches_per_step": 1,
             "roofline": _hbm_roofline("smla_topk_select", ms, nbytes, peaks,
-                                      "4 B per candidate score read + 4 B per id written")}
+                                      "4 B per candidate score read + 4 B per id written",
+                                      workload)}
 
 
 def run_gpu(args):
@@ -610,16 +626,18 @@ def run_gpu(args):
                                peaks, args.workload)
     dense_path = _dense_path(step, wl, max(3, min(n_aux, 10)), flush, stream, peaks,
                              args.workload)
-    topk_path = _topk_path(wl, n_aux, flush, stream, peaks, dev)
+    topk_path = _topk_path(wl, n_aux, flush, stream, peaks, dev, args.workload)
     # index: read the top-k ids and write the slots (4 B each per entry),
     # read the row's request id and write its valid count
     index_roof = _hbm_roofline("smla_dcp_filter_convert_index", float(idx_ms.mean()),
                                8 * T * K + 8 * T, peaks,
-                               "8 B per top-k entry (id in, slot out) + 8 B per row")
+                               "8 B per top-k entry (id in, slot out) + 8 B per row",
+                               args.workload)
     # merge: D partial rows of 512 bf16 + fp32 lse in, one merged row out
     merge_roof = _hbm_roofline("smla_dcp_lse_merge", float(mrg_ms.mean()),
                                (D + 1) * T * H * (2 * V_DIM + 4), peaks,
-                               "(D + 1) x (1024 B out row + 4 B lse) per (token, head)")
+                               "(D + 1) x (1024 B out row + 4 B lse) per (token, head)",
+                               args.workload)
 
     # End to end through the public API with host buffers: every step copies
     # q and the top-k ids from pinned host memory and reads out + lse back.
