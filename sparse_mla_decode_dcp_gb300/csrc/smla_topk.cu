@@ -197,40 +197,50 @@ __device__ __forceinline__ void find_bucket(const uint32_t* hist, int nb, int ne
 // Bitonic sort (descending) of the kp = E * 1024 keys at `sel` (E >= 2):
 // strides of 32 E or more compare across warps in shared memory; the smaller
 // ones run in registers (thread t holds keys E t .. E t + E - 1) and warp
-// shuffles, without block barriers.
+// shuffles, without block barriers, the keys staying in registers from one
+// size to the next until a stride crosses warps.
 template <int E>
 __device__ void bitonic_sort_regs(uint64_t* sel, int kp) {
   const int tid = threadIdx.x;
+  uint64_t v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = sel[E * tid + e];
   for (int size = 2; size <= kp; size <<= 1) {
     int stride = size >> 1;
-    for (; stride >= 32 * E; stride >>= 1) {
-      for (int p = tid; p < kp / 2; p += kThreads) {
-        const int lo = 2 * p - (p & (stride - 1));
-        const int hi = lo + stride;
-        const bool desc = (lo & size) == 0;
-        const uint64_t x = sel[lo], y = sel[hi];
-        if ((x < y) == desc) {
-          sel[lo] = y;
-          sel[hi] = x;
-        }
-      }
-      __syncthreads();
-    }
-    uint64_t v[E];
+    if (stride >= 32 * E) {
+      // the keys go through shared memory only around strides that cross
+      // warps; runs of sizes up to 32 E stay in registers
 #pragma unroll
-    for (int e = 0; e < E; ++e) v[e] = sel[E * tid + e];
+      for (int e = 0; e < E; ++e) sel[E * tid + e] = v[e];
+      __syncthreads();
+      for (; stride >= 32 * E; stride >>= 1) {
+        for (int p = tid; p < kp / 2; p += kThreads) {
+          const int lo = 2 * p - (p & (stride - 1));
+          const int hi = lo + stride;
+          const bool desc = (lo & size) == 0;
+          const uint64_t x = sel[lo], y = sel[hi];
+          if ((x < y) == desc) {
+            sel[lo] = y;
+            sel[hi] = x;
+          }
+        }
+        __syncthreads();
+      }
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[e] = sel[E * tid + e];
+    }
     for (; stride >= E; stride >>= 1) {
-      // partner in lane ^ (stride / E), same slot
+      // partner in lane ^ (stride / E), same slot; with stride >= E the
+      // direction (bit `size`) and the side (bit `stride`) of key E t + e
+      // are those of E t, so one flag serves the thread's E keys: the lower
+      // index keeps the larger key when descending
       const int lm = stride / E;
+      const bool keep_max = ((E * tid) & stride) == 0 ? ((E * tid) & size) == 0
+                                                       : ((E * tid) & size) != 0;
 #pragma unroll
       for (int e = 0; e < E; ++e) {
-        const int g = E * tid + e;
         const uint64_t w = __shfl_xor_sync(0xffffffffu, v[e], lm);
-        const bool desc = (g & size) == 0;
-        const bool lower = (g & stride) == 0;
-        // the lower index keeps the larger key when descending
-        const bool keep_max = (lower == desc);
-        v[e] = keep_max ? (v[e] > w ? v[e] : w) : (v[e] < w ? v[e] : w);
+        v[e] = ((v[e] > w) == keep_max) ? v[e] : w;
       }
     }
     // strides below E: both keys in this thread (compile-time indices)
@@ -251,10 +261,10 @@ __device__ void bitonic_sort_regs(uint64_t* sel, int kp) {
         }
       }
     }
-#pragma unroll
-    for (int e = 0; e < E; ++e) sel[E * tid + e] = v[e];
-    __syncthreads();
   }
+#pragma unroll
+  for (int e = 0; e < E; ++e) sel[E * tid + e] = v[e];
+  __syncthreads();
 }
 
 // The plain shared-memory network, for kp < 2048 and kp = 16384 (whose 16
@@ -346,22 +356,66 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
   const int need = select ? s_need : 0;
   const int nabove = select ? K - need : int(total);  // keys above the boundary bin
   // 2) keys of higher bins -> their bin's places in `sel`; the boundary bin ->
-  //    this warp's region of `bnd` (most keys lie below the boundary: one
-  //    ballot skips them)
-  int wc = 0;  // this warp's boundary keys (warp-uniform)
+  //    this warp's region of `bnd`.  The pass over the row only queues the
+  //    candidates at or above the boundary bin in the warp's region (score
+  //    key and position packed; most candidates lie below: one ballot skips
+  //    them), and each warp then places its queue: a warp whose lanes mostly
+  //    skip then pays nothing for the few that take.  When a queue outgrows
+  //    its region (ties or a narrow score range), the row is read again and
+  //    every key placed as it comes.
+  const uint32_t lt = (1u << lane) - 1u;
+  int wc = 0;  // this warp's queued candidates (warp-uniform)
   for_each_candidate<kExplicit, kVec4>(a, i, span, [&](bool ok, uint32_t sk, int32_t x) {
-    const int kb = int(sk >> (32 - kBinBits));
-    const bool take = ok && kb >= bin;
-    if (__ballot_sync(0xffffffffu, take) == 0) return;
-    const uint64_t key = make_key(sk, kExplicit ? x : (take ? global_id(a, x) : 0));
-    if (take && kb > bin) sel[atomicAdd(&cur[kb], 1u)] = key;
-    const uint32_t m = __ballot_sync(0xffffffffu, take && kb == bin);
-    if (take && kb == bin) {
-      const int q = wc + __popc(m & ((1u << lane) - 1u));
-      if (q < reg) bnd[warp * reg + q] = key;
+    const bool take = ok && int(sk >> (32 - kBinBits)) >= bin;
+    const uint32_t m = __ballot_sync(0xffffffffu, take);
+    if (m == 0) return;
+    if (take) {
+      const int q = wc + __popc(m & lt);
+      if (q < reg) bnd[warp * reg + q] = (uint64_t(sk) << 32) | uint32_t(x);
     }
     wc += __popc(m);
   });
+  if (lane == 0) wcount[warp] = wc;
+  __syncthreads();
+  bool queued = true;
+  for (int w = 0; w < kWarps; ++w) queued &= wcount[w] <= reg;
+  __syncthreads();  // every warp has read the counts
+  if (queued) {
+    // place this warp's queue; its boundary keys move to the front of the
+    // region (an entry is read before any write reaches its slot)
+    const int nq = wc;
+    wc = 0;  // now: this warp's boundary keys
+    uint64_t* region = bnd + warp * reg;
+    for (int q0 = 0; q0 < nq; q0 += 32) {
+      const int q = q0 + lane;
+      const uint64_t e = q < nq ? region[q] : 0;
+      const uint32_t sk = uint32_t(e >> 32);
+      const int32_t x = int32_t(uint32_t(e));
+      const int kb = int(sk >> (32 - kBinBits));
+      const bool hi = q < nq && kb > bin;
+      const bool bd = q < nq && kb == bin;
+      const uint64_t key = make_key(sk, kExplicit ? x : (q < nq ? global_id(a, x) : 0));
+      if (hi) sel[atomicAdd(&cur[kb], 1u)] = key;
+      const uint32_t m = __ballot_sync(0xffffffffu, bd);
+      if (bd) region[wc + __popc(m & lt)] = key;
+      wc += __popc(m);
+    }
+  } else {
+    wc = 0;  // this warp's boundary keys
+    for_each_candidate<kExplicit, kVec4>(a, i, span, [&](bool ok, uint32_t sk, int32_t x) {
+      const int kb = int(sk >> (32 - kBinBits));
+      const bool take = ok && kb >= bin;
+      if (__ballot_sync(0xffffffffu, take) == 0) return;
+      const uint64_t key = make_key(sk, kExplicit ? x : (take ? global_id(a, x) : 0));
+      if (take && kb > bin) sel[atomicAdd(&cur[kb], 1u)] = key;
+      const uint32_t m = __ballot_sync(0xffffffffu, take && kb == bin);
+      if (take && kb == bin) {
+        const int q = wc + __popc(m & lt);
+        if (q < reg) bnd[warp * reg + q] = key;
+      }
+      wc += __popc(m);
+    });
+  }
   if (lane == 0) wcount[warp] = wc;
   __syncthreads();
   bool overflow = false;
