@@ -309,7 +309,9 @@ smla_status smla_dcp_sparse_mla_decode_fused(
  * that point.  The groups run on library-owned streams and events (created
  * on a device's first call, kept until the process exits); the call is
  * serialised per device, so concurrent calls from several host threads
- * queue one after the other.
+ * queue one after the other.  Made inside CUDA stream capture on `stream`
+ * (after one call outside it on the device), the library's streams join the
+ * capture through those events and the graph replays the whole step.
  * Errors: as smla_dcp_sparse_mla_decode_fused, plus INVALID_ARG for a null
  * or misaligned host or staging buffer or chunks outside [1,
  * SMLA_MAX_HOST_CHUNKS]; UNSUPPORTED for chunks > 1 with K > 2048.

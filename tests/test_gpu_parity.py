@@ -547,6 +547,37 @@ def test_fused_host_equals_device_step(cuda_device, chunks):
     assert torch.equal(step.q.cpu(), q_host) and torch.equal(step.topk.cpu(), topk_host)
 
 
+def test_fused_host_replays_in_cuda_graph(cuda_device):
+    """The host-buffer step captured in a CUDA graph (its copy, group and
+    copy-out streams join the capture through their events) replays to the
+    device step's results, the host buffers refilled on every replay."""
+    dev = cuda_device
+    wl = inputs.make_workload("dcp4_long", seed=4, device=dev)
+    step = DcpDecodeStep(wl, device=dev)
+    ref_out, ref_lse = step.run_fused()
+    torch.cuda.synchronize()
+    ref_out, ref_lse = ref_out.cpu(), ref_lse.cpu()
+    q_host, topk_host = _pinned(step.q), _pinned(step.topk)
+    out_host = torch.empty(tuple(ref_out.shape), dtype=torch.bfloat16).pin_memory()
+    lse_host = torch.empty(tuple(ref_lse.shape), dtype=torch.float32).pin_memory()
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    step.stream = s
+    with torch.cuda.stream(s):
+        step.run_fused_from_host(q_host, topk_host, out_host, lse_host, chunks=4)  # warm-up
+        s.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            step.run_fused_from_host(q_host, topk_host, out_host, lse_host, chunks=4)
+    for _ in range(2):
+        out_host.fill_(7)
+        lse_host.fill_(7.0)
+        step.q.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out_host, ref_out) and torch.equal(lse_host, ref_lse)
+
+
 def test_fused_host_ragged_groups_match_oracle(cuda_device):
     """5 rows in 3 groups (2, 2, 1), each decoded without split-K, against
     the oracle's per-shard decode and merge; one row's ids all -1."""
