@@ -578,9 +578,12 @@ def test_fused_host_replays_in_cuda_graph(cuda_device):
         assert torch.equal(out_host, ref_out) and torch.equal(lse_host, ref_lse)
 
 
-def test_fused_host_ragged_groups_match_oracle(cuda_device):
-    """5 rows in 3 groups (2, 2, 1), each decoded without split-K, against
-    the oracle's per-shard decode and merge; one row's ids all -1."""
+@pytest.mark.parametrize("chunks", [1, 3, 8])
+def test_fused_host_ragged_groups_match_oracle(cuda_device, chunks):
+    """5 rows in one group (then split-K over the workspace), in 3 groups
+    (2, 2, 1) or in 8 asked for (one row per group), the groups decoded
+    without split-K, against the oracle's per-shard decode and merge; one
+    row's ids all -1."""
     dev = cuda_device
     spec = inputs.WorkloadSpec(
         name="host_ragged", num_reqs=5, tokens_per_req=1, heads=128, topk=2048, dcp=2,
@@ -592,7 +595,7 @@ def test_fused_host_ragged_groups_match_oracle(cuda_device):
     out_host = torch.empty((wl.T, wl.H, 512), dtype=torch.bfloat16).pin_memory()
     lse_host = torch.empty((wl.T, wl.H), dtype=torch.float32).pin_memory()
     capi.get_device_error(clear=True)
-    step.run_fused_from_host(q_host, topk_host, out_host, lse_host, chunks=3)
+    step.run_fused_from_host(q_host, topk_host, out_host, lse_host, chunks=chunks)
     torch.cuda.synchronize()
     assert capi.get_device_error(clear=True) == 0
     q = _q_bits(wl.q)
@@ -604,7 +607,7 @@ def test_fused_host_ragged_groups_match_oracle(cuda_device):
         outs.append(o)
         lses.append(l)
     ref_out, ref_lse = oracle.lse_merge(outs, lses)
-    compare_out_lse(out_host, lse_host, ref_out, ref_lse, where="fused from host, 3 groups")
+    compare_out_lse(out_host, lse_host, ref_out, ref_lse, where=f"fused from host, chunks={chunks}")
     assert torch.all(out_host[3].view(torch.int16) == 0) and torch.isneginf(lse_host[3]).all()
 
 
