@@ -324,6 +324,35 @@ def test_fused_small_batches_split_k(cuda_device, K):
     compare_out_lse(out, lse, ref_out, ref_lse, where=f"pipeline K={K}")
 
 
+@pytest.mark.parametrize("H,D,I", [(16, 3, 2), (100, 2, 1), (1, 5, 4)])
+def test_fused_split_k_heads_shards_interleave(cuda_device, H, D, I):
+    """The fused step with split-K (2 rows, 4 key ranges each, combined by
+    the separate kernel) over head counts that leave an 8-head group part
+    empty, odd shard counts and interleave sizes."""
+    dev = cuda_device
+    spec = inputs.WorkloadSpec(
+        name=f"fused_sk_{H}_{D}_{I}", num_reqs=2, tokens_per_req=1, heads=H, topk=1024, dcp=D,
+        block_size=16, ctx_kind="uniform", ctx_lo=700, ctx_hi=5000, interleave=I,
+        neg_frac=0.1)
+    wl = inputs.make_workload(spec, seed=H + 10 * D + I, device=dev)
+    assert capi.decode_workspace_size(wl.T, H, wl.K) > 0
+    step = DcpDecodeStep(wl, device=dev)
+    capi.get_device_error(clear=True)
+    f_out, f_lse = step.run_fused()
+    torch.cuda.synchronize()
+    assert capi.get_device_error(clear=True) == 0
+    q_bits = _q_bits(wl.q)
+    outs, lses = [], []
+    for d, sh in enumerate(wl.shards):
+        sl, _ = oracle.dcp_filter_convert_index(wl.req_id, sh.block_table, wl.topk, wl.D, d,
+                                                spec.block_size, I)
+        o, l = oracle.sparse_mla_decode(q_bits, sh.pool.cpu().numpy(), sl, spec.sm_scale)
+        outs.append(o)
+        lses.append(l)
+    ref_out, ref_lse = oracle.lse_merge(outs, lses)
+    compare_out_lse(f_out, f_lse, ref_out, ref_lse, where=f"fused split-K H={H} D={D} I={I}")
+
+
 @pytest.mark.parametrize("interleave", [2, 4, 64])
 def test_interleaved_step_matches_oracle(cuda_device, interleave):
     """Interleave size I > 1 (runs of I consecutive positions per shard) end
