@@ -126,6 +126,7 @@ struct Ctl {
   const int32_t* bt_row[kMaxMerge];
   ShardMeta meta[kMaxMerge];
   int bt_staged;              // the rows fit the staging area
+  int sm_abort;               // a softmax warp gave up on a wait (loop exit)
 };
 static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -839,14 +840,19 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
       for (int j = 0; j < 32; ++j) sown[j] = C ? s[32 + j] : s[j];
       return true;
     };
+    // The four softmax warps leave the loop together: a warp whose wait gave
+    // up records it and arrives (without waiting) at the tile's barrier (at
+    // give_up below), which the others then complete and leave after; every
+    // exit lies before that barrier, so its count always completes.
     bool ok = ntiles == 0 || start_tile(0);
+    ok = !named_bar_or(5, 128, !ok);
     for (int i = 0; i < ntiles && ok; ++i) {
       const int b = i & 1;
       const uint32_t xa_l = smem_u32(xbase) + b * kXBytes;  // this CTA's buffer set b
       const uint32_t xa_p = peer_x + b * kXBytes;           // the peer's
       // 1) full scores of this CTA's columns of tile i
       ok = __all_sync(0xffffffffu, wait_bar_cluster(&ctl->xa[b], (i >> 1) & 1, abort, kWsExchange));
-      if (!ok) break;
+      if (!ok) goto give_up;
       float f[32];
 #pragma unroll
       for (int j4 = 0; j4 < 8; ++j4) {
@@ -906,13 +912,10 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
       st_async_v2(xb_p + kXBPBytes + h * 8, my_ref, l_part, xbb);
       // 4) while that is in flight: tile i + 1's scores (its QK^T could start
       //    once S(i) was read)
-      if (i + 1 < ntiles && !start_tile(i + 1)) {
-        ok = false;
-        break;
-      }
+      if (i + 1 < ntiles && !start_tile(i + 1)) goto give_up;
       // 5) the peer's P of tile i
       ok = __all_sync(0xffffffffu, wait_bar_cluster(&ctl->xb[b], (i >> 1) & 1, abort, kWsExchangeP));
-      if (!ok) break;
+      if (!ok) goto give_up;
       const uint32_t xb_l = xa_l + kXABytes;
       uint32_t pp[16];
 #pragma unroll
@@ -953,7 +956,7 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
       l = l * alpha + (C ? l_peer + l_own : l_own + l_peer);
       if (i > 0) {
         ok = __all_sync(0xffffffffu, wait_bar(&ctl->pv_done, (i - 1) & 1, abort, kWsPvDone));
-        if (!ok) break;
+        if (!ok) goto give_up;
         tc_fence_after();
       }
       // P(i) replaces P(i-1), which PV(i-1) has finished reading: keys
@@ -989,6 +992,23 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
         mma_commit(&ctl->freed[i % kStages]);
         pv_issued = i + 1;
       }
+      // read after PV(i) is on its way (off the path to it): a warp gave up
+      // in this tile (its rows of P may be missing; the call reports the
+      // timeout and its output is not used)
+      if (*reinterpret_cast<volatile int*>(&ctl->sm_abort)) {
+        ok = false;
+        break;
+      }
+    }
+    if (false) {
+    give_up:
+      // this warp's wait gave up inside a tile: it records that and arrives
+      // (without waiting) at the tile's barrier, which the other warps then
+      // complete and leave after
+      ok = false;
+      ctl->sm_abort = 1;
+      __threadfence_block();
+      named_bar_arrive(5, 128);
     }
     // epilogue
     if (ok && ntiles > 0) {
@@ -1248,6 +1268,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&ctl->end, 1);
     mbar_init(&ctl->end_pv, 1);
     ctl->abort = 0;
+    ctl->sm_abort = 0;
     fence_mbar_init_cluster();
     // q lands in the (still idle) operand stages while the CTA sets up
     issue_q_tma(a, t, hr.c, smem_u32(sm + kOffOp), &ctl->q_tma);
