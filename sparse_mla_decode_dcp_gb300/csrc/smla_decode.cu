@@ -126,7 +126,7 @@ struct Ctl {
   const int32_t* bt_row[kMaxMerge];
   ShardMeta meta[kMaxMerge];
   int bt_staged;              // the rows fit the staging area
-  int sm_abort;               // a softmax warp gave up on a wait (loop exit)
+  int sm_abort;               // 1 + the first tile in which a softmax warp gave up (0: none)
 };
 static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -846,7 +846,8 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
     // exit lies before that barrier, so its count always completes.
     bool ok = ntiles == 0 || start_tile(0);
     ok = !named_bar_or(5, 128, !ok);
-    for (int i = 0; i < ntiles && ok; ++i) {
+    int i = 0;
+    for (; i < ntiles && ok; ++i) {
       const int b = i & 1;
       const uint32_t xa_l = smem_u32(xbase) + b * kXBytes;  // this CTA's buffer set b
       const uint32_t xa_p = peer_x + b * kXBytes;           // the peer's
@@ -993,20 +994,25 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
         pv_issued = i + 1;
       }
       // read after PV(i) is on its way (off the path to it): a warp gave up
-      // in this tile (its rows of P may be missing; the call reports the
-      // timeout and its output is not used)
-      if (*reinterpret_cast<volatile int*>(&ctl->sm_abort)) {
-        ok = false;
-        break;
+      // in this tile or before (its rows of P may be missing; the call
+      // reports the timeout and its output is not used).  A give-up in a
+      // later tile, by a warp already past this barrier, is left to that
+      // tile's barrier, which every warp still in the loop passes.
+      {
+        const int first = *reinterpret_cast<volatile int*>(&ctl->sm_abort);
+        if (first != 0 && first <= i + 1) {
+          ok = false;
+          break;
+        }
       }
     }
     if (false) {
     give_up:
-      // this warp's wait gave up inside a tile: it records that and arrives
-      // (without waiting) at the tile's barrier, which the other warps then
-      // complete and leave after
+      // this warp's wait gave up inside tile i: it records the first such
+      // tile (1 + its index) and arrives (without waiting) at the tile's
+      // barrier, which the other warps then complete and leave after
       ok = false;
-      ctl->sm_abort = 1;
+      atomicCAS(&ctl->sm_abort, 0, i + 1);
       __threadfence_block();
       named_bar_arrive(5, 128);
     }
