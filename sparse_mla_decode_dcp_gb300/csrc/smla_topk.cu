@@ -23,8 +23,9 @@
 //      (a counting sort by bin) and the boundary bin's keys in per-warp lists;
 //   3. a most-significant-digit radix select over the boundary bin's keys (8
 //      bits per step, in shared memory) picks those still needed;
-//   4. a bitonic network sorts the K selected keys (in registers and warp
-//      shuffles below 32 keys per warp apart).
+//   4. the K selected keys are sorted: each warp's run in registers by a
+//      bitonic network, then the runs by merges along the merge path (K up
+//      to 4096; larger K: the bitonic network throughout).
 // Only when the boundary bin overflows the per-warp lists (scores tied far
 // beyond K) does step 3 read the row from global memory again, digit by
 // digit.
@@ -267,6 +268,88 @@ __device__ void bitonic_sort_regs(uint64_t* sel, int kp) {
   __syncthreads();
 }
 
+// Descending sort of the kp = E * 1024 keys at `sel` by runs and merges:
+// each warp first sorts its 32 E keys in registers (the bitonic network
+// above, every run's last merge descending), then log2(kp / (32 E)) levels
+// merge pairs of runs between `tmp` and `sel`: thread t writes outputs
+// E t .. E t + E - 1 of its pair, finding how many of the first come from
+// each run by a binary search along the merge path (equal keys -- only the
+// zero padding -- are taken from the second run first, in the search as in
+// the merge).  One block barrier per level instead of one per cross-warp
+// stride of the bitonic network.
+template <int E>
+__device__ void merge_sort_desc(uint64_t* sel, uint64_t* tmp, int kp) {
+  const int tid = threadIdx.x;
+  constexpr int kRun = 32 * E;
+  uint64_t v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = sel[E * tid + e];
+  for (int size = 2; size <= kRun; size <<= 1) {
+    const bool last = size == kRun;  // the run's final merge: all descending
+    int stride = size >> 1;
+    for (; stride >= E; stride >>= 1) {
+      const int lm = stride / E;
+      const bool desc = last || ((E * tid) & size) == 0;
+      const bool keep_max = ((E * tid) & stride) == 0 ? desc : !desc;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const uint64_t w = __shfl_xor_sync(0xffffffffu, v[e], lm);
+        v[e] = ((v[e] > w) == keep_max) ? v[e] : w;
+      }
+    }
+#pragma unroll
+    for (int st = E / 2; st > 0; st >>= 1) {
+      if (st <= stride) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          if ((e & st) == 0) {
+            const bool desc = last || ((E * tid + e) & size) == 0;
+            const uint64_t x = v[e], y = v[e + st];
+            if ((x < y) == desc) {
+              v[e] = y;
+              v[e + st] = x;
+            }
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) tmp[E * tid + e] = v[e];
+  __syncthreads();
+  uint64_t* src = tmp;
+  uint64_t* dst = sel;
+  for (int R = kRun; R < kp; R <<= 1) {
+    const int k = E * tid;
+    const int base = k & ~(2 * R - 1);
+    const int k0 = k - base;  // this thread's first output within the pair
+    const uint64_t* A = src + base;
+    const uint64_t* B = A + R;
+    int lo = max(0, k0 - R), hi = min(k0, R);
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (A[mid] > B[k0 - mid - 1])
+        lo = mid + 1;
+      else
+        hi = mid;
+    }
+    int ia = lo, ib = k0 - lo;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const bool take_a = ib >= R || (ia < R && A[ia] > B[ib]);
+      dst[k + e] = take_a ? A[ia++] : B[ib++];
+    }
+    __syncthreads();
+    uint64_t* t = src;
+    src = dst;
+    dst = t;
+  }
+  if (src != sel) {  // an even number of levels: the result is in tmp
+    for (int p = tid; p < kp; p += kThreads) sel[p] = src[p];
+    __syncthreads();
+  }
+}
+
 // The plain shared-memory network, for kp < 2048 and kp = 16384 (whose 16
 // keys per thread would not fit the registers).
 __device__ void bitonic_sort_smem(uint64_t* sel, int kp) {
@@ -435,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
   // 3) the `need` largest keys of the boundary bin by a radix select over
   //    its keys, gathered into one list (a pass over global memory replaces
   //    the list when the bin overflowed the warps' regions: ties far beyond
-  //    K), then a bitonic sort of `sel`
+  //    K), then a sort of `sel`
   if (tid == 0) s_nsel = nabove;
   if (select) {
     const bool in_smem = !overflow;
@@ -518,9 +601,11 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
   __syncthreads();
   for (int p = kept + tid; p < a.kp; p += kThreads) sel[p] = 0;  // below every candidate
   __syncthreads();
+  // the histogram and cursors are free again: the merge sort's second buffer
+  static_assert(2 * kHistBytes >= 4096 * 8, "the merge buffer holds 4096 keys");
   switch (a.kp) {
-    case 2048: bitonic_sort_regs<2>(sel, a.kp); break;
-    case 4096: bitonic_sort_regs<4>(sel, a.kp); break;
+    case 2048: merge_sort_desc<2>(sel, reinterpret_cast<uint64_t*>(smem), a.kp); break;
+    case 4096: merge_sort_desc<4>(sel, reinterpret_cast<uint64_t*>(smem), a.kp); break;
     case 8192: bitonic_sort_regs<8>(sel, a.kp); break;
     default: bitonic_sort_smem(sel, a.kp); break;
   }
