@@ -85,7 +85,7 @@ __device__ __forceinline__ int32_t global_id(const TopkArgs& a, int j) {
 }
 
 // Visit every candidate of row i, all lanes of a warp together: f(valid,
-// score key, x) is called by every lane, x the candidate's id (merge: entry
+// score, x) is called by every lane, x the candidate's id (merge: entry
 // j < M, skipped when its id is -1) or its local position j < n (select:
 // global_id(x) is its id, computed only where needed).  A thread keeps
 // kUnroll loads in flight: a gather's rate is set by the bytes in flight.
@@ -111,10 +111,10 @@ __device__ __forceinline__ void for_each_candidate(const TopkArgs& a, int64_t i,
       for (int u = 0; u < kUnroll; ++u) {
         const int q = q0 + u * kThreads;
         const int j = head + 4 * q;
-        f(q < nq, score_key(v[u].x), j);
-        f(q < nq, score_key(v[u].y), j + 1);
-        f(q < nq, score_key(v[u].z), j + 2);
-        f(q < nq, score_key(v[u].w), j + 3);
+        f(q < nq, v[u].x, j);
+        f(q < nq, v[u].y, j + 1);
+        f(q < nq, v[u].z, j + 2);
+        f(q < nq, v[u].w, j + 3);
       }
     }
     if (threadIdx.x < 32 && head + tail > 0) {
@@ -122,7 +122,7 @@ __device__ __forceinline__ void for_each_candidate(const TopkArgs& a, int64_t i,
       const bool ok = l < head + tail;
       const int j = l < head ? l : head + 4 * nq + (l - head);
       const float sc = ok ? __ldg(srow + j) : 0.f;
-      f(ok, score_key(sc), ok ? j : 0);
+      f(ok, sc, ok ? j : 0);
     }
     return;
   }
@@ -141,9 +141,9 @@ __device__ __forceinline__ void for_each_candidate(const TopkArgs& a, int64_t i,
     for (int u = 0; u < kUnroll; ++u) {
       const int j = j0 + u * kThreads;
       if (kExplicit)
-        f(j < span && id[u] >= 0, score_key(sc[u]), id[u]);
+        f(j < span && id[u] >= 0, sc[u], id[u]);
       else
-        f(j < span, score_key(sc[u]), j);
+        f(j < span, sc[u], j);
     }
   }
 }
@@ -393,8 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
   // 1) histogram of the keys' top 12 bits
   for (int b = tid; b < kBins; b += kThreads) hist[b] = 0;
   __syncthreads();
-  for_each_candidate<kExplicit, kVec4>(a, i, span, [&](bool ok, uint32_t sk, int32_t) {
-    if (ok) atomicAdd(&hist[sk >> (32 - kBinBits)], 1u);
+  for_each_candidate<kExplicit, kVec4>(a, i, span, [&](bool ok, float sc, int32_t) {
+    if (ok) atomicAdd(&hist[score_key(sc) >> (32 - kBinBits)], 1u);
   });
   __syncthreads();
   // suffix sums over bins: thread t owns bins 4t .. 4t + 3
@@ -446,15 +446,22 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
   //    skip then pays nothing for the few that take.  When a queue outgrows
   //    its region (ties or a narrow score range), the row is read again and
   //    every key placed as it comes.
+  //    A candidate is at or above the boundary bin when its score is at
+  //    least the bin's lower edge (one float compare; its key is built only
+  //    when taken): the edge is the score whose key starts the bin, -inf for
+  //    bins below -inf's key (only -inf lies there), and bin 0 (NaN's) or no
+  //    boundary takes every candidate.
   const uint32_t lt = (1u << lane) - 1u;
+  const bool take_all = bin <= 0;
+  const float edge = key_score(max(uint32_t(max(bin, 0)) << (32 - kBinBits), score_key(-INFINITY)));
   int wc = 0;  // this warp's queued candidates (warp-uniform)
-  for_each_candidate<kExplicit, kVec4>(a, i, span, [&](bool ok, uint32_t sk, int32_t x) {
-    const bool take = ok && int(sk >> (32 - kBinBits)) >= bin;
+  for_each_candidate<kExplicit, kVec4>(a, i, span, [&](bool ok, float sc, int32_t x) {
+    const bool take = ok && (take_all || sc >= edge);
     const uint32_t m = __ballot_sync(0xffffffffu, take);
     if (m == 0) return;
     if (take) {
       const int q = wc + __popc(m & lt);
-      if (q < reg) bnd[warp * reg + q] = (uint64_t(sk) << 32) | uint32_t(x);
+      if (q < reg) bnd[warp * reg + q] = (uint64_t(score_key(sc)) << 32) | uint32_t(x);
     }
     wc += __popc(m);
   });
@@ -485,7 +492,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
     }
   } else {
     wc = 0;  // this warp's boundary keys
-    for_each_candidate<kExplicit, kVec4>(a, i, span, [&](bool ok, uint32_t sk, int32_t x) {
+    for_each_candidate<kExplicit, kVec4>(a, i, span, [&](bool ok, float sc, int32_t x) {
+      const uint32_t sk = score_key(sc);
       const int kb = int(sk >> (32 - kBinBits));
       const bool take = ok && kb >= bin;
       if (__ballot_sync(0xffffffffu, take) == 0) return;
@@ -562,7 +570,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
       if (in_smem) {
         for (int u = tid; u < nb; u += kThreads) count(bnd[u]);
       } else {
-        for_each_candidate<kExplicit, false>(a, i, span, [&](bool ok, uint32_t sk, int32_t x) {
+        for_each_candidate<kExplicit, false>(a, i, span, [&](bool ok, float sc, int32_t x) {
+          const uint32_t sk = score_key(sc);
           if (ok && int(sk >> (32 - kBinBits)) == bin)
             count(make_key(sk, kExplicit ? x : global_id(a, x)));
         });
@@ -591,7 +600,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
         append(u < nb && (key & mask) >= prefix, key, sel, &s_nsel, a.kp);
       }
     } else {
-      for_each_candidate<kExplicit, false>(a, i, span, [&](bool ok, uint32_t sk, int32_t x) {
+      for_each_candidate<kExplicit, false>(a, i, span, [&](bool ok, float sc, int32_t x) {
+        const uint32_t sk = score_key(sc);
         const bool inbin = ok && int(sk >> (32 - kBinBits)) == bin;
         const uint64_t key = make_key(sk, kExplicit ? x : (inbin ? global_id(a, x) : 0));
         append(inbin && (key & mask) >= prefix, key, sel, &s_nsel, a.kp);

@@ -1022,9 +1022,13 @@ def _topk_vs_oracle(dev, scores64, n_cand, K, where):
     assert np.array_equal(got.cpu().numpy(), want), where
 
 
-@pytest.mark.parametrize("L,K", [(97, 16), (5000, 2048), (131072, 2048), (40000, 16384)])
+@pytest.mark.parametrize("L,K", [(97, 16), (3000, 1000), (5000, 2048), (131072, 2048),
+                                 (50000, 3001), (20000, 4096), (30000, 8192), (40000, 16384)])
 def test_topk_select_matches_oracle(cuda_device, L, K):
-    """Random rows up to 128k candidates, some shorter than K: bit-exact ids."""
+    """Random rows up to 128k candidates, some shorter than K: bit-exact ids.
+    K covers every sort the kernel picks by the padded size kp: the shared-
+    memory network (kp 1024, 16384), warp runs and merges (kp 2048, 4096),
+    the register network (kp 8192)."""
     rng = np.random.default_rng(L + K)
     T = 6
     scores = rng.standard_normal((T, L))
