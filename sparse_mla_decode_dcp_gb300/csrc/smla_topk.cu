@@ -29,6 +29,9 @@
 // Only when the boundary bin overflows the per-warp lists (scores tied far
 // beyond K) does step 3 read the row from global memory again, digit by
 // digit.
+#include <atomic>
+#include <mutex>
+
 #include "../../include/smla.h"
 #include "smla_internal.h"
 
@@ -635,10 +638,28 @@ int pow2_at_least(int x) {
   return p;
 }
 
+// The kernel's shared-memory opt-in, set once per device and kernel form.
+constexpr int kMaxDevices = 64;
+template <bool kExplicit, bool kVec4>
+cudaError_t ensure_smem_attribute() {
+  static std::atomic<bool> done[kMaxDevices];
+  static std::mutex m;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool tracked = dev >= 0 && dev < kMaxDevices;
+  if (tracked && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(m);
+  if (tracked && done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  e = cudaFuncSetAttribute(topk_kernel<kExplicit, kVec4>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess && tracked) done[dev].store(true, std::memory_order_release);
+  return e;
+}
+
 template <bool kExplicit, bool kVec4>
 cudaError_t launch(TopkArgs a, int cap, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(topk_kernel<kExplicit, kVec4>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = ensure_smem_attribute<kExplicit, kVec4>();
   if (e != cudaSuccess) return e;
   topk_kernel<kExplicit, kVec4><<<dim3(unsigned(a.T)), dim3(kThreads), kSmemBytes, s>>>(a, cap);
   return cudaGetLastError();
