@@ -115,7 +115,7 @@ struct __align__(16) ShardMeta {
 
 struct Ctl {
   uint64_t q_tma, q_ready, full[kStages], freed[kStages], raw_full[kRawStages], raw_empty[kRawStages],
-      s_full, s_free, pv_done, xa[2][4], xb[2][4], end, end_pv;  // exchanges: per buffer set and softmax warp
+      s_full, s_free, pv_done, xa[2], xb[2], end, end_pv;
   uint32_t tbase;
   int n_list;
   int abort;
@@ -789,23 +789,18 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
     // max(own reference, peer reference), so O, l and P stay consistent.
     // Buffers alternate by tile parity: the peer writes tile i into buffer
     // set i % 2 only after it has received this CTA's tile-i partial scores,
-    // which this CTA sent after it had read tile i - 2 out of that set.  All
-    // of it holds warp by warp: softmax warp w only ever reads, writes and
-    // waits for head rows [32w, 32w + 32), on barriers of its own.
+    // which this CTA sent after it had read tile i - 2 out of that set.
     const int oc0 = 32 * C;  // this CTA's key columns (the peer's: 32 (1 - C) ..)
     uint8_t* xbase = sm + kOffX;
     const uint32_t peer_x = map_to_cta(smem_u32(xbase), peer);
-    // each softmax warp exchanges its 32 head rows with the peer's warp of
-    // the same rows, on a barrier of its own (no warp waits for the others'
-    // transfers)
-    const uint32_t peer_xa0 = map_to_cta(smem_u32(&ctl->xa[0][warp]), peer);
-    const uint32_t peer_xa1 = map_to_cta(smem_u32(&ctl->xa[1][warp]), peer);
-    const uint32_t peer_xb0 = map_to_cta(smem_u32(&ctl->xb[0][warp]), peer);
-    const uint32_t peer_xb1 = map_to_cta(smem_u32(&ctl->xb[1][warp]), peer);
-    if (lane == 0) {
+    const uint32_t peer_xa0 = map_to_cta(smem_u32(&ctl->xa[0]), peer);
+    const uint32_t peer_xa1 = map_to_cta(smem_u32(&ctl->xa[1]), peer);
+    const uint32_t peer_xb0 = map_to_cta(smem_u32(&ctl->xb[0]), peer);
+    const uint32_t peer_xb1 = map_to_cta(smem_u32(&ctl->xb[1]), peer);
+    if (h == 0) {
       for (int b = 0; b < 2 && b < ntiles; ++b) {
-        mbar_arrive_expect_tx(&ctl->xa[b][warp], kXABytes / 4);
-        mbar_arrive_expect_tx(&ctl->xb[b][warp], kXBBytes / 4);
+        mbar_arrive_expect_tx(&ctl->xa[b], kXABytes);
+        mbar_arrive_expect_tx(&ctl->xb[b], kXBBytes);
       }
     }
     // The loop is software-pipelined across tiles: while the P of tile i is
@@ -857,7 +852,7 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
       const uint32_t xa_l = smem_u32(xbase) + b * kXBytes;  // this CTA's buffer set b
       const uint32_t xa_p = peer_x + b * kXBytes;           // the peer's
       // 1) full scores of this CTA's columns of tile i
-      ok = __all_sync(0xffffffffu, wait_bar_cluster(&ctl->xa[b][warp], (i >> 1) & 1, abort, kWsExchange));
+      ok = __all_sync(0xffffffffu, wait_bar_cluster(&ctl->xa[b], (i >> 1) & 1, abort, kWsExchange));
       if (!ok) goto give_up;
       float f[32];
 #pragma unroll
@@ -868,7 +863,7 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
         f[4 * j4 + 2] = sown[4 * j4 + 2] + v.z;
         f[4 * j4 + 3] = sown[4 * j4 + 3] + v.w;
       }
-      if (lane == 0 && i + 2 < ntiles) mbar_arrive_expect_tx(&ctl->xa[b][warp], kXABytes / 4);
+      if (h == 0 && i + 2 < ntiles) mbar_arrive_expect_tx(&ctl->xa[b], kXABytes);
       const int valid = min(kTileN, n - i * kTileN) - oc0;  // valid columns of this CTA's 32
       if (valid < 32) {
 #pragma unroll
@@ -920,7 +915,7 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
       //    once S(i) was read)
       if (i + 1 < ntiles && !start_tile(i + 1)) goto give_up;
       // 5) the peer's P of tile i
-      ok = __all_sync(0xffffffffu, wait_bar_cluster(&ctl->xb[b][warp], (i >> 1) & 1, abort, kWsExchangeP));
+      ok = __all_sync(0xffffffffu, wait_bar_cluster(&ctl->xb[b], (i >> 1) & 1, abort, kWsExchangeP));
       if (!ok) goto give_up;
       const uint32_t xb_l = xa_l + kXABytes;
       uint32_t pp[16];
@@ -933,7 +928,7 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
         pp[4 * q + 3] = v.w;
       }
       const float2 peer_rl = ld_shared_f2(xb_l + kXBPBytes + h * 8);
-      if (lane == 0 && i + 2 < ntiles) mbar_arrive_expect_tx(&ctl->xb[b][warp], kXBBytes / 4);
+      if (h == 0 && i + 2 < ntiles) mbar_arrive_expect_tx(&ctl->xb[b], kXBBytes);
       // 6) the shared reference moves to the larger of the two (identically
       //    on both CTAs); what was computed against a smaller one is redone
       const float r_new = fmaxf(my_ref, peer_rl.x);
@@ -1273,10 +1268,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->raw_empty[st], 4);        // one arrival per converter warp
     }
     for (int b = 0; b < 2; ++b) {
-      for (int w = 0; w < 4; ++w) {
-        mbar_init(&ctl->xa[b][w], 1);  // one expect_tx arrival per phase
-        mbar_init(&ctl->xb[b][w], 1);
-      }
+      mbar_init(&ctl->xa[b], 1);  // one expect_tx arrival per phase
+      mbar_init(&ctl->xb[b], 1);
     }
     mbar_init(&ctl->end, 1);
     mbar_init(&ctl->end_pv, 1);
