@@ -40,10 +40,11 @@
 //     more than 2^8.
 //
 // Warp roles (384 threads): warps 0-3 softmax/epilogue (TMEM lanes 0-127,
-// one head row per thread; thread 0 also issues each tile's PV as soon as
-// the four warps have stored P), warps 4-7 dequantise, warp 8 allocates TMEM
-// and issues QK^T (one thread), warps 9-11 gather.  Every wait is bounded; a
-// wait that runs out sets SMLA_DEVERR_TIMEOUT and the CTA unwinds.
+// one head row per thread), warps 4-7 dequantise, warp 8 allocates TMEM and
+// issues every MMA (one thread: QK^T of a tile, then PV of the tile two
+// before it, once the softmax has stored that tile's P), warps 9-11 gather.
+// Every wait is bounded; a wait that runs out sets SMLA_DEVERR_TIMEOUT and
+// the CTA unwinds.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -115,7 +116,7 @@ struct __align__(16) ShardMeta {
 
 struct Ctl {
   uint64_t q_tma, q_ready, full[kStages], freed[kStages], raw_full[kRawStages], raw_empty[kRawStages],
-      s_full, s_free, pv_done, xa[2], xb[2], end, end_pv;
+      s_full, s_free, pv_done, p_full, xa[2], xb[2], end;
   uint32_t tbase;
   int n_list;
   int abort;
@@ -126,7 +127,6 @@ struct Ctl {
   const int32_t* bt_row[kMaxMerge];
   ShardMeta meta[kMaxMerge];
   int bt_staged;              // the rows fit the staging area
-  int sm_abort;               // 1 + the first tile in which a softmax warp gave up (0: none)
 };
 static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -780,7 +780,6 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
     const float scale_log2 = a.sm_scale * kLog2e;
     float m_ref = -INFINITY;  // log2-domain reference maximum
     float l = 0.f;
-    int pv_issued = 0;        // thread 0: PV MMAs issued so far
     // Key-column split of the softmax: CTA c finishes the scores of keys
     // [32c, 32c + 32) of each tile (its own partial plus the peer's, XA),
     // computes their P against a reference maximum, and sends that P, the
@@ -840,10 +839,10 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
       for (int j = 0; j < 32; ++j) sown[j] = C ? s[32 + j] : s[j];
       return true;
     };
-    // The four softmax warps leave the loop together: a warp whose wait gave
-    // up records it and arrives (without waiting) at the tile's barrier (at
-    // give_up below), which the others then complete and leave after; every
-    // exit lies before that barrier, so its count always completes.
+    // A warp whose wait gave up leaves the loop (at give_up below); the
+    // others' waits give up too, since every wait is an mbarrier wait that
+    // sees the CTA's abort flag.  The four warps enter the loop on one
+    // reduced decision and meet again only at the epilogue's barrier.
     bool ok = ntiles == 0 || start_tile(0);
     ok = !named_bar_or(5, 128, !ok);
     int i = 0;
@@ -982,51 +981,20 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
       }
       tmem_st_wait();
       tc_fence_before();
-      // P(i) of all 128 head rows is in TMEM: one softmax thread issues PV(i)
-      // at once (no other thread polls for it), and its completion releases
-      // the operand stage and lets the next P overwrite this one
-      named_bar_sync(5, 128);
-      if (h == 0) {
-        tc_fence_after();
-        issue_pv(tb, smem_u32(sm + kOffOp) + (i % kStages) * kOpTileBytes, i > 0);
-        mma_commit(&ctl->pv_done);
-        mma_commit(&ctl->freed[i % kStages]);
-        pv_issued = i + 1;
-      }
-      // read after PV(i) is on its way (off the path to it): a warp gave up
-      // in this tile or before (its rows of P may be missing; the call
-      // reports the timeout and its output is not used).  A give-up in a
-      // later tile, by a warp already past this barrier, is left to that
-      // tile's barrier, which every warp still in the loop passes.
-      {
-        const int first = *reinterpret_cast<volatile int*>(&ctl->sm_abort);
-        if (first != 0 && first <= i + 1) {
-          ok = false;
-          break;
-        }
-      }
+      // this thread's row of P(i) is in TMEM: once all 128 have arrived the
+      // MMA thread issues PV(i); its completion releases the operand stage
+      // and lets the next P overwrite this one
+      mbar_arrive(&ctl->p_full);
     }
     if (false) {
     give_up:
-      // this warp's wait gave up inside tile i: it records the first such
-      // tile (1 + its index) and arrives (without waiting) at the tile's
-      // barrier, which the other warps then complete and leave after
+      // this warp's wait gave up (the CTA's abort flag is up, so every
+      // other wait of the CTA gives up too)
       ok = false;
-      atomicCAS(&ctl->sm_abort, 0, i + 1);
-      __threadfence_block();
-      named_bar_arrive(5, 128);
     }
     // epilogue
     if (ok && ntiles > 0) {
       ok = __all_sync(0xffffffffu, wait_bar(&ctl->pv_done, (ntiles - 1) & 1, abort, kWsPvLast));
-      tc_fence_after();
-    }
-    // thread 0's PV MMAs have all completed before TMEM is read or released
-    // (waited on even after an abort, with its own bound)
-    if (h == 0 && pv_issued > 0) {
-      mma_commit(&ctl->end_pv);
-      int no_abort = 0;
-      wait_bar(&ctl->end_pv, 0, &no_abort, kWsDrain);
       tc_fence_after();
     }
     // one decision for all four softmax warps (the split epilogue below uses a
@@ -1079,20 +1047,36 @@ __device__ void run_cta(const DecodeArgs& a, uint8_t* sm, Ctl* ctl, const HalfRt
     // ------------------------------------------------ stage cache rows
     loader_loop<kMode>(a, ctl, sm, n, ntiles, C, tid - 32 * kLoaderWarp0, abort);
   } else if (lane == 0) {
-    // ------------------------------------------------ QK^T issue (one thread)
+    // ------------------------------------------------ MMA issue (one thread)
     // QK(i) needs its operand stage converted and S(i - 1) read by the
-    // softmax; the thread sleeps on each barrier until the hardware wakes it
-    // at the phase change.  (PV is issued by a softmax thread.)
+    // softmax, PV(i) the softmax's P(i); the thread sleeps on each barrier
+    // until the hardware wakes it at the phase change.  Issuing PV here
+    // rather than from a softmax thread keeps the MMA issue (~57 cycles an
+    // instruction) and a per-tile barrier of the four softmax warps off the
+    // softmax's chain.
     const uint32_t op0 = smem_u32(sm + kOffOp);
     bool ok = wait_bar(&ctl->q_ready, 0, abort, kWsQReady);
+    // QK(j), then PV(j - 2): the softmax stores P(j - 2) after it has read
+    // S(j - 1), which frees S for QK(j)
 #pragma unroll 1
-    for (int i = 0; i < ntiles && ok; ++i) {
-      ok = wait_bar(&ctl->full[i % kStages], (i / kStages) & 1, abort, kWsFull) &&
-           (i == 0 || wait_bar(&ctl->s_free, (i - 1) & 1, abort, kWsSFree));
-      if (!ok) break;
-      tc_fence_after();
-      issue_qk(tb, op0 + (i % kStages) * kOpTileBytes);
-      mma_commit(&ctl->s_full);
+    for (int j = 0; j < ntiles + 2 && ok; ++j) {
+      if (j < ntiles) {
+        ok = wait_bar(&ctl->full[j % kStages], (j / kStages) & 1, abort, kWsFull) &&
+             (j == 0 || wait_bar(&ctl->s_free, (j - 1) & 1, abort, kWsSFree));
+        if (!ok) break;
+        tc_fence_after();
+        issue_qk(tb, op0 + (j % kStages) * kOpTileBytes);
+        mma_commit(&ctl->s_full);
+      }
+      const int i = j - 2;
+      if (i >= 0) {
+        ok = wait_bar(&ctl->p_full, i & 1, abort, kWsPFull);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(tb, op0 + (i % kStages) * kOpTileBytes, i > 0);
+        mma_commit(&ctl->pv_done);
+        mma_commit(&ctl->freed[i % kStages]);
+      }
     }
     // drain: every MMA issued above has completed before TMEM is released
     // (waited on even after an abort, with its own bound).  A CTA whose row
@@ -1263,6 +1247,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&ctl->s_full, 1);
     mbar_init(&ctl->s_free, 128);
     mbar_init(&ctl->pv_done, 1);
+    mbar_init(&ctl->p_full, 128);  // one arrival per softmax thread
     for (int st = 0; st < kRawStages; ++st) {
       mbar_init(&ctl->raw_full[st], kLoaders);  // one arrival per loader
       mbar_init(&ctl->raw_empty[st], 4);        // one arrival per converter warp
@@ -1272,9 +1257,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->xb[b], 1);
     }
     mbar_init(&ctl->end, 1);
-    mbar_init(&ctl->end_pv, 1);
     ctl->abort = 0;
-    ctl->sm_abort = 0;
     fence_mbar_init_cluster();
     // q lands in the (still idle) operand stages while the CTA sets up
     issue_q_tma(a, t, hr.c, smem_u32(sm + kOffOp), &ctl->q_tma);
