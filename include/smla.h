@@ -194,7 +194,8 @@ size_t smla_decode_workspace_size(int32_t T, int32_t H, int32_t K);
  *               zero again); may be NULL when that size is 0.  Calls that
  *               run concurrently need distinct workspaces.
  * When the size is not 0 the rows are split over several key ranges
- * (split-K) and each range's partial goes through the workspace.  The
+ * (split-K) and each range's partial (its normalised output in fp16, its
+ * maximum and sum in fp32) goes through the workspace.  The
  * partials are merged by their LSE in the decode kernel (the last range of
  * a row to finish merges it) when the decode grid is larger than one wave
  * on the GPU or there are fewer than four ranges per row; otherwise by a

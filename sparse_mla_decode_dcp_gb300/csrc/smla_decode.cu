@@ -485,9 +485,12 @@ __device__ void split_epilogue(const DecodeArgs& a, Ctl* ctl, int C, int64_t t, 
   const int S = a.splits;
   const bool live = h < a.H;
   const int64_t row = (t * S + split) * a.H + (live ? h : 0);
-  float4* wo = reinterpret_cast<float4*>(a.ws_o + row * SMLA_V_DIM + C * 256);
+  // the split's own normalised output O / l, in fp16: an average of the
+  // fp16 value rows, so within their range, rounded once (2^-11 relative)
+  uint4* wo = reinterpret_cast<uint4*>(a.ws_o + row * SMLA_V_DIM + C * 256);
   const bool has = ok && ntiles > 0;
   if (has) {
+    const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
     for (int cc = 0; cc < 8; ++cc) {
       uint32_t r[32];
@@ -495,9 +498,14 @@ __device__ void split_epilogue(const DecodeArgs& a, Ctl* ctl, int C, int64_t t, 
       tmem_ld_wait();
       if (live) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          wo[cc * 8 + k] = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
-                                       __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+        for (int k = 0; k < 4; ++k) {
+          uint32_t w[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            w[q] = h2_bits(__floats2half2_rn(__uint_as_float(r[8 * k + 2 * q]) * inv,
+                                             __uint_as_float(r[8 * k + 2 * q + 1]) * inv));
+          wo[cc * 4 + k] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
       }
     }
   }
@@ -594,7 +602,7 @@ __device__ void combine_splits(const DecodeArgs& a, uint8_t* sm, int C, int64_t 
   }
   const int n_items = H * (SMLA_V_DIM / 2) / 4;  // float4 columns of the value half
   const int n_chunks = (S + kCombChunk - 1) / kCombChunk;
-  const float* o_row = a.ws_o + t * S * H * SMLA_V_DIM + C * 256;
+  const uint16_t* o_row = a.ws_o + t * S * H * SMLA_V_DIM + C * 256;
 #pragma unroll 1
   for (int pass = 0; pass < 2; ++pass) {
     const int it0 = pass * kCombItems * kThreads + tid;
@@ -634,23 +642,25 @@ __device__ void combine_splits(const DecodeArgs& a, uint8_t* sm, int C, int64_t 
           const int hh = idx - j * H;
           const float* p = ml_row + int64_t(s_list[j]) * 4 * H + hh;
           const float m1 = __ldcg(p), l1 = __ldcg(p + H);
-          s_w[idx] = (l1 != 0.f) ? ex2(m1 - s_m[hh]) * s_inv[hh] : 0.f;
+          s_w[idx] = (l1 != 0.f) ? l1 * ex2(m1 - s_m[hh]) * s_inv[hh] : 0.f;
         }
         __syncthreads();
       }
       const int n = *s_n;
 #pragma unroll 1
       for (int j = 0; j < n; ++j) {
-        const float* src = o_row + int64_t(s_list[j]) * H * SMLA_V_DIM;
+        const uint16_t* src = o_row + int64_t(s_list[j]) * H * SMLA_V_DIM;
         const float* wj = s_w + j * H;
 #pragma unroll
         for (int k = 0; k < kCombItems; ++k) {
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(src + off[k]));
+          const uint2 raw = __ldcg(reinterpret_cast<const uint2*>(src + off[k]));
+          const float2 v0 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+          const float2 v1 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
           const float w = wj[off[k] >> 9];
-          acc[k].x = fmaf(w, v.x, acc[k].x);
-          acc[k].y = fmaf(w, v.y, acc[k].y);
-          acc[k].z = fmaf(w, v.z, acc[k].z);
-          acc[k].w = fmaf(w, v.w, acc[k].w);
+          acc[k].x = fmaf(w, v0.x, acc[k].x);
+          acc[k].y = fmaf(w, v0.y, acc[k].y);
+          acc[k].z = fmaf(w, v1.x, acc[k].z);
+          acc[k].w = fmaf(w, v1.y, acc[k].w);
         }
       }
     }
@@ -1436,7 +1446,7 @@ __device__ __forceinline__ float max_nan(float x, float y) {
 }
 
 __global__ void __launch_bounds__(kCombHeads * 32)
-    split_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_ml,
+    split_combine_kernel(const uint16_t* __restrict__ ws_o, const float* __restrict__ ws_ml,
                          uint16_t* __restrict__ out, float* __restrict__ lse, int32_t H, int32_t S) {
   griddep_wait();  // the decode grid's partials are complete and visible
   const int warp = threadIdx.x >> 5;
@@ -1466,9 +1476,9 @@ __global__ void __launch_bounds__(kCombHeads * 32)
     for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
   }
   const float inv = (M == -INFINITY) ? 0.f : 1.f / L;
-  const float4* o_row =
-      reinterpret_cast<const float4*>(ws_o + (t * S * H + h) * SMLA_V_DIM + C * 256) + lane;
-  const int64_t o_stride = int64_t(H) * SMLA_V_DIM / 4;  // float4s from one split's row to the next
+  const uint2* o_row =
+      reinterpret_cast<const uint2*>(ws_o + (t * S * H + h) * SMLA_V_DIM + C * 256) + lane;
+  const int64_t o_stride = int64_t(H) * SMLA_V_DIM / 4;  // 4-value groups from one split's row to the next
   float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
   for (int base = 0; base < S; base += 32) {
     const int sp = base + lane;
@@ -1478,7 +1488,7 @@ __global__ void __launch_bounds__(kCombHeads * 32)
       l1 = __ldcg(ml + sp * ml_stride + H);
     }
     const bool held = l1 != 0.f;  // this split wrote its partial
-    const float w_lane = held ? ex2(m1 - M) * inv : 0.f;
+    const float w_lane = held ? l1 * ex2(m1 - M) * inv : 0.f;
     unsigned mask = __ballot_sync(0xffffffffu, held);
     while (mask) {
       int idx[8];
@@ -1492,9 +1502,14 @@ __global__ void __launch_bounds__(kCombHeads * 32)
       float4 v0[8], v1[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const float4* src = o_row + (base + (idx[k] < 0 ? idx[0] : idx[k])) * o_stride;
-        v0[k] = __ldcg(src);
-        v1[k] = __ldcg(src + 32);
+        const uint2* src = o_row + (base + (idx[k] < 0 ? idx[0] : idx[k])) * o_stride;
+        const uint2 r0 = __ldcg(src), r1 = __ldcg(src + 32);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&r0.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&r0.y));
+        const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&r1.x));
+        const float2 d = __half22float2(*reinterpret_cast<const __half2*>(&r1.y));
+        v0[k] = make_float4(a.x, a.y, b.x, b.y);
+        v1[k] = make_float4(c.x, c.y, d.x, d.y);
       }
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
@@ -1555,7 +1570,7 @@ WsLayout ws_layout(int32_t T, int32_t H, int32_t K) {
   if (S == 1 || T <= 0) return w;
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   w.o_off = 0;
-  w.ml_off = up(size_t(T) * S * H * SMLA_V_DIM * sizeof(float));
+  w.ml_off = up(size_t(T) * S * H * SMLA_V_DIM * sizeof(uint16_t));
   w.tick_off = w.ml_off + up(size_t(T) * S * 2 * 2 * H * sizeof(float));
   w.total = w.tick_off + up(size_t(T) * 2 * sizeof(int32_t));
   return w;
@@ -1641,7 +1656,7 @@ cudaError_t launch_impl(const DecodeArgs& args, cudaStream_t s) {
   a.splits = a.single_split ? 1 : decode_splits(a.T, a.K);
   const WsLayout w = a.splits > 1 ? ws_layout(a.T, a.H, a.K) : WsLayout{0, 0, 0, 0};
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-  a.ws_o = w.total ? reinterpret_cast<float*>(ws + w.o_off) : nullptr;
+  a.ws_o = w.total ? reinterpret_cast<uint16_t*>(ws + w.o_off) : nullptr;
   a.ws_ml = w.total ? reinterpret_cast<float*>(ws + w.ml_off) : nullptr;
   a.ws_tick = w.total ? reinterpret_cast<int32_t*>(ws + w.tick_off) : nullptr;
   int dev = 0;
@@ -1668,7 +1683,7 @@ cudaError_t launch_impl(const DecodeArgs& args, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, split_combine_kernel, static_cast<const float*>(a.ws_o),
+  return cudaLaunchKernelEx(&cfg, split_combine_kernel, static_cast<const uint16_t*>(a.ws_o),
                             static_cast<const float*>(a.ws_ml), a.out, a.lse, a.H, a.splits);
 }
 

@@ -62,7 +62,7 @@ struct DecodeArgs {
   size_t workspace_bytes;
   // filled by the launcher from the workspace (split-K partials)
   int32_t splits;
-  float* ws_o;       // [T, splits, H, 512] unnormalised partial O
+  uint16_t* ws_o;    // [T, splits, H, 512] fp16: each split's O / l (its own softmax average)
   float* ws_ml;      // [T, splits, 2 halves, 2, H]: log2-domain max, then sum
   int32_t* ws_tick;  // [T, 2] arrival counters, left at zero by every call
   int32_t combine_in_kernel;  // 1: the last split to arrive merges the row; 0: a second kernel

@@ -68,7 +68,7 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(cuda_device):
 @pytest.mark.gpu
 def test_noalloc_rejects_shapes_beyond_its_scratch(cuda_device):
     lib = capi.load()
-    T, H, K = 100, 128, 4096
+    T, H, K = 200, 128, 4096
     assert capi.decode_workspace_size(T, H, K) > capi.NOALLOC_SCRATCH_BYTES
     fake = 0x10000  # never dereferenced: the size check comes first
     st = lib.smla_sparse_mla_decode_noalloc(fake, fake, 10, fake, T, H, K, ctypes.c_float(0.07),
