@@ -177,8 +177,11 @@ def test_decode_head_counts(cuda_device, H):
     _decode_vs_oracle(q, pool, slots, 1 / math.sqrt(192), f"H={H}")
 
 
-@pytest.mark.parametrize("K", [1, 3, 37, 64, 129, 2048, 4096])
+@pytest.mark.parametrize("K", [1, 3, 37, 64, 100, 128, 129, 192, 2048, 4096])
 def test_decode_topk_sizes(cuda_device, K):
+    """Rows of 1 to 64 key tiles (one row with every other entry -1): the
+    MMA thread's QK^T(j) / PV(j - 2) order at its short-row edges (one, two
+    and three tiles) and with split-K over long rows."""
     dev = cuda_device
     n = max(K, 8) + 50
     pool = _small_pool(n, dev, seed=K)
