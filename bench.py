@@ -518,15 +518,19 @@ def _topk_path(wl, n, flush, stream, peaks, dev, workload):
     n_cand_np = np.array([int(wl.ctx[t // S]) - S + t % S + 1 for t in range(wl.T)], np.int32)
     n_cand = torch.from_numpy(n_cand_np).to(dev)
     ids = torch.empty((wl.T, wl.K), dtype=torch.int32, device=dev)
+    ws_bytes = capi.topk_select_workspace_size(wl.T, L, wl.K)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
 
     def run():
-        capi.load().smla_topk_select(scores.data_ptr(), scores.stride(0), L, n_cand.data_ptr(),
-                                     wl.T, wl.K, 1, 0, 1, ids.data_ptr(), None,
-                                     int(stream.cuda_stream))
+        st = capi.load().smla_topk_select(scores.data_ptr(), scores.stride(0), L,
+                                          n_cand.data_ptr(), wl.T, wl.K, 1, 0, 1, ids.data_ptr(),
+                                          None, ws.data_ptr(), ws_bytes, int(stream.cuda_stream))
+        assert st == capi.SMLA_OK, st
     run()
     ms = float(np.mean(_timed_steps(run, n, flush, stream)))
     nbytes = 4 * int(n_cand_np.sum()) + 4 * wl.T * wl.K
-    return {"ms_per_step": ms, "launches_per_step": 1,
+    # rows longer than a chunk: one launch over the chunks, one merging them
+    return {"ms_per_step": ms, "launches_per_step": 2 if ws_bytes else 1,
             "roofline": _hbm_roofline("smla_topk_select", ms, nbytes, peaks,
                                       "4 B per candidate score read + 4 B per id written",
                                       workload)}

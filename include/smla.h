@@ -394,6 +394,16 @@ smla_status smla_dcp_dense_mla_decode(
  *   n_cand      device int32 [T]
  *   out_ids     device int32 [T, K] output
  *   out_scores  device fp32 [T, K] output (the kept scores) or NULL
+ *   workspace   NULL, or device scratch of at least
+ *               smla_topk_select_workspace_size(T, L, K) bytes, 16-byte
+ *               aligned (no initial contents); calls that run concurrently
+ *               need distinct workspaces.  With it, a call of at most 32
+ *               rows whose L is at least 8 x max(16384, 8 x K rounded up to
+ *               a power of two) cuts each row into min(8, SMs / T) chunks,
+ *               one CTA each keeping the chunk's K best, and a second launch
+ *               selects the row's K best among those; without it (or when
+ *               the size is 0) one CTA walks each whole row.  The result is
+ *               the same either way.
  *
  * smla_dcp_topk_merge: row i's candidates are the entries j < M with
  * cand_ids[i*row_stride + j] >= 0 (global ids, unique per row) and their
@@ -402,13 +412,21 @@ smla_status smla_dcp_dense_mla_decode(
  *
  * Errors: INVALID_ARG for null pointers (T > 0), T < 0, L < 0, M < 0,
  * row_stride < L (or < M), D < 1, rank outside [0, D), interleave < 1,
- * misaligned buffers; UNSUPPORTED for K outside [1, SMLA_MAX_TOPK].
+ * misaligned buffers; UNSUPPORTED for K outside [1, SMLA_MAX_TOPK];
+ * WORKSPACE for a non-NULL workspace smaller than the size below or not
+ * 16-byte aligned.
+ *
+ * smla_topk_select_workspace_size: bytes of the optional workspace for
+ * (T, L, K), from the shape alone; 0 when no row can be long enough to be
+ * cut, or for invalid shapes.
  */
 #define SMLA_MAX_TOPK 16384
+size_t smla_topk_select_workspace_size(int32_t T, int32_t L, int32_t K);
 smla_status smla_topk_select(const float* scores, int64_t row_stride, int32_t L,
                              const int32_t* n_cand, int32_t T, int32_t K, int32_t D,
                              int32_t rank, int32_t interleave, int32_t* out_ids,
-                             float* out_scores, void* stream);
+                             float* out_scores, void* workspace, size_t workspace_bytes,
+                             void* stream);
 smla_status smla_dcp_topk_merge(const int32_t* cand_ids, const float* cand_scores,
                                 int64_t row_stride, int32_t M, int32_t T, int32_t K,
                                 int32_t* out_ids, float* out_scores, void* stream);

@@ -10,7 +10,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from typing import Optional, Sequence, Tuple
+from typing import Optional, Sequence, Tuple, Union
 
 import torch
 
@@ -63,9 +63,10 @@ SIGNATURES = {
     "smla_dcp_dense_mla_decode": (ctypes.c_int, [
         _c_vp, _c_i32, _c_i32, _c_i32, ctypes.c_float, _c_vp, _c_i32, _c_i32, _c_i32, _c_i32,
         _c_i32, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]),
+    "smla_topk_select_workspace_size": (_c_sz, [_c_i32, _c_i32, _c_i32]),
     "smla_topk_select": (ctypes.c_int, [
         _c_vp, _c_i64, _c_i32, _c_vp, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_vp, _c_vp,
-        _c_vp]),
+        _c_vp, _c_sz, _c_vp]),
     "smla_dcp_topk_merge": (ctypes.c_int, [
         _c_vp, _c_vp, _c_i64, _c_i32, _c_i32, _c_i32, _c_vp, _c_vp, _c_vp]),
     "smla_dcp_lse_merge": (ctypes.c_int, [
@@ -449,12 +450,21 @@ def dcp_dense_mla_decode(q: torch.Tensor, ctx_lens: torch.Tensor, max_ctx: int, 
 MAX_TOPK = 16384
 
 
+def topk_select_workspace_size(T: int, L: int, K: int) -> int:
+    """Bytes of the optional workspace topk_select uses to cut long rows
+    into chunks (0: no row of L candidates is cut)."""
+    return int(load().smla_topk_select_workspace_size(T, L, K))
+
+
 def topk_select(scores: torch.Tensor, n_cand: torch.Tensor, K: int, *, D: int = 1, rank: int = 0,
                 interleave: int = 1, with_scores: bool = False,
+                workspace: Union[torch.Tensor, None, bool] = True,
                 stream: Optional[torch.cuda.Stream] = None):
     """Top-K of each row's first n_cand local positions of `rank` (score
     descending, id ascending), as global ids, -1 padded.  scores is
-    [T, L] fp32 with contiguous rows."""
+    [T, L] fp32 with contiguous rows.  workspace: a uint8 device tensor of
+    at least topk_select_workspace_size(T, L, K) bytes, True (allocate one
+    here when that size is not 0) or None (one CTA walks each whole row)."""
     dev = scores.device
     if scores.dtype != torch.float32 or scores.dim() != 2 or scores.stride(1) != 1:
         raise ValueError("scores must be a 2-D fp32 tensor with contiguous rows")
@@ -462,9 +472,18 @@ def topk_select(scores: torch.Tensor, n_cand: torch.Tensor, K: int, *, D: int = 
     T, L = scores.shape
     ids = torch.empty((T, K), dtype=torch.int32, device=dev)
     sc = torch.empty((T, K), dtype=torch.float32, device=dev) if with_scores else None
+    if workspace is True:
+        need = topk_select_workspace_size(T, L, K) if 1 <= K <= MAX_TOPK else 0
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev) if need else None
+    elif workspace is False:
+        workspace = None
+    if workspace is not None:
+        _need(workspace, "workspace", torch.uint8, dev)
     st = load().smla_topk_select(scores.data_ptr(), scores.stride(0), L, n_cand.data_ptr(), T, K,
                                  D, rank, interleave, ids.data_ptr(),
                                  sc.data_ptr() if sc is not None else None,
+                                 workspace.data_ptr() if workspace is not None else None,
+                                 workspace.numel() if workspace is not None else 0,
                                  _stream_ptr(stream, dev))
     _check("smla_topk_select", st)
     return (ids, sc) if with_scores else ids

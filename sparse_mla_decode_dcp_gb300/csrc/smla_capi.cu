@@ -325,10 +325,16 @@ smla_status smla_dcp_dense_mla_decode(
   return from_cuda(smla::launch_decode_dense(a, static_cast<cudaStream_t>(stream)));
 }
 
+size_t smla_topk_select_workspace_size(int32_t T, int32_t L, int32_t K) {
+  if (T < 0 || L < 0 || K < 1 || K > SMLA_MAX_TOPK) return 0;
+  return smla::topk_workspace_bytes(T, L, K);
+}
+
 smla_status smla_topk_select(const float* scores, int64_t row_stride, int32_t L,
                              const int32_t* n_cand, int32_t T, int32_t K, int32_t D,
                              int32_t rank, int32_t interleave, int32_t* out_ids,
-                             float* out_scores, void* stream) {
+                             float* out_scores, void* workspace, size_t workspace_bytes,
+                             void* stream) {
   if (T < 0 || L < 0 || row_stride < L || D < 1 || rank < 0 || rank >= D || interleave < 1)
     return SMLA_ERR_INVALID_ARG;
   if (K < 1 || K > SMLA_MAX_TOPK) return SMLA_ERR_UNSUPPORTED;
@@ -337,6 +343,9 @@ smla_status smla_topk_select(const float* scores, int64_t row_stride, int32_t L,
   if (misaligned(scores, 4) || misaligned(n_cand, 4) || misaligned(out_ids, 4) ||
       (out_scores && misaligned(out_scores, 4)))
     return SMLA_ERR_INVALID_ARG;
+  const size_t need = smla::topk_workspace_bytes(T, L, K);
+  if (workspace != nullptr && (workspace_bytes < need || misaligned(workspace, 16)))
+    return SMLA_ERR_WORKSPACE;
   smla::TopkArgs a{};
   a.scores = scores;
   a.n_cand = n_cand;
@@ -349,7 +358,8 @@ smla_status smla_topk_select(const float* scores, int64_t row_stride, int32_t L,
   a.interleave = interleave;
   a.out_ids = out_ids;
   a.out_scores = out_scores;
-  return from_cuda(smla::launch_topk_select(a, static_cast<cudaStream_t>(stream)));
+  return from_cuda(smla::launch_topk_select(a, need > 0 ? workspace : nullptr,
+                                            static_cast<cudaStream_t>(stream)));
 }
 
 smla_status smla_dcp_topk_merge(const int32_t* cand_ids, const float* cand_scores,

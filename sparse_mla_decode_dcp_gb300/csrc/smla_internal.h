@@ -91,13 +91,21 @@ struct DecodeArgs {
 struct TopkArgs {
   const float* scores;      // [T, row_stride]: select: by local position; merge: candidates
   const int32_t* cand_ids;  // merge only: [T, row_stride] global ids, -1 = none
-  const int32_t* n_cand;    // select only: [T] candidates per row
+  const int32_t* n_cand;    // select: [T] candidates per row; merge: see `chunk`
   int64_t row_stride;
   int32_t L, M, T, K, kp;   // kp: the sort's size, a power of two >= K (set by the launcher)
   int32_t D, rank, interleave;
   FastDiv div_I;            // set by the launcher
   int32_t* out_ids;         // [T, K]
   float* out_scores;        // [T, K] or null
+  // Chunked selection (set by the launcher; 0 = one CTA per row).  Select:
+  // CTA (i, c) takes positions [c chunk, (c + 1) chunk) of row i and writes
+  // their K best, unsorted and -1 padded, to chunk_ids / chunk_scores
+  // [T, gridDim.y, K].  Merge of those: row i's entries are its first
+  // ceil(n_cand[i] / chunk) slabs of K (n_cand clipped to [0, L]).
+  int32_t chunk;
+  int32_t* chunk_ids;
+  float* chunk_scores;
 };
 
 struct MergeArgs {
@@ -119,7 +127,10 @@ constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 constexpr int32_t kDecodeMaxList = 2048;
 cudaError_t launch_decode_noalloc(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t s);
-cudaError_t launch_topk_select(const TopkArgs& a, cudaStream_t s);
+// workspace: null, or topk_workspace_bytes(T, L, K) bytes (16-byte aligned)
+// that long rows' chunked selection uses
+cudaError_t launch_topk_select(const TopkArgs& a, void* workspace, cudaStream_t s);
+size_t topk_workspace_bytes(int32_t T, int32_t L, int32_t K);
 cudaError_t launch_topk_merge(const TopkArgs& a, cudaStream_t s);
 size_t decode_workspace_bytes(int32_t T, int32_t H, int32_t K);
 

@@ -29,6 +29,7 @@
 // Only when the boundary bin overflows the per-warp lists (scores tied far
 // beyond K) does step 3 read the row from global memory again, digit by
 // digit.
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -90,7 +91,8 @@ __device__ __forceinline__ int32_t global_id(const TopkArgs& a, int j) {
 // Visit every candidate of row i, all lanes of a warp together: f(valid,
 // score, x) is called by every lane, x the candidate's id (merge: entry
 // j < M, skipped when its id is -1) or its local position j < n (select:
-// global_id(x) is its id, computed only where needed).  A thread keeps
+// global_id(x) is its id, computed only where needed; `base` is the first
+// position a chunk-mode CTA visits).  A thread keeps
 // kUnroll loads in flight: a gather's rate is set by the bytes in flight.
 // The loads are issued unconditionally (at a clamped index, the result then
 // masked): a branch around a load would make each wait for the one before.
@@ -98,26 +100,40 @@ __device__ __forceinline__ int32_t global_id(const TopkArgs& a, int j) {
 // and its up to 3 leading and 3 trailing scores, outside any aligned quad,
 // by warp 0 one per lane, so no load leaves the row whatever its alignment.
 template <bool kExplicit, bool kVec4, typename F>
-__device__ __forceinline__ void for_each_candidate(const TopkArgs& a, int64_t i, int span, F f) {
-  const float* srow = a.scores + i * a.row_stride;
+__device__ __forceinline__ void for_each_candidate(const TopkArgs& a, int64_t i, int base, int span,
+                                                   F f) {
+  const float* srow = a.scores + i * a.row_stride + base;
   if (kVec4) {
-    constexpr int kUnroll = 4;  // 16-byte loads in flight per thread
+    // 16-byte loads, kUnroll per thread a step; the next step's are issued
+    // before this step's scores are visited, so the loads overlap the work
+    constexpr int kUnroll = 2;
     const int head = min(span, int((4u - ((reinterpret_cast<uintptr_t>(srow) >> 2) & 3u)) & 3u));
     const int nq = (span - head) >> 2;  // whole aligned quads
     const int tail = span - head - 4 * nq;
     const float4* quads = reinterpret_cast<const float4*>(srow + head);
+    float4 next[kUnroll];
+    if (nq > 0) {
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        next[u] = __ldg(quads + min(int(threadIdx.x) + u * kThreads, nq - 1));
+    }
     for (int q0 = threadIdx.x; q0 - int(threadIdx.x) < nq; q0 += kThreads * kUnroll) {
       float4 v[kUnroll];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) v[u] = __ldg(quads + min(q0 + u * kThreads, nq - 1));
+      for (int u = 0; u < kUnroll; ++u) v[u] = next[u];
+      const int qn = q0 + kThreads * kUnroll;  // the next step (block-uniform test)
+      if (qn - int(threadIdx.x) < nq) {
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) next[u] = __ldg(quads + min(qn + u * kThreads, nq - 1));
+      }
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int q = q0 + u * kThreads;
         const int j = head + 4 * q;
-        f(q < nq, v[u].x, j);
-        f(q < nq, v[u].y, j + 1);
-        f(q < nq, v[u].z, j + 2);
-        f(q < nq, v[u].w, j + 3);
+        f(q < nq, v[u].x, base + j);
+        f(q < nq, v[u].y, base + j + 1);
+        f(q < nq, v[u].z, base + j + 2);
+        f(q < nq, v[u].w, base + j + 3);
       }
     }
     if (threadIdx.x < 32 && head + tail > 0) {
@@ -125,7 +141,7 @@ __device__ __forceinline__ void for_each_candidate(const TopkArgs& a, int64_t i,
       const bool ok = l < head + tail;
       const int j = l < head ? l : head + 4 * nq + (l - head);
       const float sc = ok ? __ldg(srow + j) : 0.f;
-      f(ok, sc, ok ? j : 0);
+      f(ok, sc, base + (ok ? j : 0));
     }
     return;
   }
@@ -146,7 +162,7 @@ __device__ __forceinline__ void for_each_candidate(const TopkArgs& a, int64_t i,
       if (kExplicit)
         f(j < span && id[u] >= 0, sc[u], id[u]);
       else
-        f(j < span, sc[u], j);
+        f(j < span, sc[u], base + j);
     }
   }
 }
@@ -386,17 +402,32 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
   __shared__ int wcount[kWarps];
   __shared__ int s_nsel, s_need, s_bin, s_done;
   __shared__ uint64_t s_prefix, s_mask;
-  const int64_t i = blockIdx.x;
+  const int64_t i = blockIdx.x;  // the row
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
-  const int n = kExplicit ? a.M : min(max(__ldg(a.n_cand + i), 0), a.L);
-  const int span = n;
   const int K = a.K;
+  // this CTA's candidates: positions [base, base + span) of the row (select)
+  // or its first `span` entries (merge)
+  int base = 0, span;
+  if (kExplicit) {
+    span = a.M;
+    if (a.chunk > 0) {  // the chunks' results: K entries per chunk the row has
+      const int nr = min(max(__ldg(a.n_cand + i), 0), a.L);
+      span = min(a.M, int((int64_t(nr) + a.chunk - 1) / a.chunk) * K);
+    }
+  } else {
+    span = min(max(__ldg(a.n_cand + i), 0), a.L);
+    if (a.chunk > 0) {
+      base = int(blockIdx.y) * a.chunk;
+      span = min(span - base, a.chunk);
+      if (span <= 0) return;  // past the row's end: the merge reads no slab of it
+    }
+  }
 
   // 1) histogram of the keys' top 12 bits
   for (int b = tid; b < kBins; b += kThreads) hist[b] = 0;
   __syncthreads();
-  for_each_candidate<kExplicit, kVec4>(a, i, span, [&](bool ok, float sc, int32_t) {
+  for_each_candidate<kExplicit, kVec4>(a, i, base, span, [&](bool ok, float sc, int32_t) {
     if (ok) atomicAdd(&hist[score_key(sc) >> (32 - kBinBits)], 1u);
   });
   __syncthreads();
@@ -458,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
   const bool take_all = bin <= 0;
   const float edge = key_score(max(uint32_t(max(bin, 0)) << (32 - kBinBits), score_key(-INFINITY)));
   int wc = 0;  // this warp's queued candidates (warp-uniform)
-  for_each_candidate<kExplicit, kVec4>(a, i, span, [&](bool ok, float sc, int32_t x) {
+  for_each_candidate<kExplicit, kVec4>(a, i, base, span, [&](bool ok, float sc, int32_t x) {
     const bool take = ok && (take_all || sc >= edge);
     const uint32_t m = __ballot_sync(0xffffffffu, take);
     if (m == 0) return;
@@ -495,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
     }
   } else {
     wc = 0;  // this warp's boundary keys
-    for_each_candidate<kExplicit, kVec4>(a, i, span, [&](bool ok, float sc, int32_t x) {
+    for_each_candidate<kExplicit, kVec4>(a, i, base, span, [&](bool ok, float sc, int32_t x) {
       const uint32_t sk = score_key(sc);
       const int kb = int(sk >> (32 - kBinBits));
       const bool take = ok && kb >= bin;
@@ -573,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
       if (in_smem) {
         for (int u = tid; u < nb; u += kThreads) count(bnd[u]);
       } else {
-        for_each_candidate<kExplicit, false>(a, i, span, [&](bool ok, float sc, int32_t x) {
+        for_each_candidate<kExplicit, false>(a, i, base, span, [&](bool ok, float sc, int32_t x) {
           const uint32_t sk = score_key(sc);
           if (ok && int(sk >> (32 - kBinBits)) == bin)
             count(make_key(sk, kExplicit ? x : global_id(a, x)));
@@ -603,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
         append(u < nb && (key & mask) >= prefix, key, sel, &s_nsel, a.kp);
       }
     } else {
-      for_each_candidate<kExplicit, false>(a, i, span, [&](bool ok, float sc, int32_t x) {
+      for_each_candidate<kExplicit, false>(a, i, base, span, [&](bool ok, float sc, int32_t x) {
         const uint32_t sk = score_key(sc);
         const bool inbin = ok && int(sk >> (32 - kBinBits)) == bin;
         const uint64_t key = make_key(sk, kExplicit ? x : (inbin ? global_id(a, x) : 0));
@@ -612,6 +643,16 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
     }
   }
   __syncthreads();
+  if (!kExplicit && a.chunk > 0) {
+    // chunk mode: the chunk's kept keys, unsorted, then -1 padding
+    const int64_t slab = (i * gridDim.y + blockIdx.y) * K;
+    for (int p = tid; p < K; p += kThreads) {
+      const uint64_t k = p < kept ? sel[p] : 0;
+      a.chunk_ids[slab + p] = p < kept ? int32_t(0xFFFFFFFFu - uint32_t(k)) : -1;
+      a.chunk_scores[slab + p] = p < kept ? key_score(uint32_t(k >> 32)) : 0.f;
+    }
+    return;
+  }
   for (int p = kept + tid; p < a.kp; p += kThreads) sel[p] = 0;  // below every candidate
   __syncthreads();
   // the histogram and cursors are free again: the merge sort's second buffer
@@ -658,10 +699,11 @@ cudaError_t ensure_smem_attribute() {
 }
 
 template <bool kExplicit, bool kVec4>
-cudaError_t launch(TopkArgs a, int cap, cudaStream_t s) {
+cudaError_t launch(TopkArgs a, int cap, cudaStream_t s, int chunks = 1) {
   cudaError_t e = ensure_smem_attribute<kExplicit, kVec4>();
   if (e != cudaSuccess) return e;
-  topk_kernel<kExplicit, kVec4><<<dim3(unsigned(a.T)), dim3(kThreads), kSmemBytes, s>>>(a, cap);
+  topk_kernel<kExplicit, kVec4>
+      <<<dim3(unsigned(a.T), unsigned(chunks)), dim3(kThreads), kSmemBytes, s>>>(a, cap);
   return cudaGetLastError();
 }
 
@@ -669,19 +711,94 @@ cudaError_t launch(TopkArgs a, int cap, cudaStream_t s) {
 // the boundary bin's regions.
 int boundary_cap(const TopkArgs& a) { return (kSmemBytes - 2 * kHistBytes) / 8 - a.kp; }
 
+// Few long rows leave most SMs idle with one CTA per row.  When there are at
+// most kChunkRows rows and L is at least kMaxChunks chunks of the smallest
+// size (kChunkMin candidates, and kChunkPerK times the sort size), each row
+// is cut into count = SMs / T chunks (2 to kMaxChunks): one CTA walks each
+// chunk and keeps its K best, and a second launch selects and sorts the
+// row's K best among those count K.  Each CTA costs about 10 us beyond its
+// per-candidate work (the scan, the radix select; the merge adds a sort), so
+// shorter rows, or more rows, are faster left whole.
+constexpr int kChunkMin = 16384;
+constexpr int kChunkPerK = 8;
+constexpr int kMaxChunks = 8;
+constexpr int kChunkRows = 32;
+
+bool chunkable(int32_t T, int32_t L, int32_t K) {
+  const int64_t smallest = std::max<int64_t>(kChunkMin, int64_t(kChunkPerK) * pow2_at_least(K));
+  return T >= 1 && T <= kChunkRows && int64_t(L) >= kMaxChunks * smallest;
+}
+
+// SMs of the current device, queried once per device.
+cudaError_t sm_count(int* sms) {
+  static std::atomic<int> cached[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool tracked = dev >= 0 && dev < kMaxDevices;
+  int v = tracked ? cached[dev].load(std::memory_order_relaxed) : 0;
+  if (v == 0) {
+    e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (tracked) cached[dev].store(v, std::memory_order_relaxed);
+  }
+  *sms = v;
+  return cudaSuccess;
+}
+
 }  // namespace
 
-cudaError_t launch_topk_select(const TopkArgs& args, cudaStream_t s) {
+size_t topk_workspace_bytes(int32_t T, int32_t L, int32_t K) {
+  if (!chunkable(T, L, K) || K <= 0) return 0;
+  return size_t(T) * kMaxChunks * size_t(K) * (sizeof(int32_t) + sizeof(float));
+}
+
+cudaError_t launch_topk_select(const TopkArgs& args, void* workspace, cudaStream_t s) {
   TopkArgs a = args;
   a.div_I = make_fastdiv(uint32_t(a.interleave));
   a.kp = pow2_at_least(a.K);
-  // 16-byte score loads over each row's aligned middle, whatever the stride
-  return launch<false, true>(a, boundary_cap(a), s);
+  a.chunk = 0;
+  int count = 1;
+  if (workspace != nullptr && chunkable(a.T, a.L, a.K)) {
+    int sms = 0;
+    const cudaError_t e = sm_count(&sms);
+    if (e != cudaSuccess) return e;
+    count = std::min(kMaxChunks, sms / a.T);
+  }
+  if (count < 2) {
+    // 16-byte score loads over each row's aligned middle, whatever the stride
+    return launch<false, true>(a, boundary_cap(a), s);
+  }
+  // whole quads a chunk: each chunk starts at the row's alignment
+  const int64_t chunk = ((int64_t(a.L) + count - 1) / count + 3) & ~int64_t(3);
+  const int64_t slabs = int64_t(a.T) * count * a.K;
+  a.chunk = int32_t(chunk);
+  a.chunk_scores = static_cast<float*>(workspace);
+  a.chunk_ids = reinterpret_cast<int32_t*>(a.chunk_scores + slabs);
+  cudaError_t e = launch<false, true>(a, boundary_cap(a), s, count);
+  if (e != cudaSuccess) return e;
+  TopkArgs m{};
+  m.scores = a.chunk_scores;
+  m.cand_ids = a.chunk_ids;
+  m.n_cand = a.n_cand;
+  m.row_stride = int64_t(count) * a.K;
+  m.L = a.L;
+  m.M = count * a.K;
+  m.T = a.T;
+  m.K = a.K;
+  m.kp = a.kp;
+  m.D = 1;
+  m.interleave = 1;
+  m.out_ids = a.out_ids;
+  m.out_scores = a.out_scores;
+  m.chunk = a.chunk;
+  return launch<true, false>(m, boundary_cap(m), s);
 }
 
 cudaError_t launch_topk_merge(const TopkArgs& args, cudaStream_t s) {
   TopkArgs a = args;
   a.kp = pow2_at_least(a.K);
+  a.chunk = 0;
   return launch<true, false>(a, boundary_cap(a), s);
 }
 

@@ -1017,16 +1017,44 @@ def test_dense_decode_context_out_of_range_is_flagged(cuda_device):
 
 # ------------------------------------------------------------ global top-k
 def _topk_vs_oracle(dev, scores64, n_cand, K, where):
+    """Both forms of the select: rows longer than a chunk cut into chunks
+    (with a workspace) and one CTA per whole row (without)."""
     s32 = np.asarray(scores64, dtype=np.float32)
-    got = capi.topk_select(torch.from_numpy(s32).to(dev),
-                           torch.from_numpy(np.asarray(n_cand, dtype=np.int32)).to(dev), K)
-    torch.cuda.synchronize()
     want = oracle.topk_select(s32.astype(np.float64), n_cand, K)
-    assert np.array_equal(got.cpu().numpy(), want), where
+    sc = torch.from_numpy(s32).to(dev)
+    nc = torch.from_numpy(np.asarray(n_cand, dtype=np.int32)).to(dev)
+    for ws in (True, None):
+        got = capi.topk_select(sc, nc, K, workspace=ws)
+        torch.cuda.synchronize()
+        assert np.array_equal(got.cpu().numpy(), want), (where, ws)
+
+
+def test_topk_select_chunk_edges(cuda_device):
+    """Few long rows cut into chunks (min(8, SMs / T) a row, of
+    ceil(L / count) rounded up to 4 candidates): rows ending just before, at
+    and just past a chunk's end, a row shorter than K and an empty one in a
+    chunked call, one row of 2^21 candidates with and without ties, and 32
+    rows (4 chunks each on a 152-SM GPU): the union of the chunks' K best
+    holds the row's K best."""
+    rng = np.random.default_rng(81)
+    T, L = 8, 8 * 16384 + 5
+    assert capi.topk_select_workspace_size(T, L, 2048) > 0
+    sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+    count = min(8, sms // T)
+    chunk = ((L + count - 1) // count + 3) // 4 * 4
+    scores = rng.standard_normal((T, L))
+    n_cand = [chunk - 1, chunk, chunk + 1, 2 * chunk, 2 * chunk + 1, L, 100, 0]
+    _topk_vs_oracle(cuda_device, scores, n_cand, 2048, "chunk edges")
+    big = rng.standard_normal((1, 1 << 21))
+    _topk_vs_oracle(cuda_device, big, [(1 << 21) - 3], 2048, "one long row")
+    _topk_vs_oracle(cuda_device, np.round(big, 1), [1 << 21], 4096, "one long row, ties")
+    many = rng.standard_normal((32, 131072))
+    _topk_vs_oracle(cuda_device, many, rng.integers(0, 131073, size=32), 2048, "32 rows")
 
 
 @pytest.mark.parametrize("L,K", [(97, 16), (3000, 1000), (5000, 2048), (131072, 2048),
-                                 (50000, 3001), (20000, 4096), (30000, 8192), (40000, 16384)])
+                                 (50000, 3001), (20000, 4096), (30000, 8192), (40000, 16384),
+                                 (300000, 16384)])
 def test_topk_select_matches_oracle(cuda_device, L, K):
     """Random rows up to 128k candidates, some shorter than K: bit-exact ids.
     K covers every sort the kernel picks by the padded size kp: the shared-
