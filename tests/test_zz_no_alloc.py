@@ -14,7 +14,8 @@ import numpy as np
 import pytest
 import torch
 
-from oracle.compare import LSE_ABS, OUT_MAX_ABS, OUT_REL_L2
+import oracle
+from oracle.compare import LSE_ABS, OUT_MAX_ABS, OUT_REL_L2, compare_out_lse
 from sparse_mla_decode_dcp_gb300 import capi, inputs
 
 
@@ -74,3 +75,60 @@ def test_noalloc_rejects_shapes_beyond_its_scratch(cuda_device):
     st = lib.smla_sparse_mla_decode_noalloc(fake, fake, 10, fake, T, H, K, ctypes.c_float(0.07),
                                             fake, fake, None)
     assert st == capi.SMLA_ERR_WORKSPACE
+
+
+@pytest.mark.gpu
+def test_noalloc_replays_in_cuda_graph(cuda_device):
+    """The case the entry point exists for: the call captured in a CUDA graph
+    (nothing allocated inside the capture; the reset of its scratch counters
+    becomes a memset node), replayed for two different top-k draws written
+    into the same input buffer: each replay bit-equal to the workspace entry
+    point on that draw and within the oracle's tolerance."""
+    dev = cuda_device
+    lib = capi.load()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(78)
+    n = 5000
+    pool = inputs.random_rows(n, gen, dev)
+    g = torch.Generator(device=dev).manual_seed(1078)
+    T, H, K = 3, 128, 2048  # few rows: split-K through the library's scratch
+    need = capi.decode_workspace_size(T, H, K)
+    assert 0 < need <= capi.NOALLOC_SCRATCH_BYTES
+    q = torch.randn((T, H, 576), generator=g, device=dev).to(torch.bfloat16)
+    rng = np.random.default_rng(78)
+    draws = [np.stack([rng.choice(n, K, replace=False) for _ in range(T)]).astype(np.int32)
+             for _ in range(2)]
+    draws[1][2, rng.choice(K, 1500, replace=False)] = -1
+    slots = torch.from_numpy(draws[0]).to(dev)
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    scale = 1.0 / math.sqrt(192.0)
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+
+    def call():
+        st = lib.smla_sparse_mla_decode_noalloc(
+            q.data_ptr(), pool.data_ptr(), n, slots.data_ptr(), T, H, K, ctypes.c_float(scale),
+            out.data_ptr(), lse.data_ptr(), ctypes.c_void_p(s.cuda_stream))
+        assert st == capi.SMLA_OK, capi.status_string(st)
+
+    with torch.cuda.stream(s):
+        call()  # warm-up: the scratch address and the kernel's attributes, outside the capture
+        s.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            call()
+    torch.cuda.synchronize()
+    q_bits = q.detach().cpu().contiguous().view(torch.int16).numpy().astype(np.uint16)
+    for d in draws:
+        slots.copy_(torch.from_numpy(d).to(dev))
+        out.fill_(7)
+        lse.fill_(7.0)
+        graph.replay()
+        torch.cuda.synchronize()
+        ref_out, ref_lse = capi.sparse_mla_decode(
+            q, pool, slots, scale, workspace=torch.zeros(need, dtype=torch.uint8, device=dev))
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
+        o, l = oracle.sparse_mla_decode(q_bits, pool.cpu().numpy(), d, scale)
+        compare_out_lse(out, lse, o, l, where="noalloc graph replay")
