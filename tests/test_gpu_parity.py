@@ -1045,6 +1045,17 @@ def test_topk_select_chunk_edges(cuda_device):
     scores = rng.standard_normal((T, L))
     n_cand = [chunk - 1, chunk, chunk + 1, 2 * chunk, 2 * chunk + 1, L, 100, 0]
     _topk_vs_oracle(cuda_device, scores, n_cand, 2048, "chunk edges")
+    # the kept scores come back through the chunks' slabs: each is its id's
+    # score, and the padding's is 0
+    s32 = scores.astype(np.float32)
+    ids, kept = capi.topk_select(torch.from_numpy(s32).to(cuda_device),
+                                 torch.tensor(n_cand, dtype=torch.int32, device=cuda_device),
+                                 2048, with_scores=True)
+    ids, kept = ids.cpu().numpy(), kept.cpu().numpy()
+    valid = ids >= 0
+    rows = np.broadcast_to(np.arange(T)[:, None], ids.shape)
+    assert np.array_equal(kept[valid], s32[rows[valid], ids[valid]])
+    assert np.all(kept[~valid] == 0)
     big = rng.standard_normal((1, 1 << 21))
     _topk_vs_oracle(cuda_device, big, [(1 << 21) - 3], 2048, "one long row")
     _topk_vs_oracle(cuda_device, np.round(big, 1), [1 << 21], 4096, "one long row, ties")
