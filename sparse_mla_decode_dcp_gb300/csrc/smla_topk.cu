@@ -28,7 +28,10 @@
 //      to 4096; larger K: the bitonic network throughout).
 // Only when the boundary bin overflows the per-warp lists (scores tied far
 // beyond K) does step 3 read the row from global memory again, digit by
-// digit.
+// digit.  A call of few long rows may instead cut each row into chunks, one
+// CTA each running steps 1-3 and writing its chunk's K best unsorted; a
+// second launch of the same kernel (its merge front end) then selects and
+// sorts each row's K best among its chunks' (the union holds them all).
 #include <algorithm>
 #include <atomic>
 #include <mutex>
