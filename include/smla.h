@@ -398,12 +398,14 @@ smla_status smla_dcp_dense_mla_decode(
  *               smla_topk_select_workspace_size(T, L, K) bytes, 16-byte
  *               aligned (no initial contents); calls that run concurrently
  *               need distinct workspaces.  With it, a call of at most 32
- *               rows whose L is at least 8 x max(16384, 8 x K rounded up to
- *               a power of two) cuts each row into min(8, SMs / T) chunks,
- *               one CTA each keeping the chunk's K best, and a second launch
- *               selects the row's K best among those; without it (or when
- *               the size is 0) one CTA walks each whole row.  The result is
- *               the same either way.
+ *               rows whose L is at least 16 x max(16384, 8 x K rounded up
+ *               to a power of two) cuts each row into min(8, SMs / T)
+ *               chunks, one CTA each keeping the chunk's K best, and a
+ *               second launch selects the row's K best among those; without
+ *               it (or when the size is 0) each row is walked whole, by two
+ *               CTAs (a cluster) when L >= 16384 and 2 T CTAs fit on the
+ *               GPU at once, else by one.  The result is the same either
+ *               way.
  *
  * smla_dcp_topk_merge: row i's candidates are the entries j < M with
  * cand_ids[i*row_stride + j] >= 0 (global ids, unique per row) and their

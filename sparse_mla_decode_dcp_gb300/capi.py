@@ -464,7 +464,7 @@ def topk_select(scores: torch.Tensor, n_cand: torch.Tensor, K: int, *, D: int = 
     descending, id ascending), as global ids, -1 padded.  scores is
     [T, L] fp32 with contiguous rows.  workspace: a uint8 device tensor of
     at least topk_select_workspace_size(T, L, K) bytes, True (allocate one
-    here when that size is not 0) or None (one CTA walks each whole row)."""
+    here when that size is not 0) or None (rows are never cut into chunks)."""
     dev = scores.device
     if scores.dtype != torch.float32 or scores.dim() != 2 or scores.stride(1) != 1:
         raise ValueError("scores must be a 2-D fp32 tensor with contiguous rows")

@@ -28,16 +28,20 @@
 //      to 4096; larger K: the bitonic network throughout).
 // Only when the boundary bin overflows the per-warp lists (scores tied far
 // beyond K) does step 3 read the row from global memory again, digit by
-// digit.  A call of few long rows may instead cut each row into chunks, one
-// CTA each running steps 1-3 and writing its chunk's K best unsorted; a
-// second launch of the same kernel (its merge front end) then selects and
-// sorts each row's K best among its chunks' (the union holds them all).
+// digit.  Long rows get a cluster of two CTAs, each walking half of the
+// row through steps 1 and 2, the second handing its queues to the first
+// through distributed shared memory.  A call of few long rows may instead
+// cut each row into chunks, one CTA each running steps 1-3 and writing its
+// chunk's K best unsorted; a second launch of the same kernel (its merge
+// front end) then selects and sorts each row's K best among its chunks'
+// (the union holds them all).
 #include <algorithm>
 #include <atomic>
 #include <mutex>
 
 #include "../../include/smla.h"
 #include "smla_internal.h"
+#include "smla_sm100.cuh"
 
 namespace smla {
 namespace {
@@ -49,6 +53,22 @@ constexpr int kBinShift = 64 - kBinBits;
 constexpr int kSmemBytes = 226 * 1024;  // one CTA per SM: all of it but the static part
 constexpr int kHistBytes = kBins * 4;
 constexpr int kWarps = kThreads / 32;
+
+// Distributed shared memory: a 16-byte load from, and 4- and 8-byte stores
+// into, the shared memory of another CTA of the cluster (shared::cluster
+// addresses from sm100::map_to_cta).
+__device__ __forceinline__ uint4 ld_dsmem_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_dsmem_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_dsmem_u64(uint32_t addr, uint64_t v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" :: "r"(addr), "l"(v) : "memory");
+}
 
 // Order-preserving image of a float: larger score, larger key; every NaN
 // maps to 0 (below -inf) and -0 to the key of +0.
@@ -393,25 +413,33 @@ __device__ void bitonic_sort_smem(uint64_t* sel, int kp) {
   }
 }
 
-template <bool kExplicit, bool kVec4>
+// kPair (select only): a cluster of two CTAs per row, each walking half of
+// it.  Each reads the other's histogram through distributed shared memory
+// and so finds the same boundary bin; CTA 1 queues its half's candidates at
+// or above it into CTA 0's shared memory (regions kWarps..2 kWarps - 1) and
+// leaves, and CTA 0 goes on alone over both halves' queues.  Both CTAs pass
+// both cluster barriers on every path: no return comes before the second.
+template <bool kExplicit, bool kVec4, bool kPair = false>
 __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem);                  // bin counts
   uint32_t* cur = hist + kBins;                                        // bin cursors
   uint64_t* sel = reinterpret_cast<uint64_t*>(smem + 2 * kHistBytes);  // kp keys
   uint64_t* bnd = sel + a.kp;  // boundary bin: one region of `reg` keys per warp
-  const int reg = cap / kWarps;
+  constexpr int kRegions = kPair ? 2 * kWarps : kWarps;  // boundary regions in CTA 0
+  const int reg = cap / kRegions;
   __shared__ uint32_t warp_sum[kWarps];
-  __shared__ int wcount[kWarps];
+  __shared__ int wcount[kRegions];
   __shared__ int s_nsel, s_need, s_bin, s_done;
   __shared__ uint64_t s_prefix, s_mask;
-  const int64_t i = blockIdx.x;  // the row
+  const int64_t i = kPair ? int64_t(blockIdx.x >> 1) : int64_t(blockIdx.x);  // the row
+  const uint32_t crank = kPair ? sm100::cluster_ctarank() : 0u;
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const int K = a.K;
   // this CTA's candidates: positions [base, base + span) of the row (select)
   // or its first `span` entries (merge)
-  int base = 0, span;
+  int first = 0, span, row_n = 0;
   if (kExplicit) {
     span = a.M;
     if (a.chunk > 0) {  // the chunks' results: K entries per chunk the row has
@@ -420,9 +448,15 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
     }
   } else {
     span = min(max(__ldg(a.n_cand + i), 0), a.L);
-    if (a.chunk > 0) {
-      base = int(blockIdx.y) * a.chunk;
-      span = min(span - base, a.chunk);
+    row_n = span;
+    if (kPair) {
+      // CTA 0 takes the first ceil(n / 8) quads, CTA 1 the rest (maybe none)
+      const int half = int(((int64_t(row_n) + 7) >> 3) << 2);
+      first = crank ? half : 0;
+      span = crank ? max(row_n - half, 0) : min(row_n, half);
+    } else if (a.chunk > 0) {
+      first = int(blockIdx.y) * a.chunk;
+      span = min(span - first, a.chunk);
       if (span <= 0) return;  // past the row's end: the merge reads no slab of it
     }
   }
@@ -430,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
   // 1) histogram of the keys' top 12 bits
   for (int b = tid; b < kBins; b += kThreads) hist[b] = 0;
   __syncthreads();
-  for_each_candidate<kExplicit, kVec4>(a, i, base, span, [&](bool ok, float sc, int32_t) {
+  for_each_candidate<kExplicit, kVec4>(a, i, first, span, [&](bool ok, float sc, int32_t) {
     if (ok) atomicAdd(&hist[score_key(sc) >> (32 - kBinBits)], 1u);
   });
   __syncthreads();
@@ -438,10 +472,17 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
   static_assert(kBins == 4 * kThreads, "four bins per thread");
   uint32_t own[4], own_sum = 0;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    own[q] = hist[4 * tid + q];
-    own_sum += own[q];
+  for (int q = 0; q < 4; ++q) own[q] = hist[4 * tid + q];
+  if (kPair) {
+    sm100::cluster_sync();  // #1: both halves counted
+    const uint4 o = ld_dsmem_v4(sm100::map_to_cta(sm100::smem_u32(hist + 4 * tid), crank ^ 1u));
+    own[0] += o.x;
+    own[1] += o.y;
+    own[2] += o.z;
+    own[3] += o.w;
   }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) own_sum += own[q];
   uint32_t suf = own_sum;  // inclusive suffix within the warp (lanes >= this one)
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -492,44 +533,74 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
   const bool take_all = bin <= 0;
   const float edge = key_score(max(uint32_t(max(bin, 0)) << (32 - kBinBits), score_key(-INFINITY)));
   int wc = 0;  // this warp's queued candidates (warp-uniform)
-  for_each_candidate<kExplicit, kVec4>(a, i, base, span, [&](bool ok, float sc, int32_t x) {
+  const bool remote = kPair && crank != 0;  // CTA 1 queues into CTA 0
+  const int rw = remote ? kWarps + warp : warp;  // this warp's region
+  const uint32_t region_addr = sm100::smem_u32(bnd + rw * reg);
+  const uint32_t region_cta0 = remote ? sm100::map_to_cta(region_addr, 0) : 0u;
+  for_each_candidate<kExplicit, kVec4>(a, i, first, span, [&](bool ok, float sc, int32_t x) {
     const bool take = ok && (take_all || sc >= edge);
     const uint32_t m = __ballot_sync(0xffffffffu, take);
     if (m == 0) return;
     if (take) {
       const int q = wc + __popc(m & lt);
-      if (q < reg) bnd[warp * reg + q] = (uint64_t(score_key(sc)) << 32) | uint32_t(x);
+      const uint64_t e = (uint64_t(score_key(sc)) << 32) | uint32_t(x);
+      if (q < reg) {
+        if (remote)
+          st_dsmem_u64(region_cta0 + 8u * uint32_t(q), e);
+        else
+          bnd[rw * reg + q] = e;
+      }
     }
     wc += __popc(m);
   });
-  if (lane == 0) wcount[warp] = wc;
+  if (lane == 0) {
+    if (remote)
+      st_dsmem_u32(sm100::map_to_cta(sm100::smem_u32(wcount + rw), 0), uint32_t(wc));
+    else
+      wcount[rw] = wc;
+  }
+  if (kPair) {
+    __syncwarp();
+    sm100::cluster_sync();  // #2: CTA 1's queues and counts are in CTA 0
+    if (crank != 0) return;  // CTA 1 is done; CTA 0 no longer reads its memory
+    first = 0;  // any later pass over the row covers all of it
+    span = row_n;
+  }
   __syncthreads();
   bool queued = true;
-  for (int w = 0; w < kWarps; ++w) queued &= wcount[w] <= reg;
+  for (int w = 0; w < kRegions; ++w) queued &= wcount[w] <= reg;
   __syncthreads();  // every warp has read the counts
   if (queued) {
-    // place this warp's queue; its boundary keys move to the front of the
-    // region (an entry is read before any write reaches its slot)
-    const int nq = wc;
-    wc = 0;  // now: this warp's boundary keys
-    uint64_t* region = bnd + warp * reg;
-    for (int q0 = 0; q0 < nq; q0 += 32) {
-      const int q = q0 + lane;
-      const uint64_t e = q < nq ? region[q] : 0;
-      const uint32_t sk = uint32_t(e >> 32);
-      const int32_t x = int32_t(uint32_t(e));
-      const int kb = int(sk >> (32 - kBinBits));
-      const bool hi = q < nq && kb > bin;
-      const bool bd = q < nq && kb == bin;
-      const uint64_t key = make_key(sk, kExplicit ? x : (q < nq ? global_id(a, x) : 0));
-      if (hi) sel[atomicAdd(&cur[kb], 1u)] = key;
-      const uint32_t m = __ballot_sync(0xffffffffu, bd);
-      if (bd) region[wc + __popc(m & lt)] = key;
-      wc += __popc(m);
+    // place the queues of this warp's regions (kPair: also CTA 1's warp's);
+    // their boundary keys move to the front of the region (an entry is read
+    // before any write reaches its slot)
+    for (int rr = warp; rr < kRegions; rr += kWarps) {
+      const int nq = wcount[rr];
+      int nbk = 0;  // the region's boundary keys
+      uint64_t* region = bnd + rr * reg;
+      for (int q0 = 0; q0 < nq; q0 += 32) {
+        const int q = q0 + lane;
+        const uint64_t e = q < nq ? region[q] : 0;
+        const uint32_t sk = uint32_t(e >> 32);
+        const int32_t x = int32_t(uint32_t(e));
+        const int kb = int(sk >> (32 - kBinBits));
+        const bool hi = q < nq && kb > bin;
+        const bool bd = q < nq && kb == bin;
+        const uint64_t key = make_key(sk, kExplicit ? x : (q < nq ? global_id(a, x) : 0));
+        if (hi) sel[atomicAdd(&cur[kb], 1u)] = key;
+        const uint32_t m = __ballot_sync(0xffffffffu, bd);
+        if (bd) region[nbk + __popc(m & lt)] = key;
+        nbk += __popc(m);
+      }
+      __syncwarp();
+      if (lane == 0) wcount[rr] = nbk;
     }
   } else {
+    // the queues are dropped: regions kWarps.. (kPair) stay empty
+    for (int rr = kWarps + warp; rr < kRegions; rr += kWarps)
+      if (lane == 0) wcount[rr] = 0;
     wc = 0;  // this warp's boundary keys
-    for_each_candidate<kExplicit, kVec4>(a, i, base, span, [&](bool ok, float sc, int32_t x) {
+    for_each_candidate<kExplicit, kVec4>(a, i, first, span, [&](bool ok, float sc, int32_t x) {
       const uint32_t sk = score_key(sc);
       const int kb = int(sk >> (32 - kBinBits));
       const bool take = ok && kb >= bin;
@@ -543,12 +614,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
       }
       wc += __popc(m);
     });
+    if (lane == 0) wcount[warp] = wc;
   }
-  if (lane == 0) wcount[warp] = wc;
   __syncthreads();
   bool overflow = false;
   int nb = 0;
-  for (int w = 0; w < kWarps; ++w) {
+  for (int w = 0; w < kRegions; ++w) {
     overflow |= wcount[w] > reg;
     nb += wcount[w];
   }
@@ -607,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
       if (in_smem) {
         for (int u = tid; u < nb; u += kThreads) count(bnd[u]);
       } else {
-        for_each_candidate<kExplicit, false>(a, i, base, span, [&](bool ok, float sc, int32_t x) {
+        for_each_candidate<kExplicit, false>(a, i, first, span, [&](bool ok, float sc, int32_t x) {
           const uint32_t sk = score_key(sc);
           if (ok && int(sk >> (32 - kBinBits)) == bin)
             count(make_key(sk, kExplicit ? x : global_id(a, x)));
@@ -637,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
         append(u < nb && (key & mask) >= prefix, key, sel, &s_nsel, a.kp);
       }
     } else {
-      for_each_candidate<kExplicit, false>(a, i, base, span, [&](bool ok, float sc, int32_t x) {
+      for_each_candidate<kExplicit, false>(a, i, first, span, [&](bool ok, float sc, int32_t x) {
         const uint32_t sk = score_key(sc);
         const bool inbin = ok && int(sk >> (32 - kBinBits)) == bin;
         const uint64_t key = make_key(sk, kExplicit ? x : (inbin ? global_id(a, x) : 0));
@@ -684,7 +755,7 @@ int pow2_at_least(int x) {
 
 // The kernel's shared-memory opt-in, set once per device and kernel form.
 constexpr int kMaxDevices = 64;
-template <bool kExplicit, bool kVec4>
+template <bool kExplicit, bool kVec4, bool kPair>
 cudaError_t ensure_smem_attribute() {
   static std::atomic<bool> done[kMaxDevices];
   static std::mutex m;
@@ -695,7 +766,7 @@ cudaError_t ensure_smem_attribute() {
   if (tracked && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
   std::lock_guard<std::mutex> lock(m);
   if (tracked && done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
-  e = cudaFuncSetAttribute(topk_kernel<kExplicit, kVec4>,
+  e = cudaFuncSetAttribute(topk_kernel<kExplicit, kVec4, kPair>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e == cudaSuccess && tracked) done[dev].store(true, std::memory_order_release);
   return e;
@@ -703,33 +774,56 @@ cudaError_t ensure_smem_attribute() {
 
 template <bool kExplicit, bool kVec4>
 cudaError_t launch(TopkArgs a, int cap, cudaStream_t s, int chunks = 1) {
-  cudaError_t e = ensure_smem_attribute<kExplicit, kVec4>();
+  cudaError_t e = ensure_smem_attribute<kExplicit, kVec4, false>();
   if (e != cudaSuccess) return e;
   topk_kernel<kExplicit, kVec4>
       <<<dim3(unsigned(a.T), unsigned(chunks)), dim3(kThreads), kSmemBytes, s>>>(a, cap);
   return cudaGetLastError();
 }
 
+// The select with a cluster of two CTAs per row.
+cudaError_t launch_pair(TopkArgs a, int cap, cudaStream_t s) {
+  cudaError_t e = ensure_smem_attribute<false, true, true>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2u * unsigned(a.T));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, topk_kernel<false, true, true>, a, cap);
+}
+
 // Shared memory: the histogram and the bin cursors, the selection (kp keys),
-// the boundary bin's regions.
+// the boundary bin's regions (kPair: twice as many, half the size).
 int boundary_cap(const TopkArgs& a) { return (kSmemBytes - 2 * kHistBytes) / 8 - a.kp; }
 
-// Few long rows leave most SMs idle with one CTA per row.  When there are at
-// most kChunkRows rows and L is at least kMaxChunks chunks of the smallest
-// size (kChunkMin candidates, and kChunkPerK times the sort size), each row
-// is cut into count = SMs / T chunks (2 to kMaxChunks): one CTA walks each
-// chunk and keeps its K best, and a second launch selects and sorts the
-// row's K best among those count K.  Each CTA costs about 10 us beyond its
-// per-candidate work (the scan, the radix select; the merge adds a sort), so
-// shorter rows, or more rows, are faster left whole.
+// Few long rows leave most SMs idle with one CTA (or one pair) per row.
+// When there are at most kChunkRows rows and L is at least 2 kMaxChunks
+// chunks of the smallest size (kChunkMin candidates, and kChunkPerK times
+// the sort size), each row is cut into count = SMs / T chunks (2 to
+// kMaxChunks): one CTA walks each chunk and keeps its K best, and a second
+// launch selects and sorts the row's K best among those count K.  Each CTA
+// costs about 10 us beyond its per-candidate work (the scan, the radix
+// select; the merge adds a sort), so shorter rows, or more rows, are faster
+// walked by a pair of CTAs each.
 constexpr int kChunkMin = 16384;
 constexpr int kChunkPerK = 8;
 constexpr int kMaxChunks = 8;
 constexpr int kChunkRows = 32;
+// Rows of at least kPairMin candidates get two CTAs each (a cluster) when
+// 2 T CTAs fit on the GPU at once.
+constexpr int kPairMin = 16384;
 
 bool chunkable(int32_t T, int32_t L, int32_t K) {
   const int64_t smallest = std::max<int64_t>(kChunkMin, int64_t(kChunkPerK) * pow2_at_least(K));
-  return T >= 1 && T <= kChunkRows && int64_t(L) >= kMaxChunks * smallest;
+  return T >= 1 && T <= kChunkRows && int64_t(L) >= 2 * kMaxChunks * smallest;
 }
 
 // SMs of the current device, queried once per device.
@@ -770,6 +864,12 @@ cudaError_t launch_topk_select(const TopkArgs& args, void* workspace, cudaStream
   }
   if (count < 2) {
     // 16-byte score loads over each row's aligned middle, whatever the stride
+    if (a.L >= kPairMin) {
+      int sms = 0;
+      const cudaError_t e = sm_count(&sms);
+      if (e != cudaSuccess) return e;
+      if (2 * int64_t(a.T) <= sms) return launch_pair(a, boundary_cap(a), s);
+    }
     return launch<false, true>(a, boundary_cap(a), s);
   }
   // whole quads a chunk: each chunk starts at the row's alignment

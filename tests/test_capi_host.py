@@ -349,9 +349,9 @@ def _topk_merge(lib, **kw):
     (dict(out=None), capi.SMLA_ERR_INVALID_ARG),
     (dict(out=FAKE + 2), capi.SMLA_ERR_INVALID_ARG),
     (dict(T=0, scores=None, n=None, out=None), capi.SMLA_OK),
-    # 200000 candidates, K = 16: up to 8 chunks a row, 2 x 8 x 16 x 8 = 2048 bytes
-    (dict(L=200000, stride=200000, ws=FAKE, ws_bytes=2047), capi.SMLA_ERR_WORKSPACE),
-    (dict(L=200000, stride=200000, ws=FAKE + 8, ws_bytes=4096), capi.SMLA_ERR_WORKSPACE),
+    # 300000 candidates, K = 16: up to 8 chunks a row, 2 x 8 x 16 x 8 = 2048 bytes
+    (dict(L=300000, stride=300000, ws=FAKE, ws_bytes=2047), capi.SMLA_ERR_WORKSPACE),
+    (dict(L=300000, stride=300000, ws=FAKE + 8, ws_bytes=4096), capi.SMLA_ERR_WORKSPACE),
     (dict(ws=FAKE + 8, ws_bytes=4096), capi.SMLA_ERR_WORKSPACE),
 ])
 def test_topk_select_argument_checks(lib, kw, status):
@@ -359,16 +359,16 @@ def test_topk_select_argument_checks(lib, kw, status):
 
 
 def test_topk_select_workspace_size_is_a_function_of_the_shape(lib):
-    # rows are cut only for T <= 32 and L >= 8 x max(16384, 8 x the sort
+    # rows are cut only for T <= 32 and L >= 16 x max(16384, 8 x the sort
     # size); the workspace then holds 8 chunks' K ids and scores a row
-    assert capi.topk_select_workspace_size(8, 131071, 2048) == 0
-    assert capi.topk_select_workspace_size(8, 131072, 2048) == 8 * 8 * 2048 * 8
+    assert capi.topk_select_workspace_size(8, 262143, 2048) == 0
+    assert capi.topk_select_workspace_size(8, 262144, 2048) == 8 * 8 * 2048 * 8
     assert capi.topk_select_workspace_size(32, 1 << 20, 2048) == 32 * 8 * 2048 * 8
     assert capi.topk_select_workspace_size(33, 1 << 20, 2048) == 0  # many rows: whole
     assert capi.topk_select_workspace_size(64, 65536, 2048) == 0
-    assert capi.topk_select_workspace_size(3, 200000, 16) == 3 * 8 * 16 * 8
-    assert capi.topk_select_workspace_size(2, 4096 * 256 - 1, 9000) == 0  # sort size 16384
-    assert capi.topk_select_workspace_size(2, 4096 * 256, 9000) == 2 * 8 * 9000 * 8
+    assert capi.topk_select_workspace_size(3, 300000, 16) == 3 * 8 * 16 * 8
+    assert capi.topk_select_workspace_size(2, (1 << 21) - 1, 9000) == 0  # sort size 16384
+    assert capi.topk_select_workspace_size(2, 1 << 21, 9000) == 2 * 8 * 9000 * 8
     assert capi.topk_select_workspace_size(0, 200000, 16) == 0
     assert capi.topk_select_workspace_size(2, 200000, 0) == 0
     assert capi.topk_select_workspace_size(2, 200000, 16385) == 0

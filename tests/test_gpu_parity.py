@@ -1037,7 +1037,7 @@ def test_topk_select_chunk_edges(cuda_device):
     rows (4 chunks each on a 152-SM GPU): the union of the chunks' K best
     holds the row's K best."""
     rng = np.random.default_rng(81)
-    T, L = 8, 8 * 16384 + 5
+    T, L = 8, 16 * 16384 + 5
     assert capi.topk_select_workspace_size(T, L, 2048) > 0
     sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
     count = min(8, sms // T)
@@ -1059,8 +1059,8 @@ def test_topk_select_chunk_edges(cuda_device):
     big = rng.standard_normal((1, 1 << 21))
     _topk_vs_oracle(cuda_device, big, [(1 << 21) - 3], 2048, "one long row")
     _topk_vs_oracle(cuda_device, np.round(big, 1), [1 << 21], 4096, "one long row, ties")
-    many = rng.standard_normal((32, 131072))
-    _topk_vs_oracle(cuda_device, many, rng.integers(0, 131073, size=32), 2048, "32 rows")
+    many = rng.standard_normal((32, 262144))
+    _topk_vs_oracle(cuda_device, many, rng.integers(0, 262145, size=32), 2048, "32 rows")
 
 
 @pytest.mark.parametrize("L,K", [(97, 16), (3000, 1000), (5000, 2048), (131072, 2048),
@@ -1077,6 +1077,27 @@ def test_topk_select_matches_oracle(cuda_device, L, K):
     n_cand = rng.integers(0, L + 1, size=T)
     n_cand[0], n_cand[1] = L, min(L, K // 2)  # full row, and fewer than K candidates
     _topk_vs_oracle(cuda_device, scores, n_cand, K, f"L={L} K={K}")
+
+
+def test_topk_select_pair_and_many_rows(cuda_device):
+    """Rows of 16384 or more positions take a cluster of two CTAs each
+    while two CTAs a row fit on the GPU, the first walking ceil(n / 8) quads
+    and the second the rest: rows whose second half is empty or short, NaN,
+    signed zeros and infinities among the scores; then 100 such rows, more
+    than half the SM count, which take one CTA each."""
+    rng = np.random.default_rng(91)
+    L = 20000
+    scores = rng.standard_normal((12, L))
+    scores[:, 1] = np.nan
+    scores[:, 2] = -0.0
+    scores[:, 6] = np.inf
+    scores[:, 9] = -np.inf
+    scores[5, :4000] = 0.0
+    n_cand = [0, 1, 3, 4, 5, 7, 8, 9, 16383, 16384, L, 9999]
+    for K in (4, 2048):
+        _topk_vs_oracle(cuda_device, scores, n_cand, K, f"pairs K={K}")
+    many = rng.standard_normal((100, L))
+    _topk_vs_oracle(cuda_device, many, rng.integers(0, L + 1, size=100), 2048, "100 rows")
 
 
 @pytest.mark.parametrize("decimals", [0, 1])
