@@ -430,6 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
   const int reg = cap / kRegions;
   __shared__ uint32_t warp_sum[kWarps];
   __shared__ int wcount[kRegions];
+  __shared__ int wend[kRegions];  // boundary keys in regions 0..r (inclusive prefix)
   __shared__ int s_nsel, s_need, s_bin, s_done;
   __shared__ uint64_t s_prefix, s_mask;
   const int64_t i = kPair ? int64_t(blockIdx.x >> 1) : int64_t(blockIdx.x);  // the row
@@ -640,14 +641,41 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
     const bool in_smem = !overflow;
     if (in_smem) {
       // compact the regions in place, 1024 keys at a time: a key's place in
-      // the list is never past its slot, and keys are read before written
+      // the list is never past its slot, and keys are read before written;
+      // a key's region is found by a binary search of the regions' prefix
+      // sums (warp 0 scans them: lane l holds regions kPer l .. kPer l + kPer - 1)
+      if (warp == 0) {
+        constexpr int kPer = kRegions / 32;
+        int own = 0;
+#pragma unroll
+        for (int r = 0; r < kPer; ++r) own += wcount[kPer * lane + r];
+        int inc = own;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, inc, off);
+          if (lane >= off) inc += y;
+        }
+        int acc = inc - own;
+#pragma unroll
+        for (int r = 0; r < kPer; ++r) {
+          acc += wcount[kPer * lane + r];
+          wend[kPer * lane + r] = acc;
+        }
+      }
+      __syncthreads();
       for (int c0 = 0; c0 < nb; c0 += kThreads) {
         const int u = c0 + tid;
         uint64_t x = 0;
         if (u < nb) {
-          int w = 0, base = 0;
-          while (base + wcount[w] <= u) base += wcount[w++];
-          x = bnd[w * reg + (u - base)];
+          int lo = 0, hi = kRegions - 1;  // the first region whose prefix passes u
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (wend[mid] > u)
+              hi = mid;
+            else
+              lo = mid + 1;
+          }
+          x = bnd[lo * reg + (u - (wend[lo] - wcount[lo]))];
         }
         __syncthreads();
         if (u < nb) bnd[u] = x;
