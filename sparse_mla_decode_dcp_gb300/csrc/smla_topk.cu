@@ -431,7 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
   __shared__ uint32_t warp_sum[kWarps];
   __shared__ int wcount[kRegions];
   __shared__ int wend[kRegions];  // boundary keys in regions 0..r (inclusive prefix)
-  __shared__ int s_nsel, s_need, s_bin, s_done;
+  __shared__ int s_nsel, s_need, s_bin, s_done, s_flag, s_nb;
+  __shared__ uint32_t warp_above[kWarps], s_total;  // keys in the warps above; all keys
   __shared__ uint64_t s_prefix, s_mask;
   const int64_t i = kPair ? int64_t(blockIdx.x >> 1) : int64_t(blockIdx.x);  // the row
   const uint32_t crank = kPair ? sm100::cluster_ctarank() : 0u;
@@ -492,12 +493,19 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
   }
   if (lane == 0) warp_sum[warp] = suf;  // the warp's total
   __syncthreads();
-  uint32_t higher = 0, total = 0;  // keys in warps above this one; all keys
-  for (int w = 0; w < kWarps; ++w) {
-    const uint32_t x = warp_sum[w];
-    total += x;
-    if (w > warp) higher += x;
+  if (warp == 0) {  // lane l: the keys of warps above warp l
+    const uint32_t x = warp_sum[lane];
+    uint32_t above = x;  // inclusive suffix over lanes >= l
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t y = __shfl_down_sync(0xffffffffu, above, off);
+      if (lane + off < 32) above += y;
+    }
+    warp_above[lane] = above - x;
+    if (lane == 0) s_total = above;
   }
+  __syncthreads();
+  const uint32_t higher = warp_above[warp], total = s_total;
   const bool select = total > uint32_t(K);
   {
     // keys strictly above each of this thread's bins: each bin's first place
@@ -568,9 +576,16 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
     span = row_n;
   }
   __syncthreads();
-  bool queued = true;
-  for (int w = 0; w < kRegions; ++w) queued &= wcount[w] <= reg;
-  __syncthreads();  // every warp has read the counts
+  constexpr int kPer = kRegions / 32;  // regions a lane of warp 0 reads
+  if (warp == 0) {
+    bool fit = true;
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) fit &= wcount[kPer * lane + r] <= reg;
+    fit = __all_sync(0xffffffffu, fit);
+    if (lane == 0) s_flag = fit;
+  }
+  __syncthreads();  // warp 0 has read the counts
+  const bool queued = s_flag != 0;
   if (queued) {
     // place the queues of this warp's regions (kPair: also CTA 1's warp's);
     // their boundary keys move to the front of the region (an entry is read
@@ -618,12 +633,26 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
     if (lane == 0) wcount[warp] = wc;
   }
   __syncthreads();
-  bool overflow = false;
-  int nb = 0;
-  for (int w = 0; w < kRegions; ++w) {
-    overflow |= wcount[w] > reg;
-    nb += wcount[w];
+  if (warp == 0) {
+    bool of = false;
+    int sum = 0;
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+      const int c = wcount[kPer * lane + r];
+      of |= c > reg;
+      sum += c;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    of = __any_sync(0xffffffffu, of);
+    if (lane == 0) {
+      s_flag = of;
+      s_nb = sum;
+    }
   }
+  __syncthreads();
+  const bool overflow = s_flag != 0;
+  const int nb = s_nb;
   const int kept = min(int(total), K);
   int32_t* out_ids = a.out_ids + i * K;
   float* out_scores = a.out_scores ? a.out_scores + i * K : nullptr;
@@ -645,7 +674,6 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkArgs a, int cap) 
       // a key's region is found by a binary search of the regions' prefix
       // sums (warp 0 scans them: lane l holds regions kPer l .. kPer l + kPer - 1)
       if (warp == 0) {
-        constexpr int kPer = kRegions / 32;
         int own = 0;
 #pragma unroll
         for (int r = 0; r < kPer; ++r) own += wcount[kPer * lane + r];
